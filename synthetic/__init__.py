@@ -1,0 +1,132 @@
+"""Seeded synthetic inputs for the exact-attention forward pass.
+
+This module is shared by the CPU oracle, the GPU parity tests and the benchmark.
+It draws and rounds inputs only; it holds none of the attention arithmetic.
+
+Workloads (shapes, dtypes, distributions) are the five attention-forward cases
+the FlashAttention pages motivate: a tiny exact check, a short-sequence batch,
+two causal long-context cases and an FP8 case with outliers (FlashAttention-3
+page, section "Low precision (FP8) and reducing quantisation error").
+
+Recipe (all on the CPU, one ``torch.Generator`` per case):
+  * seed = 1000 + case number (C1 -> 1001 ... C5 -> 1005);
+  * q, k, v drawn in that order as float32 ``randn`` of shape [B, N, H, d];
+  * bf16 / fp16 cases: each tensor rounded to the storage type (round to
+    nearest even, torch's cast);
+  * e4m3 case: after each ``randn`` draw, a ``rand`` draw of the same shape
+    marks outliers (u < 0.001) whose value is multiplied by 10; then one fp32
+    scale per (batch, head) s = amax|x[b, :, h, :]| / 448 and the stored code is
+    clamp(x / s, -448, 448) cast to float8_e4m3fn (round to nearest even).
+    The kernel receives the codes and the dequantisation scales ("descales").
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+E4M3_MAX = 448.0
+OUTLIER_RATE = 1e-3
+OUTLIER_GAIN = 10.0
+
+
+@dataclasses.dataclass(frozen=True)
+class Case:
+    name: str
+    B: int
+    H: int
+    N_q: int
+    N_k: int
+    d: int
+    causal: bool
+    dtype: str  # "bf16" | "fp16" | "e4m3"
+    seed: int
+    outliers: bool = False
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def flops(self) -> float:
+        """Counted FLOPs: 4*B*H*N_q*N_k*d, halved for causal."""
+        f = 4.0 * self.B * self.H * self.N_q * self.N_k * self.d
+        return f / 2.0 if self.causal else f
+
+
+CASES = {
+    "C1": Case("C1", 1, 1, 128, 128, 64, False, "bf16", 1001),
+    "C2": Case("C2", 4, 16, 1024, 1024, 64, False, "bf16", 1002),
+    "C3": Case("C3", 2, 16, 4096, 4096, 128, True, "bf16", 1003),
+    "C4": Case("C4", 1, 16, 16384, 16384, 128, True, "bf16", 1004),
+    "C5": Case("C5", 2, 16, 8192, 8192, 128, False, "e4m3", 1005, outliers=True),
+}
+
+
+def custom_case(B, H, N_q, N_k, d, causal, dtype="bf16", seed=7, outliers=None, name="custom"):
+    if outliers is None:
+        outliers = dtype == "e4m3"
+    return Case(name, B, H, N_q, N_k, d, bool(causal), dtype, seed, outliers)
+
+
+def _draw(g: torch.Generator, shape, outliers: bool) -> torch.Tensor:
+    x = torch.randn(shape, generator=g, dtype=torch.float32)
+    if outliers:
+        u = torch.rand(shape, generator=g, dtype=torch.float32)
+        x = torch.where(u < OUTLIER_RATE, x * OUTLIER_GAIN, x)
+    return x
+
+
+def quantize_e4m3_per_head(x: torch.Tensor):
+    """Per-(batch, head) e4m3 codes of x [B, N, H, d] and their fp32 descales [B, H]."""
+    amax = x.abs().amax(dim=(1, 3)).to(torch.float32)            # [B, H]
+    amax = torch.where(amax > 0, amax, torch.ones_like(amax))
+    descale = (amax / E4M3_MAX).to(torch.float32)
+    y = x / descale[:, None, :, None]
+    codes = y.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    return codes, descale.contiguous()
+
+
+def make_inputs(case: Case) -> dict:
+    """Inputs of one case as CPU tensors in [B, N, H, d] layout.
+
+    Returns a dict with q, k, v (bf16 / fp16 / float8_e4m3fn) and, for e4m3,
+    q_descale, k_descale, v_descale (float32 [B, H]); plus ``scale``.
+    """
+    g = torch.Generator().manual_seed(case.seed)
+    out = {"scale": case.scale}
+    shapes = {"q": (case.B, case.N_q, case.H, case.d),
+              "k": (case.B, case.N_k, case.H, case.d),
+              "v": (case.B, case.N_k, case.H, case.d)}
+    for name in ("q", "k", "v"):
+        x = _draw(g, shapes[name], case.outliers)
+        if case.dtype == "bf16":
+            out[name] = x.to(torch.bfloat16)
+        elif case.dtype == "fp16":
+            out[name] = x.to(torch.float16)
+        elif case.dtype == "e4m3":
+            codes, ds = quantize_e4m3_per_head(x)
+            out[name] = codes
+            out[name + "_descale"] = ds
+        else:
+            raise ValueError(f"unknown dtype {case.dtype}")
+    return out
+
+
+def sample_rows(case: Case, n: int = 256, seed: int | None = None) -> np.ndarray:
+    """Seeded (b, h, i) query-row triples, int64 [n, 3].
+
+    Always contains rows 0, 1, 127, 128, 129 and N_q-1 (tile edges and the
+    causal start) when they exist; the rest are uniform draws.
+    """
+    rng = np.random.default_rng(case.seed + 77 if seed is None else seed)
+    edges = [i for i in (0, 1, 127, 128, 129, case.N_q - 1) if 0 <= i < case.N_q]
+    rows = []
+    for j, i in enumerate(edges):
+        rows.append((j % case.B, (j * 7) % case.H, i))
+    while len(rows) < n:
+        rows.append((int(rng.integers(case.B)), int(rng.integers(case.H)), int(rng.integers(case.N_q))))
+    return np.asarray(rows[:n], dtype=np.int64)
