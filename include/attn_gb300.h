@@ -1,0 +1,110 @@
+/*
+ * attn_gb300.h - C ABI of the fused exact-attention forward pass for GB300 (sm_103a).
+ *
+ * The operation (FlashAttention page, section "Problems of standard attention",
+ * formula Attention(Q,K,V) = softmax(Q K^T / sqrt(d_k)) V; computed as the
+ * pages' fused, tiled kernel with an online softmax, sections "Tiling",
+ * "Online softmax" and "Fusing operations into one CUDA kernel"):
+ *
+ *   for every batch b, head h and query row i
+ *     s_j    = scale * <q[b,i,h,:], k[b,j,h,:]>          for j in A(i)
+ *     o[b,i,h,:] = sum_j softmax(s)_j * v[b,j,h,:]
+ *     lse[b,h,i] = ln sum_j exp(s_j)                       (natural log, fp32)
+ *
+ *   A(i) = {0 .. N_k-1}; with causal != 0, A(i) = {j : j <= i + N_k - N_q}
+ *   (bottom-right alignment; j <= i when N_q == N_k).  A row whose A(i) is
+ *   empty gets o = 0 and lse = -inf.  The N_q x N_k score matrix is never
+ *   written to memory.
+ *
+ * Layouts (all contiguous, row-major, device memory):
+ *   q, o : [B, N_q, H, d]      k, v : [B, N_k, H, d]      lse : [B, H, N_q] fp32
+ *   o is bf16 for bf16 and e4m3 inputs, fp16 for fp16 inputs.
+ *   d (head dimension) must be 64 or 128.
+ *   q, k, v, o must be 16-byte aligned; lse 4-byte aligned.  lse may be NULL
+ *   (then it is not written).
+ *
+ * FP8 (FlashAttention-3 page, section "Low precision (FP8)"): q, k, v hold
+ *   float8 e4m3 codes; the real inputs are code * descale with one fp32
+ *   descale per (batch, head): q_descale, k_descale, v_descale are device
+ *   arrays of B*H floats indexed b*H + h.
+ *
+ * Ownership: the caller allocates and owns every buffer.  The library
+ *   allocates no device memory; inputs are never modified.
+ *
+ * Asynchrony: calls are enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *   default stream) and return at once; results are valid once the stream has
+ *   reached them.  Results are deterministic (a fixed reduction order per row).
+ *
+ * Errors: arguments are checked before anything is launched and give
+ *   ATTN_ERR_INVALID_ARG (null pointer, negative size, misaligned pointer,
+ *   non-finite or non-positive scale, bad dtype) or ATTN_ERR_UNSUPPORTED
+ *   (d not 64/128, a grid dimension out of range).  ATTN_ERR_CUDA reports a
+ *   failed tensor-map encode or launch (cudaGetLastError is cleared).
+ *   Kernels never trap: every wait inside them is bounded; a wait that runs
+ *   out sets a device status word, the kernel returns, and attn_check_status
+ *   reports ATTN_ERR_TIMEOUT.  Zero-sized problems (B, H or N_q == 0) launch
+ *   nothing and return ATTN_OK; N_k == 0 writes o = 0 and lse = -inf.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,
+    ATTN_ERR_UNSUPPORTED = 2,
+    ATTN_ERR_CUDA = 3,
+    ATTN_ERR_TIMEOUT = 4
+} attn_status_t;
+
+typedef enum {
+    ATTN_BF16 = 0,
+    ATTN_FP16 = 1,
+    ATTN_FP8_E4M3 = 2
+} attn_dtype_t;
+
+/* Fused forward pass on the tensor cores (tcgen05 MMAs, TMEM accumulators,
+ * TMA-fed shared-memory ring).  dtype ATTN_FP8_E4M3 means unit descales. */
+ATTN_API attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int H, int N_q, int N_k, int d, float scale, int causal,
+                       attn_dtype_t dtype, void* stream);
+
+/* FP8 e4m3 forward pass with per-(batch, head) fp32 descales (device arrays of
+ * B*H floats; none may be NULL).  o is bf16. */
+ATTN_API attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                           const float* q_descale, const float* k_descale,
+                           const float* v_descale,
+                           int B, int H, int N_q, int N_k, int d, float scale, int causal,
+                           void* stream);
+
+/* The same operation on the CUDA cores only (fp32 FMAs, no tensor cores): a
+ * second, independent GPU implementation used to cross-check the tensor-core
+ * path.  Descales may be NULL (unit) and are used only for ATTN_FP8_E4M3. */
+ATTN_API attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const float* q_descale, const float* k_descale,
+                            const float* v_descale,
+                            int B, int H, int N_q, int N_k, int d, float scale, int causal,
+                            attn_dtype_t dtype, void* stream);
+
+/* Synchronises `stream`, then returns and clears the device status word:
+ * ATTN_ERR_TIMEOUT if a bounded wait inside a kernel ran out since the last
+ * call, ATTN_ERR_CUDA if the stream reports an error, else ATTN_OK. */
+ATTN_API attn_status_t attn_check_status(void* stream);
+
+/* Static, human-readable name of a status code. */
+ATTN_API const char* attn_status_string(attn_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -1,0 +1,190 @@
+"""GB300-native fused exact-attention forward pass (sm_103a).
+
+A thin Python binding over the C ABI of libattn_gb300.so (include/attn_gb300.h):
+it only marshals arguments (torch tensors -> device pointers, sizes, the
+current CUDA stream).  Every step of the computation runs in the library's
+CUDA kernels.  There is no CPU path: if the extension is not built, or no GPU
+is present, the calls raise.
+
+Operation: O = softmax(Q K^T * scale [+ causal mask]) V and the per-row
+logsumexp (FlashAttention page, section "Problems of standard attention",
+computed as in its sections "Tiling", "Online softmax" and "Fusing operations
+into one CUDA kernel").  Layout [B, N, H, d], lse [B, H, N_q].
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from . import ext_build as _build
+
+__all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_simt", "attn_check_status",
+           "attn_status_string", "AttnError", "lib", "build"]
+
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
+ATTN_BF16, ATTN_FP16, ATTN_FP8_E4M3 = range(3)
+
+_LIB = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {attn_status_string(status)} (status {status})")
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA extension in-tree (nvcc, sm_103a)."""
+    return _build.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it was never built)."""
+    global _LIB
+    if _LIB is None:
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA extension {os.path.basename(path)} is not built; run "
+                "io_aware_exact_03_gb300.build() (nvcc, sm_103a) first")
+        L = ctypes.CDLL(path)
+        vp, fp, i, f = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        L.attn_fwd.argtypes = [vp, vp, vp, vp, fp, i, i, i, i, i, f, i, i, vp]
+        L.attn_fwd.restype = i
+        L.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, i, i, i, i, i, f, i, vp]
+        L.attn_fwd_fp8.restype = i
+        L.attn_fwd_simt.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, i, i, i, i, i, f, i, i, vp]
+        L.attn_fwd_simt.restype = i
+        L.attn_check_status.argtypes = [vp]
+        L.attn_check_status.restype = i
+        L.attn_status_string.argtypes = [i]
+        L.attn_status_string.restype = ctypes.c_char_p
+        _LIB = L
+    return _LIB
+
+
+def attn_status_string(status: int) -> str:
+    names = {0: "ok", 1: "invalid argument", 2: "unsupported shape or dtype",
+             3: "CUDA error", 4: "bounded wait timed out inside a kernel"}
+    if _LIB is not None:
+        return _LIB.attn_status_string(int(status)).decode()
+    return names.get(int(status), "unknown status")
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    if t.dtype == torch.float16:
+        return ATTN_FP16
+    if t.dtype == torch.float8_e4m3fn:
+        return ATTN_FP8_E4M3
+    raise TypeError(f"unsupported input dtype {t.dtype}")
+
+
+def _check_inputs(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous [B, N, H, d]")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be 4-D [B, N, H, d]")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    B, N_q, H, d = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[2] != H or k.shape[3] != d:
+        raise ValueError("k and v must be [B, N_k, H, d] matching q")
+    return B, N_q, H, d, k.shape[1]
+
+
+def _outputs(q, o, lse, B, N_q, H, d):
+    torch = _torch()
+    out_dtype = torch.float16 if q.dtype == torch.float16 else torch.bfloat16
+    if o is None:
+        o = torch.empty((B, N_q, H, d), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N_q), dtype=torch.float32, device=q.device)
+    if o.dtype != out_dtype or tuple(o.shape) != (B, N_q, H, d) or not o.is_contiguous():
+        raise ValueError("o must be a contiguous [B, N_q, H, d] tensor of the output dtype")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N_q) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, N_q] tensor")
+    return o, lse
+
+
+def _stream(stream, device):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _raise(st, where):
+    if st != ATTN_OK:
+        raise AttnError(st, where)
+
+
+def attn_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, stream=None):
+    """Tensor-core forward pass. bf16 / fp16 / e4m3 (unit descales) inputs.
+
+    Returns (o, lse); outputs are allocated when not given.
+    """
+    B, N_q, H, d, N_k = _check_inputs(q, k, v)
+    o, lse = _outputs(q, o, lse, B, N_q, H, d)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N_q, N_k, d,
+                        scale, int(bool(causal)), _dtype_code(q), _stream(stream, q.device))
+    _raise(st, "attn_fwd")
+    return o, lse
+
+
+def attn_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, o=None, lse=None, scale=None,
+                 causal=False, stream=None):
+    """Tensor-core forward pass on e4m3 codes with per-(batch, head) fp32 descales [B, H]."""
+    B, N_q, H, d, N_k = _check_inputs(q, k, v)
+    torch = _torch()
+    if q.dtype != torch.float8_e4m3fn:
+        raise TypeError("attn_fwd_fp8 takes float8_e4m3fn inputs")
+    for name, t in (("q_descale", q_descale), ("k_descale", k_descale), ("v_descale", v_descale)):
+        if not (t.is_cuda and t.dtype == torch.float32 and t.numel() == B * H and t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA float32 tensor of B*H values")
+    o, lse = _outputs(q, o, lse, B, N_q, H, d)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib().attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(q_descale),
+                            _ptr(k_descale), _ptr(v_descale), B, H, N_q, N_k, d, scale,
+                            int(bool(causal)), _stream(stream, q.device))
+    _raise(st, "attn_fwd_fp8")
+    return o, lse
+
+
+def attn_fwd_simt(q, k, v, o=None, lse=None, scale=None, causal=False, q_descale=None,
+                  k_descale=None, v_descale=None, stream=None):
+    """CUDA-core (no tensor core) forward pass: the independent GPU cross-check."""
+    B, N_q, H, d, N_k = _check_inputs(q, k, v)
+    o, lse = _outputs(q, o, lse, B, N_q, H, d)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib().attn_fwd_simt(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(q_descale),
+                             _ptr(k_descale), _ptr(v_descale), B, H, N_q, N_k, d, scale,
+                             int(bool(causal)), _dtype_code(q), _stream(stream, q.device))
+    _raise(st, "attn_fwd_simt")
+    return o, lse
+
+
+def attn_check_status(stream=None, device=None):
+    """Synchronise the stream and raise AttnError if a kernel's bounded wait ran out."""
+    torch = _torch()
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    st = lib().attn_check_status(_stream(stream, dev))
+    _raise(st, "attn_check_status")
+    return st

@@ -1,0 +1,133 @@
+// C ABI of the exact-attention forward pass (declared in include/attn_gb300.h).
+// Validates arguments on the host, then enqueues one kernel on the caller's
+// stream.  No device memory is allocated here.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "attn_gb300.h"
+#include "attn_internal.h"
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+attn_status_t validate(const attn::Problem& p) {
+    if (p.B < 0 || p.H < 0 || p.N_q < 0 || p.N_k < 0) return ATTN_ERR_INVALID_ARG;
+    if (!(p.scale > 0.f) || !isfinite(p.scale)) return ATTN_ERR_INVALID_ARG;
+    if (p.dtype != attn::kBF16 && p.dtype != attn::kFP16 && p.dtype != attn::kE4M3)
+        return ATTN_ERR_INVALID_ARG;
+    if (p.d != 64 && p.d != 128) return ATTN_ERR_UNSUPPORTED;
+    const bool empty = p.B == 0 || p.H == 0 || p.N_q == 0;
+    if (empty) return ATTN_OK;
+    if (!p.q || !p.o) return ATTN_ERR_INVALID_ARG;
+    if (p.N_k > 0 && (!p.k || !p.v)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(p.q, 16) || !aligned(p.o, 16) || (p.k && !aligned(p.k, 16)) ||
+        (p.v && !aligned(p.v, 16)) || (p.lse && !aligned(p.lse, 4)))
+        return ATTN_ERR_INVALID_ARG;
+    if ((p.q_descale && !aligned(p.q_descale, 4)) || (p.k_descale && !aligned(p.k_descale, 4)) ||
+        (p.v_descale && !aligned(p.v_descale, 4)))
+        return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+attn_status_t from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return ATTN_OK;
+    if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_ERR_CUDA;
+}
+
+attn::Problem make_problem(const void* q, const void* k, const void* v, void* o, float* lse,
+                           const float* qd, const float* kd, const float* vd, int B, int H,
+                           int N_q, int N_k, int d, float scale, int causal, int dtype) {
+    attn::Problem p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.lse = lse;
+    p.q_descale = qd;
+    p.k_descale = kd;
+    p.v_descale = vd;
+    p.B = B;
+    p.H = H;
+    p.N_q = N_q;
+    p.N_k = N_k;
+    p.d = d;
+    p.scale = scale;
+    p.causal = causal ? 1 : 0;
+    p.dtype = dtype;
+    return p;
+}
+
+bool is_empty(const attn::Problem& p) { return p.B == 0 || p.H == 0 || p.N_q == 0; }
+
+attn_status_t run_tc(const attn::Problem& p, cudaStream_t s) {
+    attn_status_t st = validate(p);
+    if (st != ATTN_OK || is_empty(p)) return st;
+    cudaError_t e = attn::launch_tc(p, s);
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int N_q, int N_k, int d, float scale, int causal,
+                       attn_dtype_t dtype, void* stream) {
+    attn::Problem p = make_problem(q, k, v, o, lse, nullptr, nullptr, nullptr, B, H, N_q, N_k, d,
+                                   scale, causal, (int)dtype);
+    return run_tc(p, static_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                           const float* q_descale, const float* k_descale,
+                           const float* v_descale, int B, int H, int N_q, int N_k, int d,
+                           float scale, int causal, void* stream) {
+    if (!is_empty(make_problem(q, k, v, o, lse, nullptr, nullptr, nullptr, B, H, N_q, N_k, d,
+                               scale, causal, attn::kE4M3)) &&
+        (!q_descale || !k_descale || !v_descale))
+        return ATTN_ERR_INVALID_ARG;
+    attn::Problem p = make_problem(q, k, v, o, lse, q_descale, k_descale, v_descale, B, H, N_q,
+                                   N_k, d, scale, causal, attn::kE4M3);
+    return run_tc(p, static_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const float* q_descale, const float* k_descale,
+                            const float* v_descale, int B, int H, int N_q, int N_k, int d,
+                            float scale, int causal, attn_dtype_t dtype, void* stream) {
+    attn::Problem p = make_problem(q, k, v, o, lse, q_descale, k_descale, v_descale, B, H, N_q,
+                                   N_k, d, scale, causal, (int)dtype);
+    attn_status_t st = validate(p);
+    if (st != ATTN_OK || is_empty(p)) return st;
+    cudaError_t e = attn::launch_simt(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    return from_cuda(e);
+}
+
+attn_status_t attn_check_status(void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+    unsigned a = 0, b = 0;
+    if (attn::tc_take_status(&a, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (attn::simt_take_status(&b, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    if ((a | b) & attn::kStatusTimeout) return ATTN_ERR_TIMEOUT;
+    return ATTN_OK;
+}
+
+const char* attn_status_string(attn_status_t s) {
+    switch (s) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_INVALID_ARG: return "invalid argument";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case ATTN_ERR_CUDA: return "CUDA error";
+        case ATTN_ERR_TIMEOUT: return "bounded wait timed out inside a kernel";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,38 @@
+// Internal interface between the C ABI (attn_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+enum Dtype : int { kBF16 = 0, kFP16 = 1, kE4M3 = 2 };
+
+// Device status bits, OR-ed into a per-kernel-file status word.
+enum : unsigned { kStatusTimeout = 1u };
+
+struct Problem {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* o;
+    float* lse;              // may be null
+    const float* q_descale;  // [B*H] or null (unit) - e4m3 only
+    const float* k_descale;
+    const float* v_descale;
+    int B, H, N_q, N_k, d;
+    float scale;
+    int causal;
+    int dtype;
+};
+
+// CUDA-core kernel (attn_simt.cu).
+cudaError_t launch_simt(const Problem& p, cudaStream_t stream);
+cudaError_t simt_take_status(unsigned* out, cudaStream_t stream);
+
+// Tensor-core kernel (attn_tc.cu).  Returns cudaErrorNotSupported for shapes
+// it does not take.
+cudaError_t launch_tc(const Problem& p, cudaStream_t stream);
+cudaError_t tc_take_status(unsigned* out, cudaStream_t stream);
+
+}  // namespace attn

@@ -1,0 +1,100 @@
+"""Host-side checks of the C ABI: the library loads, exports every function the
+header declares, and rejects bad arguments before touching the GPU (no call
+here reaches a kernel launch, so these run without a GPU)."""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import io_aware_exact_03_gb300 as attn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    attn.build()
+    return attn.lib()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(attn_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_fwd_fp8", "attn_fwd_simt", "attn_check_status", "attn_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in declared_functions():
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+
+
+def test_only_the_c_abi_is_exported():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", attn.ext_build.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    assert exported == set(declared_functions())
+
+
+def test_status_strings(L):
+    for s, txt in [(0, b"ok"), (1, b"invalid argument"), (4, b"bounded wait timed out inside a kernel")]:
+        assert L.attn_status_string(s) == txt
+    assert L.attn_status_string(99) == b"unknown status"
+
+
+P = 0x10000  # a 16-byte aligned fake address; never dereferenced by these calls
+
+
+def call_fwd(L, q=P, k=P, v=P, o=P, lse=P, B=1, H=1, N_q=16, N_k=16, d=64, scale=0.125,
+             causal=0, dtype=0):
+    return L.attn_fwd(q, k, v, o, lse, B, H, N_q, N_k, d, scale, causal, dtype, None)
+
+
+def test_rejects_bad_arguments(L):
+    assert call_fwd(L, q=None) == attn.ATTN_ERR_INVALID_ARG
+    assert call_fwd(L, o=None) == attn.ATTN_ERR_INVALID_ARG
+    assert call_fwd(L, k=None) == attn.ATTN_ERR_INVALID_ARG
+    assert call_fwd(L, B=-1) == attn.ATTN_ERR_INVALID_ARG
+    assert call_fwd(L, N_k=-5) == attn.ATTN_ERR_INVALID_ARG
+    assert call_fwd(L, scale=0.0) == attn.ATTN_ERR_INVALID_ARG
+    assert call_fwd(L, scale=float("nan")) == attn.ATTN_ERR_INVALID_ARG
+    assert call_fwd(L, scale=float("inf")) == attn.ATTN_ERR_INVALID_ARG
+    assert call_fwd(L, scale=-1.0) == attn.ATTN_ERR_INVALID_ARG
+    assert call_fwd(L, q=P + 8) == attn.ATTN_ERR_INVALID_ARG      # misaligned
+    assert call_fwd(L, lse=P + 2) == attn.ATTN_ERR_INVALID_ARG
+    assert call_fwd(L, dtype=7) == attn.ATTN_ERR_INVALID_ARG
+    assert call_fwd(L, d=96) == attn.ATTN_ERR_UNSUPPORTED
+    assert call_fwd(L, d=256) == attn.ATTN_ERR_UNSUPPORTED
+
+
+def test_empty_problems_launch_nothing(L):
+    # B, H or N_q == 0: nothing to compute; returns before any CUDA call
+    assert call_fwd(L, B=0, q=None, k=None, v=None, o=None, lse=None) == attn.ATTN_OK
+    assert call_fwd(L, H=0) == attn.ATTN_OK
+    assert call_fwd(L, N_q=0) == attn.ATTN_OK
+
+
+def test_fp8_requires_descales(L):
+    st = L.attn_fwd_fp8(P, P, P, P, P, None, P, P, 1, 1, 16, 16, 128, 0.1, 0, None)
+    assert st == attn.ATTN_ERR_INVALID_ARG
+    st = L.attn_fwd_simt(None, P, P, P, P, None, None, None, 1, 1, 16, 16, 128, 0.1, 0, 2, None)
+    assert st == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        attn.attn_fwd(q, q, q)

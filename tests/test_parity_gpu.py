@@ -1,0 +1,122 @@
+"""GPU parity: both CUDA implementations (tensor-core attn_fwd / attn_fwd_fp8 and
+the CUDA-core attn_fwd_simt) against the fp64 CPU oracle, element by element.
+
+The five workload cases are checked in full where the oracle finishes in
+seconds (C1, C2) and on 256 seeded (b, h, i) rows otherwise (C3-C5, at their
+full sizes and in the launch configuration the benchmark times).  Edge cases
+cover ragged tiles, N_q != N_k under the causal mask (including rows with no
+allowed key), N_k = 1, N_k = 0, N_q = 0, several batches and heads, every
+dtype and both head dimensions.
+"""
+
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import io_aware_exact_03_gb300 as attn
+import synthetic
+from parity import check_full, check_sampled, compare, oracle_full, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+IMPLS = ["tc", "simt"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    attn.build()
+    attn.lib()
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("name", ["C1", "C2"])
+def test_case_full(name, impl):
+    check_full(synthetic.CASES[name], impl)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("name", ["C3", "C4", "C5"])
+def test_case_sampled(name, impl):
+    check_sampled(synthetic.CASES[name], impl)
+
+
+EDGE = [
+    # B, H, N_q, N_k, d, causal, dtype
+    (1, 1, 1, 1, 64, False, "bf16"),
+    (2, 3, 200, 200, 64, True, "bf16"),
+    (2, 3, 200, 200, 128, False, "fp16"),
+    (1, 2, 100, 300, 128, True, "bf16"),
+    (1, 2, 300, 100, 64, True, "bf16"),      # first 200 rows see no key
+    (1, 1, 257, 129, 128, False, "bf16"),
+    (1, 2, 130, 1, 64, False, "bf16"),       # N_k = 1: O = v row 0
+    (1, 1, 384, 384, 128, True, "fp16"),
+    (3, 5, 129, 255, 64, False, "bf16"),
+    (2, 2, 129, 383, 128, True, "e4m3"),
+    (1, 3, 256, 256, 64, False, "e4m3"),
+    (1, 2, 640, 640, 128, True, "e4m3"),
+]
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("shape", EDGE, ids=lambda s: "x".join(map(str, s)))
+def test_edge_cases(shape, impl):
+    B, H, N_q, N_k, d, causal, dtype = shape
+    case = synthetic.custom_case(B, H, N_q, N_k, d, causal, dtype, seed=zlib.crc32(repr(shape).encode()) % 10000,
+                                 outliers=False)
+    inputs = synthetic.make_inputs(case)
+    O, lse = run_gpu(case, to_device(inputs), impl)
+    O_ref, lse_ref = oracle_full(case, inputs)
+    compare(case, O, lse, O_ref, lse_ref)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_no_keys_gives_zero_and_minus_inf(impl):
+    case = synthetic.custom_case(2, 2, 70, 0, 64, False, "bf16")
+    q = torch.randn(2, 70, 2, 64, device="cuda").to(torch.bfloat16)
+    kv = torch.empty(2, 0, 2, 64, device="cuda", dtype=torch.bfloat16)
+    o = torch.full((2, 70, 2, 64), 7.0, device="cuda", dtype=torch.bfloat16)
+    lse = torch.zeros(2, 2, 70, device="cuda")
+    fn = attn.attn_fwd if impl == "tc" else attn.attn_fwd_simt
+    fn(q, kv, kv, o=o, lse=lse, scale=case.scale)
+    attn.attn_check_status()
+    assert torch.all(o == 0)
+    assert torch.all(torch.isneginf(lse))
+
+
+def test_empty_query_is_a_no_op():
+    q = torch.empty(1, 0, 2, 64, device="cuda", dtype=torch.bfloat16)
+    k = torch.randn(1, 5, 2, 64, device="cuda").to(torch.bfloat16)
+    o, lse = attn.attn_fwd(q, k, k)
+    attn.attn_check_status()
+    assert o.shape == (1, 0, 2, 64) and lse.shape == (1, 2, 0)
+
+
+def test_deterministic_bitwise():
+    case = synthetic.CASES["C3"]
+    dev = to_device(synthetic.make_inputs(case))
+    o1, l1 = attn.attn_fwd(dev["q"], dev["k"], dev["v"], scale=case.scale, causal=True)
+    o2, l2 = attn.attn_fwd(dev["q"], dev["k"], dev["v"], scale=case.scale, causal=True)
+    attn.attn_check_status()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_tc_and_simt_agree_closely():
+    case = synthetic.CASES["C2"]
+    dev = to_device(synthetic.make_inputs(case))
+    O1, l1 = run_gpu(case, dev, "tc")
+    O2, l2 = run_gpu(case, dev, "simt")
+    assert np.abs(O1 - O2).max() < 1e-2
+    assert np.abs(l1 - l2).max() < 1e-3
+
+
+def test_inputs_are_not_modified():
+    case = synthetic.CASES["C1"]
+    dev = to_device(synthetic.make_inputs(case))
+    before = {k: dev[k].clone() for k in ("q", "k", "v")}
+    attn.attn_fwd(dev["q"], dev["k"], dev["v"], scale=case.scale)
+    attn.attn_check_status()
+    for k in before:
+        assert torch.equal(before[k], dev[k])
