@@ -54,7 +54,19 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--case", choices=["C1", "C2", "C3", "C4", "C5"], default=None,
+                    help="measure one workload case alone instead of the C4 + C5 step")
     return ap.parse_args()
+
+
+def workload(args):
+    """(case names, description) of one step."""
+    if args.case:
+        import synthetic
+        c = synthetic.CASES[args.case]
+        return (args.case,), (f"{c.name} {c.dtype} {'causal' if c.causal else 'non-causal'} "
+                              f"B{c.B} H{c.H} N_q{c.N_q} N_k{c.N_k} d{c.d}; one attention call per step")
+    return WORKLOAD, WORKLOAD_DESC
 
 
 def env_rank():
@@ -147,8 +159,8 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ CPU oracle leg
-def oracle_rows_rate(n_rows_c4, n_rows_c5, seed):
-    """Time the fp64 CPU oracle on sampled rows of C4 and C5; returns (flops, seconds, threads)."""
+def oracle_rows_rate(counts, seed):
+    """Time the fp64 CPU oracle on sampled rows of the named cases; returns (flops, seconds, threads)."""
     import numpy as np
     import oracle
     import synthetic
@@ -156,10 +168,10 @@ def oracle_rows_rate(n_rows_c4, n_rows_c5, seed):
     threads = oracle.default_threads()
     flops = 0.0
     secs = 0.0
-    for name, n in (("C4", n_rows_c4), ("C5", n_rows_c5)):
+    for j, (name, n) in enumerate(counts.items()):
         case = synthetic.CASES[name]
         q, k, v = _f64_inputs(name)
-        rows = synthetic.sample_rows(case, n, seed=seed + (7 if name == "C5" else 0))
+        rows = synthetic.sample_rows(case, n, seed=seed + 7 * j)
         keys = np.array([_allowed(case, int(i)) for i in rows[:, 2]], dtype=np.float64)
         t0 = time.perf_counter()
         oracle.attention_rows(q, k, v, case.scale, case.causal, rows, n_threads=threads)
@@ -185,16 +197,18 @@ def _allowed(case, i):
     return max(0, min(case.N_k, i + case.N_k - case.N_q + 1))
 
 
-def cpu_baseline(target_s=12.0):
-    _f64_inputs("C4")
-    _f64_inputs("C5")
-    f, s, thr = oracle_rows_rate(32, 16, seed=11)              # calibration
+def cpu_baseline(names, target_s=12.0):
+    base = {n: (32 if i == 0 else 16) for i, n in enumerate(names)}
+    for n in names:
+        _f64_inputs(n)
+    f, s, thr = oracle_rows_rate(base, seed=11)                # calibration
     scale = max(1.0, target_s / max(s, 1e-3))
-    n4, n5 = int(32 * scale), int(16 * scale)
-    f, s, thr = oracle_rows_rate(n4, n5, seed=12)
+    counts = {n: int(c * scale) for n, c in base.items()}
+    f, s, thr = oracle_rows_rate(counts, seed=12)
+    desc = " and ".join(f"{c} of {n}" for n, c in counts.items())
     return {"value": f / s / 1e12, "unit": UNIT, "cores": thr, "kind": "oracle",
-            "sample": f"{n4} seeded query rows of C4 and {n5} of C5 (full key range each), "
-                      f"fp64 one-pass oracle, {s:.1f} s"}
+            "sample": f"seeded query rows ({desc}; full key range each), fp64 one-pass oracle, "
+                      f"{s:.1f} s"}
 
 
 # ----------------------------------------------------------------- our arm
@@ -212,14 +226,15 @@ def run_ours(args):
     attn.build()
     attn.lib()
 
-    cases = [synthetic.CASES[n] for n in WORKLOAD]
+    names, desc = workload(args)
+    cases = [synthetic.CASES[n] for n in names]
     host, dev, outs = [], [], []
     for c in cases:
         c_r = dataclasses.replace(c, seed=c.seed + 100 * rank)
         inp = synthetic.make_inputs(c_r)
         host.append(inp)
         dev.append({k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()})
-        out_dtype = torch.bfloat16
+        out_dtype = torch.float16 if c.dtype == "fp16" else torch.bfloat16
         outs.append((torch.empty((c.B, c.N_q, c.H, c.d), dtype=out_dtype, device="cuda"),
                      torch.empty((c.B, c.H, c.N_q), dtype=torch.float32, device="cuda")))
     stream = torch.cuda.current_stream()
@@ -290,7 +305,7 @@ def run_ours(args):
     dc = cases[dom]
     dom_peak = fp8_peak if dc.dtype == "e4m3" else bf16_peak
     dom_ach = dc.flops / (kern_ms[dom] / 1e3) / 1e12
-    traffic = read_traffic() if dc.name == "C4" else None
+    traffic = read_traffic() if (dc.name == "C4" and len(cases) == 2) else None
     roofline = {"bound": "tensor", "achieved": round(dom_ach, 1), "peak": round(dom_peak, 1),
                 "unit": "TFLOP/s", "frac": round(dom_ach / dom_peak, 4), "traffic": traffic,
                 "kernel": f"attn_tc_kernel {dc.name} ({dc.dtype}, causal={dc.causal})",
@@ -304,15 +319,15 @@ def run_ours(args):
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            cpu = cpu_baseline()
+            cpu = cpu_baseline(names)
         result = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_total / K, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16,e4m3", "data": "synthetic (seeded N(0,1); C5 with 0.1% x10 outliers)",
-            "config": {"workload": WORKLOAD_DESC, "global_batch": sum(c.B * c.H for c in cases) * world,
+            "config": {"workload": desc, "global_batch": sum(c.B * c.H for c in cases) * world,
                        "seq_len": [c.N_q for c in cases], "parallelism": f"dp{world} (independent shards)",
-                       "l2": "inputs larger than L2 (288 MiB of Q/K/V per step), no flush"},
+                       "l2": f"Q/K/V of one step: {sum(3 * c.B * c.H * c.N_q * c.d * (1 if c.dtype == 'e4m3' else 2) for c in cases) / 2**20:.0f} MiB (L2 is 129 MB); no flush"},
             "pct_of_tensor_peak_step": round(100 * step_frac, 2),
             "per_kernel": per_kernel,
             "roofline": roofline,
@@ -392,15 +407,16 @@ def run_reference(args):
     if rank != 0:
         return None
     import oracle
-    _f64_inputs("C4")
-    _f64_inputs("C5")
-    n4, n5 = 32, 16
+    names, desc = workload(args)
+    counts = {n: (32 if i == 0 else 16) for i, n in enumerate(names)}
+    for n in names:
+        _f64_inputs(n)
     for s in range(args.warmup):
-        oracle_rows_rate(n4, n5, seed=1000 + s)
+        oracle_rows_rate(counts, seed=1000 + s)
     flops = secs = 0.0
     thr = oracle.default_threads()
     for s in range(args.steps):
-        f, t, thr = oracle_rows_rate(n4, n5, seed=5000 + s)
+        f, t, thr = oracle_rows_rate(counts, seed=5000 + s)
         flops += f
         secs += t
     value = flops / secs / 1e12
@@ -409,10 +425,10 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1); C5 with 0.1% x10 outliers)",
-        "config": {"workload": WORKLOAD_DESC, "parallelism": "CPU host cores, rank 0 only"},
+        "config": {"workload": desc, "parallelism": "CPU host cores, rank 0 only"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
-                         "sample": f"per step {n4} seeded query rows of C4 and {n5} of C5 "
-                                   "(full key range), fp64 one-pass oracle"},
+                         "sample": "per step " + " and ".join(f"{c} seeded query rows of {n}" for n, c in counts.items())
+                                   + " (full key range), fp64 one-pass oracle"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(result), flush=True)

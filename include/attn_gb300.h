@@ -1,7 +1,7 @@
 /*
  * attn_gb300.h - C ABI of the fused exact-attention forward pass for GB300 (sm_103a).
  *
- * The operation (FlashAttention page, section "Problems of standard attention",
+ * The operation ("FlashAttention (HI)" page, section "Problems of standard attention",
  * formula Attention(Q,K,V) = softmax(Q K^T / sqrt(d_k)) V; computed as the
  * pages' fused, tiled kernel with an online softmax, sections "Tiling",
  * "Online softmax" and "Fusing operations into one CUDA kernel"):
@@ -23,7 +23,8 @@
  *   q, k, v, o must be 16-byte aligned; lse 4-byte aligned.  lse may be NULL
  *   (then it is not written).
  *
- * FP8 (FlashAttention-3 page, section "Low precision (FP8)"): q, k, v hold
+ * FP8 ("FlashAttention-3 (BN)" page, section "Low precision (FP8) and reducing
+ * quantisation error"): q, k, v hold
  *   float8 e4m3 codes; the real inputs are code * descale with one fp32
  *   descale per (batch, head): q_descale, k_descale, v_descale are device
  *   arrays of B*H floats indexed b*H + h.

@@ -7,7 +7,7 @@ CUDA kernels.  There is no CPU path: if the extension is not built, or no GPU
 is present, the calls raise.
 
 Operation: O = softmax(Q K^T * scale [+ causal mask]) V and the per-row
-logsumexp (FlashAttention page, section "Problems of standard attention",
+logsumexp ("FlashAttention (HI)" page, section "Problems of standard attention",
 computed as in its sections "Tiling", "Online softmax" and "Fusing operations
 into one CUDA kernel").  Layout [B, N, H, d], lse [B, H, N_q].
 """

@@ -1,6 +1,6 @@
 // Exact attention forward on the CUDA cores: a plain tiled kernel with an
-// online softmax (FlashAttention page, sections "Tiling" and "Online
-// softmax").  fp32 scores, fp32 exponentials, fp32 accumulation.  It is the
+// online softmax ("FlashAttention (HI)" page, sections "Tiling and block
+// processing" and "Online softmax computation").  fp32 scores, fp32 exponentials, fp32 accumulation.  It is the
 // second, independent GPU implementation that cross-checks the tensor-core
 // kernel; it is not the timed path.
 //

@@ -1,9 +1,10 @@
 // Fused exact-attention forward on the fifth-generation tensor cores (sm_103a).
 //
-// The pages' method (FlashAttention page: "Tiling", "Online softmax",
-// "Fusing operations into one CUDA kernel"; FlashAttention-2 page: "Improved
-// parallelism"; FlashAttention-3 page: "Asynchronous execution and warp
-// specialisation", "Reducing memory operations") mapped onto Blackwell:
+// The pages' method ("FlashAttention (HI)": "Tiling and block processing",
+// "Online softmax computation", "Combining operations in one CUDA kernel";
+// "FlashAttention-2 (BN)": "Improved parallelism"; "FlashAttention-3 (BN)":
+// "Asynchronous execution and warp specialisation", "Reducing memory
+// operations") mapped onto Blackwell:
 //
 //   * one CTA owns a 128-row query tile of one (batch, head); the grid spans
 //     batch x heads x query tiles, so one head is spread over many SMs;
@@ -16,8 +17,9 @@
 //   * warps 2-5 (128 threads, one query row each) run the online softmax:
 //     TMEM -> registers, causal / ragged mask on the tiles that need it, row
 //     maximum, exp2, row sum, P back to TMEM as bf16 / fp16 / e4m3; they
-//     rescale the running output in TMEM only when the row maximum grew by
-//     more than 2^8 (so the P values stay <= 256), and write O / lse at the end.
+//     rescale the running output in TMEM only when the row maximum grew (for
+//     bf16 / fp16: by more than 2^8, so the P values stay <= 256), and write
+//     O / lse at the end.
 //   While the softmax works on S_j the tensor core already computes S_{j+1}
 //   and finishes P_{j-1} V_{j-1}.
 //
@@ -49,7 +51,6 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0;    // two score buffers: columns [0,128) and [128,256)
 constexpr uint32_t kColO = 256;
 constexpr uint32_t kColP = 384;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D, int KIND>
 struct Cfg {
@@ -70,6 +71,10 @@ struct Cfg {
     static constexpr uint32_t IDESC_QK = instr_desc(FMT, FMT, 0, 0, BM, BN);
     static constexpr uint32_t IDESC_PV = instr_desc(FMT, FMT, 0, 1, BM, D);
     static constexpr uint32_t P_COLS = BN * E / 4;         // TMEM columns holding P
+    // Rescale the running output only when the row maximum grew by more than
+    // this (log2 units).  bf16/fp16 P tolerate values up to 2^8; an e4m3 P
+    // must keep its largest weight exactly 1, so e4m3 rescales on every growth.
+    static constexpr float RESCALE_THRESHOLD = (KIND == kE4M3) ? 0.0f : 8.0f;
 };
 
 struct TcParams {
@@ -373,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int x = 1; x < BN; ++x) mx = fmaxf(mx, s[x]);
             const float m_new = mx * c;
-            const bool need = m_new > m_used + kRescaleThreshold;
+            const bool need = m_new > m_used + C::RESCALE_THRESHOLD;
             const bool any = __any_sync(0xffffffffu, need);
             float alpha = 1.f;
             if (any) {

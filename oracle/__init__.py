@@ -7,12 +7,12 @@ lives in attn_oracle.c (built here with gcc, no CUDA), the two-pass cross-check
 in two_pass.py (numpy).
 
 Definition followed: Attention(Q,K,V) = softmax(Q K^T / sqrt(d_k)) V from the
-FlashAttention page, section "Problems of standard attention"; the one-pass
-form follows the same page, section "Online softmax".  Inputs are the rounded
+"FlashAttention (HI)" page, section "Problems of standard attention"; the one-pass
+form follows the same page, section "Online softmax computation".  Inputs are the rounded
 values the GPU sees: bf16 / fp16 are converted to float64 exactly; e4m3 codes
 are converted exactly and multiplied by their fp32 per-(batch, head) descale in
-float64 (the FP8 inputs of the FlashAttention-3 page, section "Low precision
-(FP8)").  The oracle does not imitate any rounding the GPU applies inside the
+float64 (the FP8 inputs of the "FlashAttention-3 (BN)" page, section "Low precision
+(FP8) and reducing quantisation error").  The oracle does not imitate any rounding the GPU applies inside the
 computation; the tolerances cover that.
 """
 

@@ -6,7 +6,7 @@
  * product path never links or calls it, and it shares no code with the CUDA
  * sources.
  *
- * What it computes (FlashAttention page, section "Problems of standard
+ * What it computes ("FlashAttention (HI)" page, section "Problems of standard
  * attention", formula Attention(Q,K,V) = softmax(Q K^T / sqrt(d_k)) V):
  *   for every query row (b, h, i) and every key j in the allowed set A(i)
  *     s_j   = scale * sum_t q[b,i,h,t] * k[b,j,h,t]
@@ -16,7 +16,7 @@
  *   (bottom-right alignment; equals j <= i when N_q == N_k).  A row with an
  *   empty A(i) gets O = 0 and lse = -inf.
  *
- * How (FlashAttention page, section "Online softmax"): one pass over the keys
+ * How ("FlashAttention (HI)" page, section "Online softmax computation"): one pass over the keys
  * that keeps a running maximum m, a running sum of exponentials l and a
  * running unnormalised output o, rescaling l and o whenever m grows:
  *   m' = max(m, s_j);  l = l e^{m-m'} + e^{s_j-m'};  o = o e^{m-m'} + e^{s_j-m'} v_j

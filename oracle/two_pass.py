@@ -1,7 +1,7 @@
 """Two-pass (materialised) softmax attention in numpy float64.
 
 TEST INFRASTRUCTURE ONLY: the oracle's own cross-check.  It follows the
-standard-attention definition on the FlashAttention page, section "Problems
+standard-attention definition on the "FlashAttention (HI)" page, section "Problems
 of standard attention": build the whole score row S = scale * q K^T, apply the
 mask, take the softmax with the row maximum subtracted, multiply by V.  It is
 the "naive" O(N^2)-memory method the pages contrast with the fused kernel, so

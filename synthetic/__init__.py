@@ -5,7 +5,7 @@ It draws and rounds inputs only; it holds none of the attention arithmetic.
 
 Workloads (shapes, dtypes, distributions) are the five attention-forward cases
 the FlashAttention pages motivate: a tiny exact check, a short-sequence batch,
-two causal long-context cases and an FP8 case with outliers (FlashAttention-3
+two causal long-context cases and an FP8 case with outliers ("FlashAttention-3 (BN)"
 page, section "Low precision (FP8) and reducing quantisation error").
 
 Recipe (all on the CPU, one ``torch.Generator`` per case):

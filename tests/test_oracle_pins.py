@@ -6,7 +6,7 @@ Each pin is a fact fixed by the pages or by mathematics:
   * special cases with closed forms: N_k = 1, identical key rows, Q = 0 causal;
   * invariances: shifting every key by one vector, permuting keys with values;
   * the online (one-pass) result equals the two-pass softmax (the online-softmax
-    claim of the FlashAttention page, section "Online softmax");
+    claim of the "FlashAttention (HI)" page, section "Online softmax computation");
   * a library special case: torch's fp64 math attention on the CPU.
 The mutant tests rebuild the oracle with one planted mistake each (a dropped
 scale, a wrong sign, a wrong index, an off-by-one mask, a missing rescale, a
