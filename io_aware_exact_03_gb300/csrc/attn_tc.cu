@@ -6,22 +6,25 @@
 // "Asynchronous execution and warp specialisation", "Reducing memory
 // operations") mapped onto Blackwell:
 //
-//   * one CTA owns a 128-row query tile of one (batch, head); the grid spans
-//     batch x heads x query tiles, so one head is spread over many SMs;
-//   * warp 0 (producer) streams the Q tile once and then K_j / V_j tiles
-//     through a ring of shared-memory slots with TMA, in the order the MMAs
-//     consume them (K0, K1, V0, K2, V1, ...), guarded by mbarriers;
-//   * warp 1 (one thread) issues tcgen05 MMAs: S_j = Q K_j^T into one of two
-//     TMEM score buffers, and O += P_j V_j with P_j read from TMEM; it owns the
-//     TMEM allocation;
-//   * warps 2-5 (128 threads, one query row each) run the online softmax:
-//     TMEM -> registers, causal / ragged mask on the tiles that need it, row
-//     maximum, exp2, row sum, P back to TMEM as bf16 / fp16 / e4m3; they
-//     rescale the running output in TMEM only when the row maximum grew (for
-//     bf16 / fp16: by more than 2^8, so the P values stay <= 256), and write
-//     O / lse at the end.
-//   While the softmax works on S_j the tensor core already computes S_{j+1}
-//   and finishes P_{j-1} V_{j-1}.
+//   * one CTA owns two adjacent 128-row query tiles (A, B) of one (batch,
+//     head), so every K/V tile brought on chip serves 256 query rows; the
+//     grid spans batch x heads x tile pairs (one head over many SMs), a few
+//     heads at a time so their K/V stay in L2, heaviest causal pairs first;
+//   * warp 0 (producer) streams Q_A, Q_B once and then K_0, V_0, K_1, V_1, ...
+//     through a ring of shared-memory slots with TMA, guarded by mbarriers;
+//   * warp 1 (one thread) issues the tcgen05 MMAs and owns TMEM:
+//     S_t = Q_t K_j^T into the TMEM score buffer of tile t, and
+//     O_t += P_t V_j with P_t read from TMEM (P overwrites its own S buffer;
+//     the next S_t is issued only after that P V MMA has completed);
+//   * warps 2-5 (tile A) and 6-9 (tile B), one query row per thread, run the
+//     online softmax: TMEM -> registers, causal / ragged mask on the tiles that
+//     need it, row maximum, exp2, row sum, P back to TMEM as bf16 / fp16 /
+//     e4m3; they rescale the running output in TMEM only when the row maximum
+//     grew (bf16 / fp16: by more than 2^8, so P stays <= 256), and write O /
+//     lse at the end.
+//   The two softmax groups interleave with each other's MMAs: while group A
+//   turns S_A into P_A the tensor core runs P_B V_j and the next S_B, and the
+//   other way round (the pages' ping-pong between two warp groups).
 //
 // Scores are kept in base 2: the logit scale folds in log2(e) (and, for e4m3,
 // the q and k descales); lse is converted back to the natural log.
@@ -44,13 +47,11 @@ using namespace ptx;
 
 __device__ unsigned g_tc_status = 0;
 
-constexpr int BM = 128;       // query rows per tile (MMA M)
-constexpr int BN = 128;       // keys per tile (MMA N of Q K^T, K of P V)
-constexpr int kThreads = 192; // 6 warps
+constexpr int BM = 128;        // query rows per tile (MMA M)
+constexpr int BN = 128;        // keys per tile (MMA N of Q K^T, K of P V)
+constexpr int kThreads = 320;  // 10 warps: producer, MMA, 2 x 4 softmax
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0;    // two score buffers: columns [0,128) and [128,256)
-constexpr uint32_t kColO = 256;
-constexpr uint32_t kColP = 384;
+constexpr int kSmemLimit = 232448;  // max dynamic shared memory per CTA
 
 template <int D, int KIND>
 struct Cfg {
@@ -60,11 +61,13 @@ struct Cfg {
     static constexpr int NC = RB / CB;                     // chunks per row
     static constexpr int TILE = BM * RB;                   // bytes per 128-row tile
     static constexpr int CHUNK = BM * CB;                  // bytes per chunk of a tile
-    static constexpr int SLOTS = (TILE >= 32768) ? 6 : 8;  // K/V ring depth
+    static constexpr int NB_FIXED = 1 + 2 + 2 + 2 + 1;     // q_full, s_full, p_full, pv_done, drain
+    static constexpr int SLOTS_FIT = (kSmemLimit - 1024 - 2 * TILE - 512) / TILE;
+    static constexpr int SLOTS = SLOTS_FIT > 8 ? 8 : SLOTS_FIT;  // K/V ring depth
     static constexpr uint32_t LAYOUT = (CB == 128) ? 2u : 4u;  // 128B / 64B swizzle
     static constexpr int MMA_K = 32 / E;                   // K per MMA instruction
-    static constexpr int NB = 1 + 2 * SLOTS + 2 + 2 + 1 + 1 + 1;  // mbarriers
-    static constexpr size_t SMEM_USED = 1024 + (size_t)TILE * (1 + SLOTS) + NB * 8 + 16;
+    static constexpr int NB = NB_FIXED + 2 * SLOTS;        // mbarriers
+    static constexpr size_t SMEM_USED = 1024 + (size_t)TILE * (2 + SLOTS) + NB * 8 + 16;
     // at least ~120 KB so two CTAs never share an SM (each takes all of TMEM)
     static constexpr size_t SMEM = SMEM_USED > 122880 ? SMEM_USED : 122880;
     static constexpr uint32_t FMT = (KIND == kBF16) ? 1u : 0u;  // bf16 = 1, f16 / e4m3 = 0
@@ -75,11 +78,20 @@ struct Cfg {
     // this (log2 units).  bf16/fp16 P tolerate values up to 2^8; an e4m3 P
     // must keep its largest weight exactly 1, so e4m3 rescales on every growth.
     static constexpr float RESCALE_THRESHOLD = (KIND == kE4M3) ? 0.0f : 8.0f;
+    static_assert(SLOTS >= 2, "K/V ring needs two slots");
+    static_assert(SMEM_USED <= (size_t)kSmemLimit, "shared memory budget");
 };
+
+// TMEM columns: S_A [0,128), S_B [128,256) (P_t overwrites the start of S_t),
+// O_A [256, 256+D), O_B [256+D, 256+2D).
+__device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
+template <int D>
+__device__ __forceinline__ uint32_t col_o(int t) { return 256u + (uint32_t)(D * t); }
 
 struct TcParams {
     int B, H, N_q, N_k;
-    int n_qt;
+    int n_pairs;       // ceil(N_q / 256)
+    int heads_per_group;
     int causal;
     float scale;
     void* o;
@@ -122,7 +134,10 @@ __device__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long lim
     }
 }
 
+// Number of K/V tiles the query tile starting at row q0 needs (0 if the tile
+// is past N_q or every row in it is fully masked).
 __device__ __forceinline__ int kv_tiles_for(int q0, const TcParams& p) {
+    if (q0 >= p.N_q) return 0;
     const int last_row = min(q0 + BM - 1, p.N_q - 1);
     int last_key = p.N_k - 1;
     if (p.causal) last_key = min(last_key, last_row + (p.N_k - p.N_q));
@@ -137,42 +152,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sQ = smem;
-    uint8_t* sKV = smem + C::TILE;
+    uint8_t* sQ = smem;                      // two tiles: A then B
+    uint8_t* sKV = smem + 2 * C::TILE;       // SLOTS tiles
     uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + (size_t)C::SLOTS * C::TILE);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NB);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const uint32_t b_q_full = smem_u32(bars);
-    const uint32_t b_kv_full = smem_u32(bars + 1);                 // + 8 * slot
-    const uint32_t b_kv_empty = smem_u32(bars + 1 + C::SLOTS);     // + 8 * slot
-    const uint32_t b_s_full = smem_u32(bars + 1 + 2 * C::SLOTS);   // + 8 * buf
-    const uint32_t b_s_free = smem_u32(bars + 3 + 2 * C::SLOTS);   // + 8 * buf
-    const uint32_t b_p_full = smem_u32(bars + 5 + 2 * C::SLOTS);
-    const uint32_t b_pv_done = smem_u32(bars + 6 + 2 * C::SLOTS);
-    const uint32_t b_drain = smem_u32(bars + 7 + 2 * C::SLOTS);
+    const uint32_t b_s_full = smem_u32(bars + 1);     // + 8 * tile
+    const uint32_t b_p_full = smem_u32(bars + 3);     // + 8 * tile
+    const uint32_t b_pv_done = smem_u32(bars + 5);    // + 8 * tile
+    const uint32_t b_drain = smem_u32(bars + 7);
+    const uint32_t b_kv_full = smem_u32(bars + 8);                // + 8 * slot
+    const uint32_t b_kv_empty = smem_u32(bars + 8 + C::SLOTS);    // + 8 * slot
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
+
+    // ---- schedule: groups of heads_per_group heads; inside a group the pair
+    // index is the slow coordinate (heaviest causal pair first) and the head
+    // the fast one, so CTAs running together share a few heads' K/V.
+    const long long n_bh = (long long)p.B * p.H;
+    const long long G = p.heads_per_group;
+    const long long per_group = (long long)p.n_pairs * G;
+    const long long n_full = n_bh / G;
+    const long long L = blockIdx.x;
+    long long g, rem, Gg;
+    if (L < n_full * per_group) {
+        g = L / per_group;
+        rem = L % per_group;
+        Gg = G;
+    } else {
+        g = n_full;
+        rem = L - n_full * per_group;
+        Gg = n_bh - n_full * G;
+    }
+    const int rank = (int)(rem / Gg);
+    const int bh = (int)(g * G + rem % Gg);
     const int b = bh / p.H, h = bh % p.H;
-    const int qt = p.causal ? (p.n_qt - 1 - (int)blockIdx.y) : (int)blockIdx.y;
-    const int q0 = qt * BM;
-    const int n_kv = kv_tiles_for(q0, p);
+    const int pair = p.causal ? (p.n_pairs - 1 - rank) : rank;
+    int q0[2], n_kv[2];
+    q0[0] = pair * 2 * BM;
+    q0[1] = q0[0] + BM;
+    n_kv[0] = kv_tiles_for(q0[0], p);
+    n_kv[1] = kv_tiles_for(q0[1], p);
+    const int n_max = max(n_kv[0], n_kv[1]);
     const unsigned long long lim = p.timeout_ns;
 
     if (threadIdx.x == 0) {
         mbar_init(b_q_full, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(b_s_full + 8 * t, 1);
+            mbar_init(b_p_full + 8 * t, 128);
+            mbar_init(b_pv_done + 8 * t, 1);
+        }
+        mbar_init(b_drain, 1);
         for (int s = 0; s < C::SLOTS; ++s) {
             mbar_init(b_kv_full + 8 * s, 1);
             mbar_init(b_kv_empty + 8 * s, 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(b_s_full + 8 * i, 1);
-            mbar_init(b_s_free + 8 * i, 128);
-        }
-        mbar_init(b_p_full, 128);
-        mbar_init(b_pv_done, 1);
-        mbar_init(b_drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -193,33 +230,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0 && n_kv > 0) {
-            mbar_arrive_expect_tx(b_q_full, C::TILE);
-            for (int c = 0; c < C::NC; ++c)
-                tma_load_4d(smem_u32(sQ + c * C::CHUNK), &tmQ, b_q_full, c * (C::CB / C::E), h, q0,
-                            b);
+        if (lane == 0 && n_max > 0) {
+            const int nq = (n_kv[0] > 0) + (n_kv[1] > 0);
+            mbar_arrive_expect_tx(b_q_full, (uint32_t)(nq * C::TILE));
+            for (int t = 0; t < 2; ++t) {
+                if (n_kv[t] == 0) continue;
+                for (int c = 0; c < C::NC; ++c)
+                    tma_load_4d(smem_u32(sQ + t * C::TILE + c * C::CHUNK), &tmQ, b_q_full,
+                                c * (C::CB / C::E), h, q0[t], b);
+            }
+            // item 2j = K_j, item 2j+1 = V_j (the order the MMAs first use them)
             int it = 0;
             bool ok = true;
-            // consumption order: K0, then per j: K_{j+1} (if any), V_j
-            const int n_items = 2 * n_kv;
-            for (int item = 0; item < n_items && ok; ++item) {
-                int tile;
-                const CUtensorMap* tm;
-                if (item == 0) {
-                    tile = 0;
-                    tm = &tmK;
-                } else {
-                    const int j = (item - 1) >> 1;
-                    const bool is_k = ((item - 1) & 1) == 0 && (j + 1 < n_kv);
-                    if (j + 1 < n_kv) {
-                        tile = is_k ? j + 1 : j;
-                        tm = is_k ? &tmK : &tmV;
-                    } else {
-                        // last tile: only V_{n-1} remains (item == 2 n - 1)
-                        tile = n_kv - 1;
-                        tm = &tmV;
-                    }
-                }
+            for (; it < 2 * n_max; ++it) {
                 const int slot = it % C::SLOTS;
                 const uint32_t ph = (uint32_t)(it / C::SLOTS) & 1u;
                 if (!wait_bar(b_kv_empty + 8 * slot, ph ^ 1u, abort_flag, lim)) {
@@ -227,11 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 mbar_arrive_expect_tx(b_kv_full + 8 * slot, C::TILE);
+                const CUtensorMap* tm = (it & 1) ? &tmV : &tmK;
                 uint8_t* dst = sKV + (size_t)slot * C::TILE;
                 for (int c = 0; c < C::NC; ++c)
                     tma_load_4d(smem_u32(dst + c * C::CHUNK), tm, b_kv_full + 8 * slot,
-                                c * (C::CB / C::E), h, tile * BN, b);
-                ++it;
+                                c * (C::CB / C::E), h, (it >> 1) * BN, b);
             }
             if (!ok) {
                 // let every load already issued land before the CTA can exit
@@ -243,11 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ----------------------------------------------------- MMA issuer
-        if (lane == 0 && n_kv > 0) {
-            bool ok = wait_bar(b_q_full, 0, abort_flag, lim);
-            int it = 0;
-            const uint32_t q_base = smem_u32(sQ);
-            auto issue_qk = [&](int buf, int slot) {
+        if (lane == 0 && n_max > 0) {
+            auto issue_qk = [&](int t, int slot) {
+                const uint32_t q_base = smem_u32(sQ + t * C::TILE);
                 const uint32_t k_base = smem_u32(sKV + (size_t)slot * C::TILE);
 #pragma unroll
                 for (int c = 0; c < C::NC; ++c) {
@@ -258,64 +279,75 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t db = smem_desc(k_base + off, 16, 8 * C::CB, C::LAYOUT);
                         const uint32_t acc = (c | ks) != 0;
                         if constexpr (KIND == kE4M3)
-                            mma_f8_ss(tmem + kColS0 + 128u * buf, da, db, C::IDESC_QK, acc);
+                            mma_f8_ss(tmem + col_s(t), da, db, C::IDESC_QK, acc);
                         else
-                            mma_f16_ss(tmem + kColS0 + 128u * buf, da, db, C::IDESC_QK, acc);
+                            mma_f16_ss(tmem + col_s(t), da, db, C::IDESC_QK, acc);
                     }
                 }
             };
-            auto issue_pv = [&](int slot, bool first) {
+            auto issue_pv = [&](int t, int slot, bool first) {
                 const uint32_t v_base = smem_u32(sKV + (size_t)slot * C::TILE);
 #pragma unroll
                 for (int ks = 0; ks < BN / C::MMA_K; ++ks) {
                     // V is MN-major: 8-key groups 8*CB apart, d-chunks CHUNK apart
                     const uint64_t db = smem_desc(v_base + ks * C::MMA_K * C::CB, C::CHUNK,
                                                   8 * C::CB, C::LAYOUT);
-                    const uint32_t a_tmem = tmem + kColP + ks * (C::MMA_K * C::E / 4);
+                    const uint32_t a_tmem = tmem + col_s(t) + ks * (C::MMA_K * C::E / 4);
                     const uint32_t acc = (!first || ks > 0) ? 1u : 0u;
                     if constexpr (KIND == kE4M3)
-                        mma_f8_ts(tmem + kColO, a_tmem, db, C::IDESC_PV, acc);
+                        mma_f8_ts(tmem + col_o<D>(t), a_tmem, db, C::IDESC_PV, acc);
                     else
-                        mma_f16_ts(tmem + kColO, a_tmem, db, C::IDESC_PV, acc);
+                        mma_f16_ts(tmem + col_o<D>(t), a_tmem, db, C::IDESC_PV, acc);
                 }
             };
+            auto slot_of = [](int it) { return it % C::SLOTS; };
+            auto par_of = [](int it) { return (uint32_t)(it / C::SLOTS) & 1u; };
+
+            bool ok = wait_bar(b_q_full, 0, abort_flag, lim);
+            if (ok) ok = wait_bar(b_kv_full + 8 * slot_of(0), par_of(0), abort_flag, lim);
             if (ok) {
-                // S_0 = Q K_0^T
-                ok = wait_bar(b_kv_full, 0, abort_flag, lim);
-                if (ok) {
-                    tc_fence_after();
-                    issue_qk(0, 0);
-                    mma_commit(b_kv_empty);
-                    mma_commit(b_s_full);
-                    it = 1;
-                }
-            }
-            for (int j = 0; j < n_kv && ok; ++j) {
-                if (j + 1 < n_kv) {
-                    const int slot = it % C::SLOTS;
-                    const int jj = j + 1, buf = jj & 1;
-                    ok = wait_bar(b_kv_full + 8 * slot, (uint32_t)(it / C::SLOTS) & 1u, abort_flag,
-                                  lim);
-                    if (ok && jj >= 2)
-                        ok = wait_bar(b_s_free + 8 * buf, (uint32_t)((jj >> 1) - 1) & 1u,
-                                      abort_flag, lim);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_qk(buf, slot);
-                    mma_commit(b_kv_empty + 8 * slot);
-                    mma_commit(b_s_full + 8 * buf);
-                    ++it;
-                }
-                ok = wait_bar(b_p_full, (uint32_t)j & 1u, abort_flag, lim);
-                if (!ok) break;
-                const int slot = it % C::SLOTS;
-                ok = wait_bar(b_kv_full + 8 * slot, (uint32_t)(it / C::SLOTS) & 1u, abort_flag, lim);
-                if (!ok) break;
                 tc_fence_after();
-                issue_pv(slot, j == 0);
-                if (j + 1 < n_kv) mma_commit(b_kv_empty + 8 * slot);
-                mma_commit(b_pv_done);
-                ++it;
+                for (int t = 0; t < 2; ++t) {
+                    if (n_kv[t] == 0) continue;
+                    issue_qk(t, slot_of(0));
+                    mma_commit(b_s_full + 8 * t);
+                }
+                mma_commit(b_kv_empty + 8 * slot_of(0));
+            }
+            for (int j = 0; j < n_max && ok; ++j) {
+                const int itV = 2 * j + 1, itK = 2 * j + 2;
+                ok = wait_bar(b_kv_full + 8 * slot_of(itV), par_of(itV), abort_flag, lim);
+                bool k_ready = false;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j < n_kv[t]) {
+                        ok = wait_bar(b_p_full + 8 * t, (uint32_t)j & 1u, abort_flag, lim);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(t, slot_of(itV), j == 0);
+                        mma_commit(b_pv_done + 8 * t);
+                    }
+                    if (j + 1 < n_kv[t]) {
+                        if (!k_ready) {
+                            ok = wait_bar(b_kv_full + 8 * slot_of(itK), par_of(itK), abort_flag,
+                                          lim);
+                            k_ready = true;
+                        }
+                        // P_t lives in S_t's columns: the P V MMA must be done
+                        // reading it before the next S_t is written
+                        if (ok) ok = wait_bar(b_pv_done + 8 * t, (uint32_t)j & 1u, abort_flag, lim);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_qk(t, slot_of(itK));
+                        mma_commit(b_s_full + 8 * t);
+                    }
+                }
+                if (!ok) break;
+                // release V_j (every P V of it is issued) and K_{j+1}; the last
+                // V's release is not needed (nothing is loaded after it)
+                if (j + 1 < n_max) {
+                    mma_commit(b_kv_empty + 8 * slot_of(itV));
+                    mma_commit(b_kv_empty + 8 * slot_of(itK));
+                }
             }
             if (!ok) {
                 // make sure no MMA is still reading or writing when TMEM is freed
@@ -325,15 +357,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------- softmax + epilogue (128 thr)
-        const int quad = warp & 3;
+        // --------------------------------------- softmax + epilogue (2 x 128 thr)
+        const int t = (warp - 2) >> 2;       // tile of this warp group
+        const int quad = warp & 3;           // TMEM lane quadrant this warp may access
         const int r = quad * 32 + lane;
-        const int row_g = q0 + r;
+        const int row_g = q0[t] + r;
+        const int nt = n_kv[t];
         const uint32_t t_row = tmem + ((uint32_t)(quad * 32) << 16);
+        const uint32_t s_full = b_s_full + 8 * t, p_full = b_p_full + 8 * t;
+        const uint32_t pv_done = b_pv_done + 8 * t;
         const int shift = p.N_k - p.N_q;
         int row_lim = p.N_k - 1;  // last allowed key of this row
         if (p.causal) row_lim = min(row_lim, row_g + shift);
-        const int tile_lim = p.causal ? min(p.N_k - 1, q0 + shift) : p.N_k - 1;  // row 0's
+        // tiles with any column beyond the tile's first row's limit need a mask
+        const int tile_lim = p.causal ? min(p.N_k - 1, q0[t] + shift) : p.N_k - 1;
         float dq = 1.f, dk = 1.f, dv = 1.f;
         if (KIND == kE4M3) {
             if (p.q_descale) dq = p.q_descale[bh];
@@ -344,28 +381,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
 
-        for (int j = 0; j < n_kv; ++j) {
-            const int buf = j & 1;
-            if (!__all_sync(0xffffffffu,
-                            wait_bar(b_s_full + 8 * buf, (uint32_t)(j >> 1) & 1u, abort_flag, lim))) {
+        for (int j = 0; j < nt; ++j) {
+            if (!__all_sync(0xffffffffu, wait_bar(s_full, (uint32_t)j & 1u, abort_flag, lim))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            // all four 32-column loads in flight before one wait
+            uint32_t sr[BN];
+#pragma unroll
+            for (int u = 0; u < BN / 32; ++u)
+                tmem_ld32(t_row + col_s(t) + 32 * u,
+                          *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * u]));
+            tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < BN / 32; ++u)
+                reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[32 * u]));
             float s[BN];
-            {
-                uint32_t rr[32];
 #pragma unroll
-                for (int u = 0; u < BN / 32; ++u) {
-                    tmem_ld32(t_row + kColS0 + 128u * buf + 32 * u, rr);
-                    tmem_ld_wait();
-                    reg_fence32(rr);
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) s[32 * u + x] = __uint_as_float(rr[x]);
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(b_s_free + 8 * buf);
+            for (int x = 0; x < BN; ++x) s[x] = __uint_as_float(sr[x]);
 
             const int kbase = j * BN;
             if (kbase + BN - 1 > tile_lim) {
@@ -374,9 +408,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int x = 0; x < BN; ++x)
                     if (x > cl) s[x] = -INFINITY;
             }
-            float mx = s[0];
+            // row maximum: 8 independent 3-input-max chains, then a small tree
+            float mc[8];
 #pragma unroll
-            for (int x = 1; x < BN; ++x) mx = fmaxf(mx, s[x]);
+            for (int k = 0; k < 8; ++k) mc[k] = fmaxf(s[k], s[k + 8]);
+#pragma unroll
+            for (int x = 16; x < BN; x += 16) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mc[k] = max3(mc[k], s[x + k], s[x + k + 8]);
+            }
+            const float mx = max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]),
+                                  fmaxf(mc[6], mc[7]));
             const float m_new = mx * c;
             const bool need = m_new > m_used + C::RESCALE_THRESHOLD;
             const bool any = __any_sync(0xffffffffu, need);
@@ -387,32 +429,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_used = mu;
             }
             const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
-            uint32_t pk[C::P_COLS];
-            float sum = 0.f;
-            if constexpr (KIND == kE4M3) {
+            float sc[8];  // independent partial row sums
 #pragma unroll
-                for (int x = 0; x < BN; x += 4) {
-                    const float p0 = ex2(fmaf(s[x], c, -m_ref));
-                    const float p1 = ex2(fmaf(s[x + 1], c, -m_ref));
-                    const float p2 = ex2(fmaf(s[x + 2], c, -m_ref));
-                    const float p3 = ex2(fmaf(s[x + 3], c, -m_ref));
-                    sum += (p0 + p1) + (p2 + p3);
-                    pk[x / 4] = pack_e4m3(p0, p1, p2, p3);
-                }
-            } else {
+            for (int k = 0; k < 8; ++k) sc[k] = 0.f;
+            // P_t goes over the first P_COLS columns of S_t (already read above;
+            // the previous P_t V MMA completed before this S_t was written), 32
+            // columns at a time so only one chunk of packed P is live
+            constexpr int PER_CHUNK = 32 * 4 / C::E;  // score columns per 32 TMEM columns
 #pragma unroll
-                for (int x = 0; x < BN; x += 2) {
-                    const float p0 = ex2(fmaf(s[x], c, -m_ref));
-                    const float p1 = ex2(fmaf(s[x + 1], c, -m_ref));
-                    sum += p0 + p1;
-                    pk[x / 2] = (KIND == kBF16) ? pack_bf16(p0, p1) : pack_f16(p0, p1);
+            for (int u = 0; u < (int)C::P_COLS / 32; ++u) {
+                uint32_t pk[32];
+                if constexpr (KIND == kE4M3) {
+#pragma unroll
+                    for (int x = 0; x < PER_CHUNK; x += 4) {
+                        const int y = u * PER_CHUNK + x;
+                        const float p0 = ex2(fmaf(s[y], c, -m_ref));
+                        const float p1 = ex2(fmaf(s[y + 1], c, -m_ref));
+                        const float p2 = ex2(fmaf(s[y + 2], c, -m_ref));
+                        const float p3 = ex2(fmaf(s[y + 3], c, -m_ref));
+                        sc[(x / 4) & 7] += (p0 + p1) + (p2 + p3);
+                        pk[x / 4] = pack_e4m3(p0, p1, p2, p3);
+                    }
+                } else {
+#pragma unroll
+                    for (int x = 0; x < PER_CHUNK; x += 2) {
+                        const int y = u * PER_CHUNK + x;
+                        const float p0 = ex2(fmaf(s[y], c, -m_ref));
+                        const float p1 = ex2(fmaf(s[y + 1], c, -m_ref));
+                        sc[(x / 2) & 7] += p0 + p1;
+                        pk[x / 2] = (KIND == kBF16) ? pack_bf16(p0, p1) : pack_f16(p0, p1);
+                    }
                 }
+                tmem_st32(t_row + col_s(t) + 32 * u, pk);
             }
+            const float sum =
+                ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));
             l = l * alpha + sum;
 
             if (j > 0) {
+                // O_t is stable once P_{j-1} V_{j-1} has completed
                 if (!__all_sync(0xffffffffu,
-                                wait_bar(b_pv_done, (uint32_t)(j - 1) & 1u, abort_flag, lim))) {
+                                wait_bar(pv_done, (uint32_t)(j - 1) & 1u, abort_flag, lim))) {
                     ok = false;
                     break;
                 }
@@ -421,31 +478,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t oo[32];
 #pragma unroll
                     for (int u = 0; u < D / 32; ++u) {
-                        tmem_ld32(t_row + kColO + 32 * u, oo);
+                        tmem_ld32(t_row + col_o<D>(t) + 32 * u, oo);
                         tmem_ld_wait();
                         reg_fence32(oo);
 #pragma unroll
                         for (int x = 0; x < 32; ++x)
                             oo[x] = __float_as_uint(__uint_as_float(oo[x]) * alpha);
-                        tmem_st32(t_row + kColO + 32 * u, oo);
+                        tmem_st32(t_row + col_o<D>(t) + 32 * u, oo);
                     }
                 }
             }
-#pragma unroll
-            for (int u = 0; u < (int)C::P_COLS / 32; ++u) {
-                uint32_t pp[32];
-#pragma unroll
-                for (int x = 0; x < 32; ++x) pp[x] = pk[32 * u + x];
-                tmem_st32(t_row + kColP + 32 * u, pp);
-            }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(b_p_full);
+            mbar_arrive(p_full);
         }
 
-        if (ok && n_kv > 0)
-            ok = __all_sync(0xffffffffu,
-                            wait_bar(b_pv_done, (uint32_t)(n_kv - 1) & 1u, abort_flag, lim));
+        if (ok && nt > 0)
+            ok = __all_sync(0xffffffffu, wait_bar(pv_done, (uint32_t)(nt - 1) & 1u, abort_flag, lim));
         if (ok) {
             tc_fence_after();
             const bool valid = row_g < p.N_q;
@@ -456,8 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < D / 32; ++u) {
                 uint32_t oo[32];
-                if (n_kv > 0) {
-                    tmem_ld32(t_row + kColO + 32 * u, oo);
+                if (nt > 0) {
+                    tmem_ld32(t_row + col_o<D>(t) + 32 * u, oo);
                     tmem_ld_wait();
                     reg_fence32(oo);
                 } else {
@@ -552,7 +601,7 @@ cudaError_t launch_t(const Problem& pr, cudaStream_t stream) {
     p.H = pr.H;
     p.N_q = pr.N_q;
     p.N_k = pr.N_k;
-    p.n_qt = (pr.N_q + BM - 1) / BM;
+    p.n_pairs = (pr.N_q + 2 * BM - 1) / (2 * BM);
     p.causal = pr.causal;
     p.scale = pr.scale;
     p.o = pr.o;
@@ -561,11 +610,19 @@ cudaError_t launch_t(const Problem& pr, cudaStream_t stream) {
     p.k_descale = pr.k_descale;
     p.v_descale = pr.v_descale;
     p.timeout_ns = 2000000000ull;
-    if (p.n_qt > 65535) return cudaErrorNotSupported;
+    const long long n_bh = (long long)pr.B * pr.H;
+    // heads scheduled together: their K/V (2 N_k d E bytes each) fill ~48 MiB of L2
+    const long long kv_bytes = 2LL * (pr.N_k > 0 ? pr.N_k : 1) * D * C::E;
+    long long G = (48LL << 20) / kv_bytes;
+    if (G < 1) G = 1;
+    if (G > n_bh) G = n_bh;
+    p.heads_per_group = (int)G;
+    const long long n_cta = (long long)p.n_pairs * n_bh;
+    if (n_cta > 0x7fffffffLL) return cudaErrorNotSupported;
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, KIND>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)(pr.B * pr.H), (unsigned)p.n_qt);
+    dim3 grid((unsigned)n_cta);
     attn_tc_kernel<D, KIND><<<grid, kThreads, C::SMEM, stream>>>(mq, mk, mv, p);
     return cudaGetLastError();
 }
@@ -573,7 +630,6 @@ cudaError_t launch_t(const Problem& pr, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_tc(const Problem& p, cudaStream_t stream) {
-    if ((long long)p.B * p.H > 0x7fffffffLL) return cudaErrorNotSupported;
     switch (p.dtype) {
         case kBF16:
             if (p.d == 64) return launch_t<64, kBF16>(p, stream);
