@@ -15,7 +15,8 @@
 //   * warp 1 (one thread) issues the tcgen05 MMAs and owns TMEM:
 //     S_t = Q_t K_j^T into the TMEM score buffer of tile t, and
 //     O_t += P_t V_j with P_t read from TMEM (P overwrites its own S buffer;
-//     the next S_t is issued only after that P V MMA has completed);
+//     the next S_t MMA is issued right behind that P V MMA: one thread's
+//     MMAs execute in issue order);
 //   * warps 2-5 (tile A) and 6-9 (tile B), one query row per thread, run the
 //     online softmax: TMEM -> registers, causal / ragged mask on the tiles that
 //     need it, row maximum, exp2, row sum, P back to TMEM as bf16 / fp16 /
@@ -314,6 +315,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(b_kv_empty + 8 * slot_of(0));
             }
+            // Per tile: O_t += P_t V_j, then at once S_t = Q_t K_{j+1}^T into the
+            // same TMEM columns.  One thread's tcgen05.mma operations execute in
+            // issue order, so the P V MMA has read P_t before the next score
+            // MMA overwrites it; no completion wait is needed in between.
+            // While softmax A works, the tensor core runs tile B's pair of MMAs
+            // and the other way round.
             for (int j = 0; j < n_max && ok; ++j) {
                 const int itV = 2 * j + 1, itK = 2 * j + 2;
                 ok = wait_bar(b_kv_full + 8 * slot_of(itV), par_of(itV), abort_flag, lim);
@@ -332,9 +339,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           lim);
                             k_ready = true;
                         }
-                        // P_t lives in S_t's columns: the P V MMA must be done
-                        // reading it before the next S_t is written
-                        if (ok) ok = wait_bar(b_pv_done + 8 * t, (uint32_t)j & 1u, abort_flag, lim);
                         if (!ok) break;
                         tc_fence_after();
                         issue_qk(t, slot_of(itK));
