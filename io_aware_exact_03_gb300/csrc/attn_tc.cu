@@ -433,12 +433,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_used = mu;
             }
             const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
-            float sc[8];  // independent partial row sums
+            float sc[8];  // independent partial row sums (four packed pairs)
 #pragma unroll
             for (int k = 0; k < 8; ++k) sc[k] = 0.f;
             // P_t goes over the first P_COLS columns of S_t (already read above;
-            // the previous P_t V MMA completed before this S_t was written), 32
-            // columns at a time so only one chunk of packed P is live
+            // the previous P_t V MMA read P before this S_t was written), 32
+            // columns at a time so only one chunk of packed P is live.  The
+            // scale-and-subtract and the sums use packed f32x2 instructions:
+            // this loop is bound by instruction issue, not by ex2 throughput.
             constexpr int PER_CHUNK = 32 * 4 / C::E;  // score columns per 32 TMEM columns
 #pragma unroll
             for (int u = 0; u < (int)C::P_COLS / 32; ++u) {
@@ -447,20 +449,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int x = 0; x < PER_CHUNK; x += 4) {
                         const int y = u * PER_CHUNK + x;
-                        const float p0 = ex2(fmaf(s[y], c, -m_ref));
-                        const float p1 = ex2(fmaf(s[y + 1], c, -m_ref));
-                        const float p2 = ex2(fmaf(s[y + 2], c, -m_ref));
-                        const float p3 = ex2(fmaf(s[y + 3], c, -m_ref));
-                        sc[(x / 4) & 7] += (p0 + p1) + (p2 + p3);
+                        float a0, a1, a2, a3;
+                        ffma2(a0, a1, s[y], s[y + 1], c, c, -m_ref, -m_ref);
+                        ffma2(a2, a3, s[y + 2], s[y + 3], c, c, -m_ref, -m_ref);
+                        const float p0 = ex2(a0), p1 = ex2(a1), p2 = ex2(a2), p3 = ex2(a3);
+                        const int k = ((x / 4) & 3) * 2;
+                        fadd2(sc[k], sc[k + 1], sc[k], sc[k + 1], p0, p1);
+                        fadd2(sc[k], sc[k + 1], sc[k], sc[k + 1], p2, p3);
                         pk[x / 4] = pack_e4m3(p0, p1, p2, p3);
                     }
                 } else {
 #pragma unroll
                     for (int x = 0; x < PER_CHUNK; x += 2) {
                         const int y = u * PER_CHUNK + x;
-                        const float p0 = ex2(fmaf(s[y], c, -m_ref));
-                        const float p1 = ex2(fmaf(s[y + 1], c, -m_ref));
-                        sc[(x / 2) & 7] += p0 + p1;
+                        float a0, a1;
+                        ffma2(a0, a1, s[y], s[y + 1], c, c, -m_ref, -m_ref);
+                        const float p0 = ex2(a0), p1 = ex2(a1);
+                        const int k = ((x / 2) & 3) * 2;
+                        fadd2(sc[k], sc[k + 1], sc[k], sc[k + 1], p0, p1);
                         pk[x / 2] = (KIND == kBF16) ? pack_bf16(p0, p1) : pack_f16(p0, p1);
                     }
                 }
@@ -470,26 +476,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));
             l = l * alpha + sum;
 
-            if (j > 0) {
-                // O_t is stable once P_{j-1} V_{j-1} has completed
+            if (any && j > 0) {
+                // O_t is touched only to rescale it; it is stable once
+                // P_{j-1} V_{j-1} has completed
                 if (!__all_sync(0xffffffffu,
                                 wait_bar(pv_done, (uint32_t)(j - 1) & 1u, abort_flag, lim))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (any) {
-                    uint32_t oo[32];
+                uint32_t oo[32];
 #pragma unroll
-                    for (int u = 0; u < D / 32; ++u) {
-                        tmem_ld32(t_row + col_o<D>(t) + 32 * u, oo);
-                        tmem_ld_wait();
-                        reg_fence32(oo);
+                for (int u = 0; u < D / 32; ++u) {
+                    tmem_ld32(t_row + col_o<D>(t) + 32 * u, oo);
+                    tmem_ld_wait();
+                    reg_fence32(oo);
 #pragma unroll
-                        for (int x = 0; x < 32; ++x)
-                            oo[x] = __float_as_uint(__uint_as_float(oo[x]) * alpha);
-                        tmem_st32(t_row + col_o<D>(t) + 32 * u, oo);
+                    for (int x = 0; x < 32; x += 2) {
+                        float a0 = __uint_as_float(oo[x]), a1 = __uint_as_float(oo[x + 1]);
+                        ffma2(a0, a1, a0, a1, alpha, alpha, 0.f, 0.f);
+                        oo[x] = __float_as_uint(a0);
+                        oo[x + 1] = __float_as_uint(a1);
                     }
+                    tmem_st32(t_row + col_o<D>(t) + 32 * u, oo);
                 }
             }
             tmem_st_wait();
