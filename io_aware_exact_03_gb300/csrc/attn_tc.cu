@@ -485,20 +485,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                uint32_t oo[32];
+                // 64 columns per load round: two loads in flight per wait
 #pragma unroll
-                for (int u = 0; u < D / 32; ++u) {
-                    tmem_ld32(t_row + col_o<D>(t) + 32 * u, oo);
+                for (int u = 0; u < D / 64; ++u) {
+                    uint32_t oo[64];
+                    const uint32_t ta = t_row + col_o<D>(t) + 64 * u;
+                    tmem_ld32(ta, *reinterpret_cast<uint32_t(*)[32]>(&oo[0]));
+                    tmem_ld32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(&oo[32]));
                     tmem_ld_wait();
-                    reg_fence32(oo);
+                    reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&oo[0]));
+                    reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&oo[32]));
 #pragma unroll
-                    for (int x = 0; x < 32; x += 2) {
+                    for (int x = 0; x < 64; x += 2) {
                         float a0 = __uint_as_float(oo[x]), a1 = __uint_as_float(oo[x + 1]);
                         ffma2(a0, a1, a0, a1, alpha, alpha, 0.f, 0.f);
                         oo[x] = __float_as_uint(a0);
                         oo[x + 1] = __float_as_uint(a1);
                     }
-                    tmem_st32(t_row + col_o<D>(t) + 32 * u, oo);
+                    tmem_st32(ta, *reinterpret_cast<const uint32_t(*)[32]>(&oo[0]));
+                    tmem_st32(ta + 32, *reinterpret_cast<const uint32_t(*)[32]>(&oo[32]));
                 }
             }
             tmem_st_wait();
