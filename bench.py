@@ -54,19 +54,26 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--case", choices=["C1", "C2", "C3", "C4", "C5"], default=None,
+    ap.add_argument("--case", choices=["C1", "C2", "C3", "C4", "C5", "LKV"], default=None,
                     help="measure one workload case alone instead of the C4 + C5 step")
+    ap.add_argument("--splits", type=int, default=1,
+                    help="with --case: split each query tile's K/V range over this many CTAs")
     return ap.parse_args()
 
 
 def workload(args):
     """(case names, description) of one step."""
     if args.case:
-        import synthetic
-        c = synthetic.CASES[args.case]
+        c = case_by_name(args.case)
+        sp = f", split-KV over {args.splits} CTAs" if args.splits > 1 else ""
         return (args.case,), (f"{c.name} {c.dtype} {'causal' if c.causal else 'non-causal'} "
-                              f"B{c.B} H{c.H} N_q{c.N_q} N_k{c.N_k} d{c.d}; one attention call per step")
+                              f"B{c.B} H{c.H} N_q{c.N_q} N_k{c.N_k} d{c.d}{sp}; one attention call per step")
     return WORKLOAD, WORKLOAD_DESC
+
+
+def case_by_name(name):
+    import synthetic
+    return synthetic.CASES.get(name) or synthetic.EXTRA_CASES[name]
 
 
 def env_rank():
@@ -169,7 +176,7 @@ def oracle_rows_rate(counts, seed):
     flops = 0.0
     secs = 0.0
     for j, (name, n) in enumerate(counts.items()):
-        case = synthetic.CASES[name]
+        case = case_by_name(name)
         q, k, v = _f64_inputs(name)
         rows = synthetic.sample_rows(case, n, seed=seed + 7 * j)
         keys = np.array([_allowed(case, int(i)) for i in rows[:, 2]], dtype=np.float64)
@@ -187,7 +194,7 @@ def _f64_inputs(name):
     if name not in _F64:
         import oracle
         import synthetic
-        _F64[name] = oracle.case_inputs_f64(synthetic.make_inputs(synthetic.CASES[name]))
+        _F64[name] = oracle.case_inputs_f64(synthetic.make_inputs(case_by_name(name)))
     return _F64[name]
 
 
@@ -227,7 +234,7 @@ def run_ours(args):
     attn.lib()
 
     names, desc = workload(args)
-    cases = [synthetic.CASES[n] for n in names]
+    cases = [case_by_name(n) for n in names]
     host, dev, outs = [], [], []
     for c in cases:
         c_r = dataclasses.replace(c, seed=c.seed + 100 * rank)
@@ -238,11 +245,20 @@ def run_ours(args):
         outs.append((torch.empty((c.B, c.N_q, c.H, c.d), dtype=out_dtype, device="cuda"),
                      torch.empty((c.B, c.H, c.N_q), dtype=torch.float32, device="cuda")))
     stream = torch.cuda.current_stream()
+    ws = None
+    if args.splits > 1:
+        need = max(attn.attn_splitkv_workspace_bytes(c.B, c.H, c.N_q, c.d, args.splits) for c in cases)
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
 
     def call(i, d):
         c = cases[i]
         o, lse = outs[i]
-        if c.dtype == "e4m3":
+        if args.splits > 1:
+            attn.attn_fwd_splitkv(d["q"], d["k"], d["v"], args.splits, o=o, lse=lse,
+                                  scale=c.scale, causal=c.causal, q_descale=d.get("q_descale"),
+                                  k_descale=d.get("k_descale"), v_descale=d.get("v_descale"),
+                                  workspace=ws, stream=stream)
+        elif c.dtype == "e4m3":
             attn.attn_fwd_fp8(d["q"], d["k"], d["v"], d["q_descale"], d["k_descale"],
                               d["v_descale"], o=o, lse=lse, scale=c.scale, causal=c.causal,
                               stream=stream)

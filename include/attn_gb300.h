@@ -49,6 +49,8 @@
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H
 
+#include <stddef.h>
+
 #if defined(__GNUC__)
 #define ATTN_API __attribute__((visibility("default")))
 #else
@@ -95,6 +97,33 @@ ATTN_API attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v
                             const float* v_descale,
                             int B, int H, int N_q, int N_k, int d, float scale, int causal,
                             attn_dtype_t dtype, void* stream);
+
+/* Split-KV forward pass (the same operation as attn_fwd / attn_fwd_fp8).  Each
+ * 256-row query-tile pair's K/V range is cut into num_splits contiguous parts
+ * processed by separate CTAs, which adds parallelism when B*H*N_q is small and
+ * N_k is long ("FlashAttention-2 (BN)" page, section "Improved parallelism":
+ * spreading one head's work over more SMs).  Each part writes its partial
+ * output, normalised by its own row sum, and its log-sum-exp to `workspace`;
+ * a second kernel merges the parts exactly:
+ *   lse = ln sum_s exp(lse_s),   o = sum_s exp(lse_s - lse) * o_s.
+ * num_splits: 1..32 (1 = the plain tensor-core kernel, workspace unused).
+ * workspace: caller-allocated device memory of at least
+ *   attn_splitkv_workspace_bytes(B, H, N_q, d, num_splits) bytes, 16-byte
+ *   aligned; it is overwritten (layout: fp32 partial outputs
+ *   [num_splits][B*H][N_q][d], then fp32 partial lse [num_splits][B*H][N_q]).
+ * Descales: as attn_fwd_simt (NULL = unit; used for ATTN_FP8_E4M3 only).
+ * Errors as attn_fwd, plus ATTN_ERR_INVALID_ARG for num_splits out of range or
+ * a missing, misaligned or too small workspace. */
+ATTN_API attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o,
+                                        float* lse, const float* q_descale,
+                                        const float* k_descale, const float* v_descale, int B,
+                                        int H, int N_q, int N_k, int d, float scale, int causal,
+                                        attn_dtype_t dtype, int num_splits, void* workspace,
+                                        size_t workspace_bytes, void* stream);
+
+/* Workspace bytes attn_fwd_splitkv needs (0 for num_splits == 1 or invalid
+ * arguments). */
+ATTN_API size_t attn_splitkv_workspace_bytes(int B, int H, int N_q, int d, int num_splits);
 
 /* Synchronises `stream`, then returns and clears the device status word:
  * ATTN_ERR_TIMEOUT if a bounded wait inside a kernel ran out since the last

@@ -20,8 +20,9 @@ import os
 
 from . import ext_build as _build
 
-__all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_simt", "attn_check_status",
-           "attn_status_string", "AttnError", "lib", "build"]
+__all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_simt", "attn_fwd_splitkv",
+           "attn_splitkv_workspace_bytes", "attn_check_status", "attn_status_string",
+           "AttnError", "lib", "build"]
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
 ATTN_BF16, ATTN_FP16, ATTN_FP8_E4M3 = range(3)
@@ -57,6 +58,12 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd_fp8.restype = i
         L.attn_fwd_simt.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, i, i, i, i, i, f, i, i, vp]
         L.attn_fwd_simt.restype = i
+        sz = ctypes.c_size_t
+        L.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, i, i, i, i, i, f, i, i, i,
+                                       vp, sz, vp]
+        L.attn_fwd_splitkv.restype = i
+        L.attn_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
+        L.attn_splitkv_workspace_bytes.restype = sz
         L.attn_check_status.argtypes = [vp]
         L.attn_check_status.restype = i
         L.attn_status_string.argtypes = [i]
@@ -178,6 +185,29 @@ def attn_fwd_simt(q, k, v, o=None, lse=None, scale=None, causal=False, q_descale
                              _ptr(k_descale), _ptr(v_descale), B, H, N_q, N_k, d, scale,
                              int(bool(causal)), _dtype_code(q), _stream(stream, q.device))
     _raise(st, "attn_fwd_simt")
+    return o, lse
+
+
+def attn_splitkv_workspace_bytes(B, H, N_q, d, num_splits) -> int:
+    return int(lib().attn_splitkv_workspace_bytes(B, H, N_q, d, num_splits))
+
+
+def attn_fwd_splitkv(q, k, v, num_splits, o=None, lse=None, scale=None, causal=False,
+                     q_descale=None, k_descale=None, v_descale=None, workspace=None,
+                     stream=None):
+    """Split-KV tensor-core forward pass; the workspace is allocated when not given."""
+    B, N_q, H, d, N_k = _check_inputs(q, k, v)
+    o, lse = _outputs(q, o, lse, B, N_q, H, d)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    need = attn_splitkv_workspace_bytes(B, H, N_q, d, num_splits)
+    if workspace is None and need > 0:
+        workspace = _torch().empty(need, dtype=_torch().uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().attn_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(q_descale),
+                                _ptr(k_descale), _ptr(v_descale), B, H, N_q, N_k, d, scale,
+                                int(bool(causal)), _dtype_code(q), int(num_splits),
+                                _ptr(workspace), ws_bytes, _stream(stream, q.device))
+    _raise(st, "attn_fwd_splitkv")
     return o, lse
 
 

@@ -108,6 +108,39 @@ attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o
     return from_cuda(e);
 }
 
+size_t attn_splitkv_workspace_bytes(int B, int H, int N_q, int d, int num_splits) {
+    if (B < 0 || H < 0 || N_q < 0 || (d != 64 && d != 128) || num_splits < 1 ||
+        num_splits > attn::kMaxSplits)
+        return 0;
+    if (num_splits == 1) return 0;
+    return attn::splitkv_workspace_bytes(B, H, N_q, d, num_splits);
+}
+
+attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                               const float* q_descale, const float* k_descale,
+                               const float* v_descale, int B, int H, int N_q, int N_k, int d,
+                               float scale, int causal, attn_dtype_t dtype, int num_splits,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+    attn::Problem p = make_problem(q, k, v, o, lse, q_descale, k_descale, v_descale, B, H, N_q,
+                                   N_k, d, scale, causal, (int)dtype);
+    attn_status_t st = validate(p);
+    if (st != ATTN_OK) return st;
+    if (num_splits < 1 || num_splits > attn::kMaxSplits) return ATTN_ERR_INVALID_ARG;
+    if (is_empty(p)) return ATTN_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (num_splits == 1) {
+        e = attn::launch_tc(p, s);
+    } else {
+        if (!workspace || !aligned(workspace, 16) ||
+            workspace_bytes < attn::splitkv_workspace_bytes(B, H, N_q, d, num_splits))
+            return ATTN_ERR_INVALID_ARG;
+        e = attn::launch_tc_splitkv(p, num_splits, workspace, workspace_bytes, s);
+    }
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    return from_cuda(e);
+}
+
 attn_status_t attn_check_status(void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaStreamSynchronize(s);

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 namespace attn {
@@ -34,5 +35,11 @@ cudaError_t simt_take_status(unsigned* out, cudaStream_t stream);
 // it does not take.
 cudaError_t launch_tc(const Problem& p, cudaStream_t stream);
 cudaError_t tc_take_status(unsigned* out, cudaStream_t stream);
+
+// Split-KV on the tensor-core kernel plus the combine kernel (attn_tc.cu).
+constexpr int kMaxSplits = 32;
+size_t splitkv_workspace_bytes(long long B, long long H, long long N_q, int d, int n_splits);
+cudaError_t launch_tc_splitkv(const Problem& p, int n_splits, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
 
 }  // namespace attn

@@ -101,6 +101,11 @@ struct TcParams {
     const float* k_descale;
     const float* v_descale;
     unsigned long long timeout_ns;
+    // split-KV: grid.y = n_splits CTAs share one query-tile pair's K/V range;
+    // each writes its partial (O normalised within the split, fp32) and lse
+    int n_splits;
+    float* part_o;    // [n_splits][B*H][N_q][D]
+    float* part_lse;  // [n_splits][B*H][N_q]
 };
 
 // Bounded wait on an mbarrier phase.  Returns false (after flagging) when the
@@ -196,6 +201,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     q0[1] = q0[0] + BM;
     n_kv[0] = kv_tiles_for(q0[0], p);
     n_kv[1] = kv_tiles_for(q0[1], p);
+    // Split-KV: this CTA takes K/V tiles [j0, j1) of the pair's range; the loops
+    // below count tiles from 0 and only the tile coordinates add j0.
+    int j0 = 0;
+    if (p.n_splits > 1) {
+        const int n_all = max(n_kv[0], n_kv[1]);
+        const int per = (n_all + p.n_splits - 1) / p.n_splits;
+        j0 = min(n_all, (int)blockIdx.y * per);
+        const int j1 = min(n_all, j0 + per);
+        n_kv[0] = max(0, min(j1, n_kv[0]) - j0);
+        n_kv[1] = max(0, min(j1, n_kv[1]) - j0);
+    }
     const int n_max = max(n_kv[0], n_kv[1]);
     const unsigned long long lim = p.timeout_ns;
 
@@ -255,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* dst = sKV + (size_t)slot * C::TILE;
                 for (int c = 0; c < C::NC; ++c)
                     tma_load_4d(smem_u32(dst + c * C::CHUNK), tm, b_kv_full + 8 * slot,
-                                c * (C::CB / C::E), h, (it >> 1) * BN, b);
+                                c * (C::CB / C::E), h, (j0 + (it >> 1)) * BN, b);
             }
             if (!ok) {
                 // let every load already issued land before the CTA can exit
@@ -405,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int x = 0; x < BN; ++x) s[x] = __uint_as_float(sr[x]);
 
-            const int kbase = j * BN;
+            const int kbase = (j0 + j) * BN;
             if (kbase + BN - 1 > tile_lim) {
                 const int cl = row_lim - kbase;  // columns > cl are masked
 #pragma unroll
@@ -518,8 +534,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool valid = row_g < p.N_q;
             const bool has = l > 0.f;
             const float inv = has ? dv / l : 0.f;
+            const bool split = p.n_splits > 1;
+            const size_t prow_idx =
+                ((size_t)blockIdx.y * ((size_t)p.B * p.H) + bh) * p.N_q + (valid ? row_g : 0);
             uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
                              (((size_t)b * p.N_q + (valid ? row_g : 0)) * p.H + h) * D;
+            float* prow = split ? p.part_o + prow_idx * D : nullptr;
 #pragma unroll
             for (int u = 0; u < D / 32; ++u) {
                 uint32_t oo[32];
@@ -530,6 +550,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
 #pragma unroll
                     for (int x = 0; x < 32; ++x) oo[x] = 0u;
+                }
+                if (split) {
+                    // partial of this split, normalised by its own row sum
+                    if (valid) {
+                        float4* dst = reinterpret_cast<float4*>(prow + 32 * u);
+#pragma unroll
+                        for (int x = 0; x < 8; ++x)
+                            dst[x] = make_float4(__uint_as_float(oo[4 * x]) * inv,
+                                                 __uint_as_float(oo[4 * x + 1]) * inv,
+                                                 __uint_as_float(oo[4 * x + 2]) * inv,
+                                                 __uint_as_float(oo[4 * x + 3]) * inv);
+                    }
+                    continue;
                 }
                 uint32_t packed[16];
 #pragma unroll
@@ -546,9 +579,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             packed[4 * x + 3]);
                 }
             }
-            if (valid && p.lse)
-                p.lse[(size_t)bh * p.N_q + row_g] =
-                    has ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+            const float lse_row = has ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+            if (valid && split)
+                p.part_lse[prow_idx] = lse_row;
+            else if (valid && p.lse)
+                p.lse[(size_t)bh * p.N_q + row_g] = lse_row;
         }
     }
 
@@ -558,6 +593,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// Split-KV combine: one warp per query row.  Exact merge of the splits'
+// softmaxes: lse = log sum_s exp(lse_s), O = sum_s exp(lse_s - lse) O_s.
+template <int D>
+__global__ void __launch_bounds__(256) splitkv_combine_kernel(const float* __restrict__ part_o,
+                                                              const float* __restrict__ part_lse,
+                                                              void* o, float* lse, int n_splits,
+                                                              int H, int N_q, long long rows,
+                                                              int out_fp16) {
+    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const long long bh = row / N_q;
+    const int i = (int)(row % N_q);
+    const size_t stride = (size_t)rows;  // one split's [B*H][N_q] block
+    const float ls = lane < n_splits ? part_lse[(size_t)lane * stride + row] : -INFINITY;
+    float mx = ls;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float w = (mx == -INFINITY) ? 0.f : __expf(ls - mx);
+    float tot = w;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+    constexpr int PER = D / 32;
+    float acc[PER];
+#pragma unroll
+    for (int x = 0; x < PER; ++x) acc[x] = 0.f;
+    for (int sidx = 0; sidx < n_splits; ++sidx) {
+        const float ws = __shfl_sync(0xffffffffu, w, sidx);
+        if (ws == 0.f) continue;
+        const float* src = part_o + ((size_t)sidx * stride + row) * D;
+#pragma unroll
+        for (int x = 0; x < PER; ++x) acc[x] = fmaf(ws, src[lane + 32 * x], acc[x]);
+    }
+    const float inv = tot > 0.f ? 1.f / tot : 0.f;
+    const int b = (int)(bh / H), h = (int)(bh % H);
+    const size_t ob = (((size_t)b * N_q + i) * H + h) * D;
+#pragma unroll
+    for (int x = 0; x < PER; ++x) {
+        const float val = acc[x] * inv;
+        if (out_fp16)
+            reinterpret_cast<__half*>(o)[ob + lane + 32 * x] = __float2half_rn(val);
+        else
+            reinterpret_cast<__nv_bfloat16*>(o)[ob + lane + 32 * x] = __float2bfloat16_rn(val);
+    }
+    if (lane == 0 && lse) lse[(size_t)bh * N_q + i] = tot > 0.f ? mx + __logf(tot) : -INFINITY;
 }
 
 // ------------------------------------------------------------------- host side
@@ -606,7 +688,8 @@ bool encode_map(CUtensorMap* m, const void* base, int dtype, int B, int N, int H
 }
 
 template <int D, int KIND>
-cudaError_t launch_t(const Problem& pr, cudaStream_t stream) {
+cudaError_t launch_t(const Problem& pr, cudaStream_t stream, int n_splits = 1,
+                     float* part_o = nullptr, float* part_lse = nullptr) {
     using C = Cfg<D, KIND>;
     CUtensorMap mq, mk, mv;
     const int ce = C::CB / C::E;
@@ -628,6 +711,9 @@ cudaError_t launch_t(const Problem& pr, cudaStream_t stream) {
     p.k_descale = pr.k_descale;
     p.v_descale = pr.v_descale;
     p.timeout_ns = 2000000000ull;
+    p.n_splits = n_splits;
+    p.part_o = part_o;
+    p.part_lse = part_lse;
     const long long n_bh = (long long)pr.B * pr.H;
     // heads scheduled together: their K/V (2 N_k d E bytes each) fill ~48 MiB of L2
     const long long kv_bytes = 2LL * (pr.N_k > 0 ? pr.N_k : 1) * D * C::E;
@@ -640,7 +726,8 @@ cudaError_t launch_t(const Problem& pr, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, KIND>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)n_cta);
+    if (n_splits < 1 || n_splits > 65535) return cudaErrorInvalidValue;
+    dim3 grid((unsigned)n_cta, (unsigned)n_splits);
     attn_tc_kernel<D, KIND><<<grid, kThreads, C::SMEM, stream>>>(mq, mk, mv, p);
     return cudaGetLastError();
 }
@@ -663,6 +750,46 @@ cudaError_t launch_tc(const Problem& p, cudaStream_t stream) {
             break;
     }
     return cudaErrorNotSupported;
+}
+
+size_t splitkv_workspace_bytes(long long B, long long H, long long N_q, int d, int n_splits) {
+    return (size_t)n_splits * (size_t)(B * H * N_q) * (size_t)(d + 1) * sizeof(float);
+}
+
+cudaError_t launch_tc_splitkv(const Problem& p, int n_splits, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+    if (n_splits < 2 || n_splits > kMaxSplits) return cudaErrorInvalidValue;
+    const long long rows = (long long)p.B * p.H * p.N_q;
+    if (workspace_bytes < splitkv_workspace_bytes(p.B, p.H, p.N_q, p.d, n_splits))
+        return cudaErrorInvalidValue;
+    float* part_o = static_cast<float*>(workspace);
+    float* part_lse = part_o + (size_t)n_splits * rows * p.d;
+    cudaError_t e = cudaErrorNotSupported;
+    switch (p.dtype) {
+        case kBF16:
+            if (p.d == 64) e = launch_t<64, kBF16>(p, stream, n_splits, part_o, part_lse);
+            if (p.d == 128) e = launch_t<128, kBF16>(p, stream, n_splits, part_o, part_lse);
+            break;
+        case kFP16:
+            if (p.d == 64) e = launch_t<64, kFP16>(p, stream, n_splits, part_o, part_lse);
+            if (p.d == 128) e = launch_t<128, kFP16>(p, stream, n_splits, part_o, part_lse);
+            break;
+        case kE4M3:
+            if (p.d == 64) e = launch_t<64, kE4M3>(p, stream, n_splits, part_o, part_lse);
+            if (p.d == 128) e = launch_t<128, kE4M3>(p, stream, n_splits, part_o, part_lse);
+            break;
+    }
+    if (e != cudaSuccess) return e;
+    const unsigned blocks = (unsigned)((rows + 7) / 8);
+    if (p.d == 64)
+        splitkv_combine_kernel<64><<<blocks, 256, 0, stream>>>(part_o, part_lse, p.o, p.lse,
+                                                              n_splits, p.H, p.N_q, rows,
+                                                              p.dtype == kFP16);
+    else
+        splitkv_combine_kernel<128><<<blocks, 256, 0, stream>>>(part_o, part_lse, p.o, p.lse,
+                                                               n_splits, p.H, p.N_q, rows,
+                                                               p.dtype == kFP16);
+    return cudaGetLastError();
 }
 
 cudaError_t tc_take_status(unsigned* out, cudaStream_t stream) {

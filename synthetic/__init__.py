@@ -65,6 +65,13 @@ CASES = {
     "C5": Case("C5", 2, 16, 8192, 8192, 128, False, "e4m3", 1005, outliers=True),
 }
 
+# Extra workloads for the rows beyond the five cases (not benchmark headlines):
+# a long K/V range with few query rows, where one CTA per query-tile pair leaves
+# most SMs idle and the K/V range is split across CTAs.
+EXTRA_CASES = {
+    "LKV": Case("LKV", 1, 8, 512, 65536, 128, False, "bf16", 1101),
+}
+
 
 def custom_case(B, H, N_q, N_k, d, causal, dtype="bf16", seed=7, outliers=None, name="custom"):
     if outliers is None:

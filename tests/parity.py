@@ -32,6 +32,11 @@ def run_gpu(case: synthetic.Case, dev: dict, impl: str = "tc"):
                                        dev["v_descale"], **kw)
         else:
             o, lse = attn.attn_fwd(q, k, v, **kw)
+    elif impl.startswith("split"):
+        n = int(impl[len("split"):])
+        o, lse = attn.attn_fwd_splitkv(q, k, v, n, q_descale=dev.get("q_descale"),
+                                       k_descale=dev.get("k_descale"),
+                                       v_descale=dev.get("v_descale"), **kw)
     elif impl == "simt":
         o, lse = attn.attn_fwd_simt(q, k, v, q_descale=dev.get("q_descale"),
                                     k_descale=dev.get("k_descale"),

@@ -31,7 +31,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("attn_fwd", "attn_fwd_fp8", "attn_fwd_simt", "attn_check_status", "attn_status_string"):
+    for n in ("attn_fwd", "attn_fwd_fp8", "attn_fwd_simt", "attn_fwd_splitkv",
+              "attn_splitkv_workspace_bytes", "attn_check_status", "attn_status_string"):
         assert n in names
 
 
@@ -98,3 +99,21 @@ def test_python_binding_refuses_cpu_tensors():
     q = torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         attn.attn_fwd(q, q, q)
+
+
+def test_splitkv_workspace_size(L):
+    # fp32 partial outputs [splits][B*H][N_q][d] plus fp32 partial lse [splits][B*H][N_q]
+    assert L.attn_splitkv_workspace_bytes(2, 3, 100, 128, 4) == 4 * 2 * 3 * 100 * (128 + 1) * 4
+    assert L.attn_splitkv_workspace_bytes(2, 3, 100, 64, 1) == 0
+    assert L.attn_splitkv_workspace_bytes(2, 3, 100, 96, 4) == 0
+    assert L.attn_splitkv_workspace_bytes(2, 3, 100, 64, 33) == 0
+
+
+def test_splitkv_rejects_bad_workspace(L):
+    need = L.attn_splitkv_workspace_bytes(1, 1, 16, 64, 4)
+    args = (P, P, P, P, P, None, None, None, 1, 1, 16, 16, 64, 0.125, 0, 0)
+    assert L.attn_fwd_splitkv(*args, 4, None, need, None) == attn.ATTN_ERR_INVALID_ARG
+    assert L.attn_fwd_splitkv(*args, 4, P, need - 1, None) == attn.ATTN_ERR_INVALID_ARG
+    assert L.attn_fwd_splitkv(*args, 4, P + 4, need, None) == attn.ATTN_ERR_INVALID_ARG
+    assert L.attn_fwd_splitkv(*args, 0, P, need, None) == attn.ATTN_ERR_INVALID_ARG
+    assert L.attn_fwd_splitkv(*args, 33, P, need, None) == attn.ATTN_ERR_INVALID_ARG
