@@ -66,7 +66,8 @@ typedef enum {
     ATTN_ERR_INVALID_ARG = 1,
     ATTN_ERR_UNSUPPORTED = 2,
     ATTN_ERR_CUDA = 3,
-    ATTN_ERR_TIMEOUT = 4
+    ATTN_ERR_TIMEOUT = 4,
+    ATTN_ERR_SCRATCH_LIMIT = 5
 } attn_status_t;
 
 typedef enum {
@@ -124,6 +125,35 @@ ATTN_API attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void
 /* Workspace bytes attn_fwd_splitkv needs (0 for num_splits == 1 or invalid
  * arguments). */
 ATTN_API size_t attn_splitkv_workspace_bytes(int B, int H, int N_q, int d, int num_splits);
+
+/* Size of the fixed scratch array attn_fwd_splitkv_static uses (bytes). */
+#define ATTN_STATIC_SCRATCH_BYTES (32 * 1024 * 1024)
+
+/* attn_fwd_splitkv without a caller workspace, for callers that cannot
+ * allocate device memory (for example a plugin inside a host program that owns
+ * all device memory through its own pool and forbids raw cudaMalloc, or a
+ * latency-critical loop that cannot afford the device-wide synchronisation an
+ * allocation can cause).  The pages have no counterpart: this is a deployment
+ * interface, not part of the method.
+ *
+ * Scratch: a fixed array of ATTN_STATIC_SCRATCH_BYTES compiled into the
+ * library, held by every GPU that loads it until the process exits.  The call
+ * allocates nothing (no cudaMalloc, no allocating library routine).  The
+ * problem must fit: attn_splitkv_workspace_bytes(B, H, N_q, d, num_splits) <=
+ * ATTN_STATIC_SCRATCH_BYTES, else ATTN_ERR_SCRATCH_LIMIT and nothing runs.
+ * num_splits: 2..32.  Other arguments, layouts and errors as attn_fwd_splitkv.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the one array, so calls whose
+ * work overlaps on the GPU (other streams, other host threads) race: order
+ * them on one stream or synchronise between them.  No state carries over from
+ * one call to the next that the result depends on. */
+ATTN_API attn_status_t attn_fwd_splitkv_static(const void* q, const void* k, const void* v,
+                                               void* o, float* lse, const float* q_descale,
+                                               const float* k_descale, const float* v_descale,
+                                               int B, int H, int N_q, int N_k, int d, float scale,
+                                               int causal, attn_dtype_t dtype, int num_splits,
+                                               void* stream);
 
 /* Synchronises `stream`, then returns and clears the device status word:
  * ATTN_ERR_TIMEOUT if a bounded wait inside a kernel ran out since the last

@@ -24,7 +24,9 @@ __all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_simt", "attn_fwd_splitkv",
            "attn_splitkv_workspace_bytes", "attn_check_status", "attn_status_string",
            "AttnError", "lib", "build"]
 
-ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
+(ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT,
+ ATTN_ERR_SCRATCH_LIMIT) = range(6)
+ATTN_STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
 ATTN_BF16, ATTN_FP16, ATTN_FP8_E4M3 = range(3)
 
 _LIB = None
@@ -64,6 +66,9 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd_splitkv.restype = i
         L.attn_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
         L.attn_splitkv_workspace_bytes.restype = sz
+        L.attn_fwd_splitkv_static.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, i, i, i, i, i, f,
+                                              i, i, i, vp]
+        L.attn_fwd_splitkv_static.restype = i
         L.attn_check_status.argtypes = [vp]
         L.attn_check_status.restype = i
         L.attn_status_string.argtypes = [i]
@@ -74,7 +79,8 @@ def lib() -> ctypes.CDLL:
 
 def attn_status_string(status: int) -> str:
     names = {0: "ok", 1: "invalid argument", 2: "unsupported shape or dtype",
-             3: "CUDA error", 4: "bounded wait timed out inside a kernel"}
+             3: "CUDA error", 4: "bounded wait timed out inside a kernel",
+             5: "problem needs more scratch than the library's fixed scratch array holds"}
     if _LIB is not None:
         return _LIB.attn_status_string(int(status)).decode()
     return names.get(int(status), "unknown status")

@@ -159,6 +159,8 @@ const char* attn_status_string(attn_status_t s) {
         case ATTN_ERR_UNSUPPORTED: return "unsupported shape or dtype";
         case ATTN_ERR_CUDA: return "CUDA error";
         case ATTN_ERR_TIMEOUT: return "bounded wait timed out inside a kernel";
+        case ATTN_ERR_SCRATCH_LIMIT:
+            return "problem needs more scratch than the library's fixed scratch array holds";
     }
     return "unknown status";
 }
