@@ -99,6 +99,20 @@ ATTN_API attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v
                             int B, int H, int N_q, int N_k, int d, float scale, int causal,
                             attn_dtype_t dtype, void* stream);
 
+/* Grouped-query / multi-query attention: q, o are [B, N_q, H, d]; k, v are
+ * [B, N_k, H_kv, d] with H % H_kv == 0, and query head h attends with K/V head
+ * h / (H / H_kv) (H_kv == H: multi-head; H_kv == 1: multi-query).  These are
+ * the Multi-Query Attention architectures "FlashAttention (HI)" lists under
+ * FlashAttention-2.  Descales (e4m3 only, NULL = unit): q_descale [B*H],
+ * k_descale and v_descale [B*H_kv], indexed b*H + h and b*H_kv + h_kv.
+ * Everything else as attn_fwd; ATTN_ERR_INVALID_ARG if H_kv < 1 or H is not a
+ * multiple of H_kv. */
+ATTN_API attn_status_t attn_fwd_gqa(const void* q, const void* k, const void* v, void* o,
+                                    float* lse, const float* q_descale, const float* k_descale,
+                                    const float* v_descale, int B, int H, int H_kv, int N_q,
+                                    int N_k, int d, float scale, int causal, attn_dtype_t dtype,
+                                    void* stream);
+
 /* Split-KV forward pass (the same operation as attn_fwd / attn_fwd_fp8).  Each
  * 256-row query-tile pair's K/V range is cut into num_splits contiguous parts
  * processed by separate CTAs, which adds parallelism when B*H*N_q is small and
@@ -154,6 +168,13 @@ ATTN_API attn_status_t attn_fwd_splitkv_static(const void* q, const void* k, con
                                                int B, int H, int N_q, int N_k, int d, float scale,
                                                int causal, attn_dtype_t dtype, int num_splits,
                                                void* stream);
+
+/* Health check of the kernels' bounded waits: launches a one-thread kernel
+ * that waits, with the wait the attention kernel uses, on a barrier nothing
+ * arrives at, so the wait runs out after timeout_us microseconds (1 .. 10^7)
+ * and sets the device status word; the next attn_check_status then returns
+ * ATTN_ERR_TIMEOUT and the context stays usable.  Nothing traps or hangs. */
+ATTN_API attn_status_t attn_selftest_wait(unsigned timeout_us, void* stream);
 
 /* Synchronises `stream`, then returns and clears the device status word:
  * ATTN_ERR_TIMEOUT if a bounded wait inside a kernel ran out since the last

@@ -20,7 +20,7 @@ import os
 
 from . import ext_build as _build
 
-__all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_simt", "attn_fwd_splitkv",
+__all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_simt", "attn_fwd_splitkv", "attn_fwd_gqa",
            "attn_splitkv_workspace_bytes", "attn_check_status", "attn_status_string",
            "AttnError", "lib", "build"]
 
@@ -69,6 +69,10 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd_splitkv_static.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, i, i, i, i, i, f,
                                               i, i, i, vp]
         L.attn_fwd_splitkv_static.restype = i
+        L.attn_fwd_gqa.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, i, i, i, i, i, i, f, i, i, vp]
+        L.attn_fwd_gqa.restype = i
+        L.attn_selftest_wait.argtypes = [ctypes.c_uint, vp]
+        L.attn_selftest_wait.restype = i
         L.attn_check_status.argtypes = [vp]
         L.attn_check_status.restype = i
         L.attn_status_string.argtypes = [i]
@@ -102,7 +106,7 @@ def _dtype_code(t) -> int:
     raise TypeError(f"unsupported input dtype {t.dtype}")
 
 
-def _check_inputs(q, k, v):
+def _check_inputs(q, k, v, gqa=False):
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
@@ -113,8 +117,10 @@ def _check_inputs(q, k, v):
     if q.dtype != k.dtype or q.dtype != v.dtype:
         raise TypeError("q, k, v must share one dtype")
     B, N_q, H, d = q.shape
-    if k.shape != v.shape or k.shape[0] != B or k.shape[2] != H or k.shape[3] != d:
-        raise ValueError("k and v must be [B, N_k, H, d] matching q")
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d or (
+            k.shape[2] != H if not gqa else (k.shape[2] < 1 or H % k.shape[2] != 0)):
+        raise ValueError("k and v must be [B, N_k, H, d] matching q "
+                         "([B, N_k, H_kv, d] with H % H_kv == 0 for grouped-query attention)")
     return B, N_q, H, d, k.shape[1]
 
 
@@ -194,6 +200,20 @@ def attn_fwd_simt(q, k, v, o=None, lse=None, scale=None, causal=False, q_descale
     return o, lse
 
 
+def attn_fwd_gqa(q, k, v, o=None, lse=None, scale=None, causal=False, q_descale=None,
+                 k_descale=None, v_descale=None, stream=None):
+    """Grouped-query / multi-query attention: k, v are [B, N_k, H_kv, d]."""
+    B, N_q, H, d, N_k = _check_inputs(q, k, v, gqa=True)
+    H_kv = k.shape[2]
+    o, lse = _outputs(q, o, lse, B, N_q, H, d)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib().attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(q_descale),
+                            _ptr(k_descale), _ptr(v_descale), B, H, H_kv, N_q, N_k, d, scale,
+                            int(bool(causal)), _dtype_code(q), _stream(stream, q.device))
+    _raise(st, "attn_fwd_gqa")
+    return o, lse
+
+
 def attn_splitkv_workspace_bytes(B, H, N_q, d, num_splits) -> int:
     return int(lib().attn_splitkv_workspace_bytes(B, H, N_q, d, num_splits))
 
@@ -215,6 +235,14 @@ def attn_fwd_splitkv(q, k, v, num_splits, o=None, lse=None, scale=None, causal=F
                                 _ptr(workspace), ws_bytes, _stream(stream, q.device))
     _raise(st, "attn_fwd_splitkv")
     return o, lse
+
+
+def attn_selftest_wait(timeout_us=1000, stream=None, device=None):
+    """Launch the bounded-wait health check (its wait runs out after timeout_us)."""
+    torch = _torch()
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    st = lib().attn_selftest_wait(int(timeout_us), _stream(stream, dev))
+    _raise(st, "attn_selftest_wait")
 
 
 def attn_check_status(stream=None, device=None):

@@ -51,6 +51,7 @@ attn::Problem make_problem(const void* q, const void* k, const void* v, void* o,
     p.v_descale = vd;
     p.B = B;
     p.H = H;
+    p.H_kv = H;
     p.N_q = N_q;
     p.N_k = N_k;
     p.d = d;
@@ -137,6 +138,24 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
             return ATTN_ERR_INVALID_ARG;
         e = attn::launch_tc_splitkv(p, num_splits, workspace, workspace_bytes, s);
     }
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    return from_cuda(e);
+}
+
+attn_status_t attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                           const float* q_descale, const float* k_descale,
+                           const float* v_descale, int B, int H, int H_kv, int N_q, int N_k,
+                           int d, float scale, int causal, attn_dtype_t dtype, void* stream) {
+    if (H_kv < 1 || H < 0 || (H > 0 && H % H_kv != 0)) return ATTN_ERR_INVALID_ARG;
+    attn::Problem p = make_problem(q, k, v, o, lse, q_descale, k_descale, v_descale, B, H, N_q,
+                                   N_k, d, scale, causal, (int)dtype);
+    p.H_kv = H_kv;
+    return run_tc(p, static_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_selftest_wait(unsigned timeout_us, void* stream) {
+    if (timeout_us == 0 || timeout_us > 10u * 1000u * 1000u) return ATTN_ERR_INVALID_ARG;
+    cudaError_t e = attn::launch_wait_selftest(1000ull * timeout_us, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) (void)cudaGetLastError();
     return from_cuda(e);
 }

@@ -22,6 +22,7 @@ struct Problem {
     const float* k_descale;
     const float* v_descale;
     int B, H, N_q, N_k, d;
+    int H_kv;                // K/V heads (H for multi-head; H % H_kv == 0)
     float scale;
     int causal;
     int dtype;
@@ -35,6 +36,9 @@ cudaError_t simt_take_status(unsigned* out, cudaStream_t stream);
 // it does not take.
 cudaError_t launch_tc(const Problem& p, cudaStream_t stream);
 cudaError_t tc_take_status(unsigned* out, cudaStream_t stream);
+
+// Bounded-wait health check (attn_tc.cu).
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream);
 
 // Split-KV on the tensor-core kernel plus the combine kernel (attn_tc.cu).
 constexpr int kMaxSplits = 32;

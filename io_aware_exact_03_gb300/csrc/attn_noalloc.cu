@@ -84,6 +84,7 @@ extern "C" ATTN_API attn_status_t attn_fwd_splitkv_static(
     p.v_descale = v_descale;
     p.B = B;
     p.H = H;
+    p.H_kv = H;
     p.N_q = N_q;
     p.N_k = N_k;
     p.d = d;

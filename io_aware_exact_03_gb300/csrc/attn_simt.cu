@@ -46,14 +46,17 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(Problem p) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t ldq = (int64_t)p.H * D;      // element stride between rows
     const int64_t q_base = ((int64_t)b * p.N_q * p.H + h) * D;
-    const int64_t k_base = ((int64_t)b * p.N_k * p.H + h) * D;
+    const int h_kv = h / (p.H / p.H_kv);   // grouped-query attention: shared K/V head
+    const int64_t ldk = (int64_t)p.H_kv * D;
+    const int64_t k_base = ((int64_t)b * p.N_k * p.H_kv + h_kv) * D;
     const int bh = b * p.H + h;
+    const int bh_kv = b * p.H_kv + h_kv;
 
     float dq = 1.f, dk = 1.f, dv = 1.f;
     if (p.dtype == kE4M3) {
         if (p.q_descale) dq = p.q_descale[bh];
-        if (p.k_descale) dk = p.k_descale[bh];
-        if (p.v_descale) dv = p.v_descale[bh];
+        if (p.k_descale) dk = p.k_descale[bh_kv];
+        if (p.v_descale) dv = p.v_descale[bh_kv];
     }
     // scores are kept in base 2: s2 = s * log2(e); the factor is folded into Q
     const float c = p.scale * dq * dk * 1.4426950408889634f;
@@ -85,7 +88,7 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(Problem p) {
             int r = e / D, t = e % D;
             int j = kt * kKeys + r;
             bool ok = j < p.N_k;
-            int64_t gi = k_base + (int64_t)j * ldq + t;
+            int64_t gi = k_base + (int64_t)j * ldk + t;
             Ks[r * (D + 1) + t] = ok ? load_elem(p.k, gi, p.dtype) : 0.f;
             Vs[r * D + t] = ok ? load_elem(p.v, gi, p.dtype) * dv : 0.f;
         }

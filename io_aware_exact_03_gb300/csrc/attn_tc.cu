@@ -91,6 +91,7 @@ __device__ __forceinline__ uint32_t col_o(int t) { return 256u + (uint32_t)(D * 
 
 struct TcParams {
     int B, H, N_q, N_k;
+    int H_kv;          // K/V heads: query head h reads K/V head h / (H / H_kv)
     int n_pairs;       // ceil(N_q / 256)
     int heads_per_group;
     int causal;
@@ -195,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rank = (int)(rem / Gg);
     const int bh = (int)(g * G + rem % Gg);
     const int b = bh / p.H, h = bh % p.H;
+    const int h_kv = h / (p.H / p.H_kv);  // grouped-query attention: shared K/V head
     const int pair = p.causal ? (p.n_pairs - 1 - rank) : rank;
     int q0[2], n_kv[2];
     q0[0] = pair * 2 * BM;
@@ -271,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* dst = sKV + (size_t)slot * C::TILE;
                 for (int c = 0; c < C::NC; ++c)
                     tma_load_4d(smem_u32(dst + c * C::CHUNK), tm, b_kv_full + 8 * slot,
-                                c * (C::CB / C::E), h, (j0 + (it >> 1)) * BN, b);
+                                c * (C::CB / C::E), h_kv, (j0 + (it >> 1)) * BN, b);
             }
             if (!ok) {
                 // let every load already issued land before the CTA can exit
@@ -394,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float dq = 1.f, dk = 1.f, dv = 1.f;
         if (KIND == kE4M3) {
             if (p.q_descale) dq = p.q_descale[bh];
-            if (p.k_descale) dk = p.k_descale[bh];
-            if (p.v_descale) dv = p.v_descale[bh];
+            if (p.k_descale) dk = p.k_descale[b * p.H_kv + h_kv];
+            if (p.v_descale) dv = p.v_descale[b * p.H_kv + h_kv];
         }
         const float c = p.scale * dq * dk * 1.4426950408889634f;
         float m_used = -INFINITY, l = 0.f;
@@ -595,6 +597,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Health check of the bounded-wait path: one thread waits on an mbarrier that
+// nothing arrives at, with the same wait the attention kernel uses, and must
+// come back with the timeout flagged instead of hanging.
+__global__ void wait_selftest_kernel(unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+    (void)wait_bar(smem_u32(&bar), 0, &abort_flag, limit_ns);
+}
+
 // Split-KV combine: one warp per query row.  Exact merge of the splits'
 // softmaxes: lse = log sum_s exp(lse_s), O = sum_s exp(lse_s - lse) O_s.
 template <int D>
@@ -694,12 +709,13 @@ cudaError_t launch_t(const Problem& pr, cudaStream_t stream, int n_splits = 1,
     CUtensorMap mq, mk, mv;
     const int ce = C::CB / C::E;
     if (!encode_map(&mq, pr.q, KIND, pr.B, pr.N_q, pr.H, D, ce) ||
-        !encode_map(&mk, pr.N_k > 0 ? pr.k : pr.q, KIND, pr.B, pr.N_k, pr.H, D, ce) ||
-        !encode_map(&mv, pr.N_k > 0 ? pr.v : pr.q, KIND, pr.B, pr.N_k, pr.H, D, ce))
+        !encode_map(&mk, pr.N_k > 0 ? pr.k : pr.q, KIND, pr.B, pr.N_k, pr.H_kv, D, ce) ||
+        !encode_map(&mv, pr.N_k > 0 ? pr.v : pr.q, KIND, pr.B, pr.N_k, pr.H_kv, D, ce))
         return cudaErrorInvalidValue;
     TcParams p;
     p.B = pr.B;
     p.H = pr.H;
+    p.H_kv = pr.H_kv;
     p.N_q = pr.N_q;
     p.N_k = pr.N_k;
     p.n_pairs = (pr.N_q + 2 * BM - 1) / (2 * BM);
@@ -716,7 +732,8 @@ cudaError_t launch_t(const Problem& pr, cudaStream_t stream, int n_splits = 1,
     p.part_lse = part_lse;
     const long long n_bh = (long long)pr.B * pr.H;
     // heads scheduled together: their K/V (2 N_k d E bytes each) fill ~48 MiB of L2
-    const long long kv_bytes = 2LL * (pr.N_k > 0 ? pr.N_k : 1) * D * C::E;
+    // (a group of H / H_kv query heads shares one K/V head)
+    const long long kv_bytes = 2LL * (pr.N_k > 0 ? pr.N_k : 1) * D * C::E * pr.H_kv / pr.H + 1;
     long long G = (48LL << 20) / kv_bytes;
     if (G < 1) G = 1;
     if (G > n_bh) G = n_bh;
@@ -789,6 +806,11 @@ cudaError_t launch_tc_splitkv(const Problem& p, int n_splits, void* workspace,
         splitkv_combine_kernel<128><<<blocks, 256, 0, stream>>>(part_o, part_lse, p.o, p.lse,
                                                                n_splits, p.H, p.N_q, rows,
                                                                p.dtype == kFP16);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
     return cudaGetLastError();
 }
 

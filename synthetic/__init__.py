@@ -45,6 +45,7 @@ class Case:
     dtype: str  # "bf16" | "fp16" | "e4m3"
     seed: int
     outliers: bool = False
+    H_kv: int | None = None   # K/V heads (grouped-query attention); None = H
 
     @property
     def scale(self) -> float:
@@ -73,10 +74,11 @@ EXTRA_CASES = {
 }
 
 
-def custom_case(B, H, N_q, N_k, d, causal, dtype="bf16", seed=7, outliers=None, name="custom"):
+def custom_case(B, H, N_q, N_k, d, causal, dtype="bf16", seed=7, outliers=None, name="custom",
+                H_kv=None):
     if outliers is None:
         outliers = dtype == "e4m3"
-    return Case(name, B, H, N_q, N_k, d, bool(causal), dtype, seed, outliers)
+    return Case(name, B, H, N_q, N_k, d, bool(causal), dtype, seed, outliers, H_kv)
 
 
 def _draw(g: torch.Generator, shape, outliers: bool) -> torch.Tensor:
@@ -105,9 +107,10 @@ def make_inputs(case: Case) -> dict:
     """
     g = torch.Generator().manual_seed(case.seed)
     out = {"scale": case.scale}
+    h_kv = case.H if case.H_kv is None else case.H_kv
     shapes = {"q": (case.B, case.N_q, case.H, case.d),
-              "k": (case.B, case.N_k, case.H, case.d),
-              "v": (case.B, case.N_k, case.H, case.d)}
+              "k": (case.B, case.N_k, h_kv, case.d),
+              "v": (case.B, case.N_k, h_kv, case.d)}
     for name in ("q", "k", "v"):
         x = _draw(g, shapes[name], case.outliers)
         if case.dtype == "bf16":

@@ -32,6 +32,10 @@ def run_gpu(case: synthetic.Case, dev: dict, impl: str = "tc"):
                                        dev["v_descale"], **kw)
         else:
             o, lse = attn.attn_fwd(q, k, v, **kw)
+    elif impl == "gqa":
+        o, lse = attn.attn_fwd_gqa(q, k, v, q_descale=dev.get("q_descale"),
+                                   k_descale=dev.get("k_descale"),
+                                   v_descale=dev.get("v_descale"), **kw)
     elif impl.startswith("split"):
         n = int(impl[len("split"):])
         o, lse = attn.attn_fwd_splitkv(q, k, v, n, q_descale=dev.get("q_descale"),
@@ -49,6 +53,10 @@ def run_gpu(case: synthetic.Case, dev: dict, impl: str = "tc"):
 
 def oracle_full(case, inputs):
     q, k, v = oracle.case_inputs_f64(inputs)
+    if k.shape[2] != q.shape[2]:
+        # grouped-query attention: query head h attends with K/V head h // group
+        g = q.shape[2] // k.shape[2]
+        k, v = np.repeat(k, g, axis=2), np.repeat(v, g, axis=2)
     return oracle.attention(q, k, v, case.scale, case.causal)
 
 

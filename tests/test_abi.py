@@ -31,8 +31,9 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("attn_fwd", "attn_fwd_fp8", "attn_fwd_simt", "attn_fwd_splitkv",
-              "attn_splitkv_workspace_bytes", "attn_check_status", "attn_status_string"):
+    for n in ("attn_fwd", "attn_fwd_fp8", "attn_fwd_simt", "attn_fwd_splitkv", "attn_fwd_gqa",
+              "attn_splitkv_workspace_bytes", "attn_selftest_wait", "attn_check_status",
+              "attn_status_string"):
         assert n in names
 
 
@@ -117,3 +118,14 @@ def test_splitkv_rejects_bad_workspace(L):
     assert L.attn_fwd_splitkv(*args, 4, P + 4, need, None) == attn.ATTN_ERR_INVALID_ARG
     assert L.attn_fwd_splitkv(*args, 0, P, need, None) == attn.ATTN_ERR_INVALID_ARG
     assert L.attn_fwd_splitkv(*args, 33, P, need, None) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_selftest_wait_rejects_bad_limits(L):
+    assert L.attn_selftest_wait(0, None) == attn.ATTN_ERR_INVALID_ARG
+    assert L.attn_selftest_wait(20 * 1000 * 1000, None) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_gqa_rejects_bad_head_counts(L):
+    args = (P, P, P, P, P, None, None, None, 1)
+    assert L.attn_fwd_gqa(*args, 8, 3, 16, 16, 64, 0.125, 0, 0, None) == attn.ATTN_ERR_INVALID_ARG
+    assert L.attn_fwd_gqa(*args, 8, 0, 16, 16, 64, 0.125, 0, 0, None) == attn.ATTN_ERR_INVALID_ARG

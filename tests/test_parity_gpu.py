@@ -151,3 +151,33 @@ def test_splitkv_agrees_with_single_pass_on_C3():
     O2, l2 = run_gpu(case, dev, "split4")
     assert np.abs(O1 - O2).max() < 1e-2
     assert np.abs(l1 - l2).max() < 1e-3
+
+
+def test_bounded_wait_times_out_and_context_stays_usable():
+    """A wait that nothing satisfies runs out, is reported, and clears."""
+    attn.attn_selftest_wait(2000)            # 2 ms limit on a barrier nothing arrives at
+    with pytest.raises(attn.AttnError) as err:
+        attn.attn_check_status()
+    assert err.value.status == attn.ATTN_ERR_TIMEOUT
+    assert attn.attn_check_status() == attn.ATTN_OK   # the status word was cleared
+    check_full(synthetic.CASES["C1"], "tc")  # and the context still computes correctly
+
+
+GQA = [
+    # B, H, H_kv, N_q, N_k, d, causal, dtype
+    (2, 8, 2, 300, 300, 128, True, "bf16"),
+    (1, 6, 1, 257, 700, 64, False, "fp16"),     # multi-query
+    (2, 4, 2, 384, 384, 128, False, "e4m3"),
+    (1, 4, 4, 200, 200, 64, True, "bf16"),      # H_kv == H: plain multi-head
+]
+
+
+@pytest.mark.parametrize("shape", GQA, ids=lambda s: "x".join(map(str, s)))
+def test_gqa_matches_oracle(shape):
+    B, H, H_kv, N_q, N_k, d, causal, dtype = shape
+    case = synthetic.custom_case(B, H, N_q, N_k, d, causal, dtype, outliers=False, H_kv=H_kv,
+                                 seed=zlib.crc32(repr(shape).encode()) % 10000)
+    inputs = synthetic.make_inputs(case)
+    O, lse = run_gpu(case, to_device(inputs), "gqa")
+    O_ref, lse_ref = oracle_full(case, inputs)
+    compare(case, O, lse, O_ref, lse_ref)
