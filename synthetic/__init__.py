@@ -126,6 +126,22 @@ def make_inputs(case: Case) -> dict:
     return out
 
 
+def make_raw_inputs(case: Case) -> dict:
+    """The fp32 q, k, v of a case before any rounding (same draws as make_inputs)."""
+    g = torch.Generator().manual_seed(case.seed)
+    h_kv = case.H if case.H_kv is None else case.H_kv
+    shapes = {"q": (case.B, case.N_q, case.H, case.d),
+              "k": (case.B, case.N_k, h_kv, case.d),
+              "v": (case.B, case.N_k, h_kv, case.d)}
+    return {n: _draw(g, shapes[n], case.outliers) for n in ("q", "k", "v")}
+
+
+def random_signs(d: int, seed: int) -> torch.Tensor:
+    """A seeded vector of d random signs (+1 / -1), float32."""
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randint(0, 2, (d,), generator=g) * 2 - 1).to(torch.float32)
+
+
 def sample_rows(case: Case, n: int = 256, seed: int | None = None) -> np.ndarray:
     """Seeded (b, h, i) query-row triples, int64 [n, 3].
 
