@@ -73,7 +73,8 @@ typedef enum {
 typedef enum {
     ATTN_BF16 = 0,
     ATTN_FP16 = 1,
-    ATTN_FP8_E4M3 = 2
+    ATTN_FP8_E4M3 = 2,
+    ATTN_FP32 = 3  /* input of attn_quantize_e4m3 only */
 } attn_dtype_t;
 
 /* Fused forward pass on the tensor cores (tcgen05 MMAs, TMEM accumulators,
@@ -98,6 +99,23 @@ ATTN_API attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v
                             const float* v_descale,
                             int B, int H, int N_q, int N_k, int d, float scale, int causal,
                             attn_dtype_t dtype, void* stream);
+
+/* Incoherent processing + FP8 quantisation ("FlashAttention-3 (BN)" page,
+ * section "Low precision (FP8) and reducing quantisation error"): each row of
+ * x [B, N, H, d] (ATTN_BF16, ATTN_FP16 or ATTN_FP32) is multiplied by the
+ * random orthogonal matrix M = diag(signs) H_d / sqrt(d), H_d the Sylvester
+ * Hadamard matrix, then quantised to e4m3 codes [B, N, H, d] with one fp32
+ * descale per (batch, head) written to descale [B*H]: descale = amax / 448
+ * (1 when amax = 0), code = round-to-nearest-even(y / descale) saturated to
+ * +-448.  signs: device array of d values +1 / -1; NULL quantises without the
+ * rotation (use that for V).  Apply the same signs to q and k: Q M (K M)^T =
+ * Q K^T, so attn_fwd_fp8 on the outputs computes the same attention with
+ * outliers spread over all coordinates.  d must be 64 or 128; codes 16-byte
+ * aligned.  Enqueued on `stream`; allocates nothing (descale also serves as
+ * the amax accumulator). */
+ATTN_API attn_status_t attn_quantize_e4m3(const void* x, attn_dtype_t x_dtype, void* codes,
+                                          float* descale, int B, int N, int H, int d,
+                                          const float* signs, void* stream);
 
 /* Grouped-query / multi-query attention: q, o are [B, N_q, H, d]; k, v are
  * [B, N_k, H_kv, d] with H % H_kv == 0, and query head h attends with K/V head

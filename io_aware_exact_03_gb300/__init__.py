@@ -21,13 +21,14 @@ import os
 from . import ext_build as _build
 
 __all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_simt", "attn_fwd_splitkv", "attn_fwd_gqa",
+           "attn_quantize_e4m3",
            "attn_splitkv_workspace_bytes", "attn_check_status", "attn_status_string",
            "AttnError", "lib", "build"]
 
 (ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT,
  ATTN_ERR_SCRATCH_LIMIT) = range(6)
 ATTN_STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
-ATTN_BF16, ATTN_FP16, ATTN_FP8_E4M3 = range(3)
+ATTN_BF16, ATTN_FP16, ATTN_FP8_E4M3, ATTN_FP32 = range(4)
 
 _LIB = None
 
@@ -71,6 +72,8 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd_splitkv_static.restype = i
         L.attn_fwd_gqa.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, i, i, i, i, i, i, f, i, i, vp]
         L.attn_fwd_gqa.restype = i
+        L.attn_quantize_e4m3.argtypes = [vp, i, vp, fp, i, i, i, i, fp, vp]
+        L.attn_quantize_e4m3.restype = i
         L.attn_selftest_wait.argtypes = [ctypes.c_uint, vp]
         L.attn_selftest_wait.restype = i
         L.attn_check_status.argtypes = [vp]
@@ -212,6 +215,29 @@ def attn_fwd_gqa(q, k, v, o=None, lse=None, scale=None, causal=False, q_descale=
                             int(bool(causal)), _dtype_code(q), _stream(stream, q.device))
     _raise(st, "attn_fwd_gqa")
     return o, lse
+
+
+def attn_quantize_e4m3(x, signs=None, codes=None, descale=None, stream=None):
+    """Rotate rows of x [B, N, H, d] by diag(signs) H_d / sqrt(d) (skipped when signs is
+    None) and quantise to e4m3 with one fp32 descale per (batch, head)."""
+    torch = _torch()
+    if not (x.is_cuda and x.is_contiguous() and x.dim() == 4):
+        raise ValueError("x must be a contiguous CUDA tensor [B, N, H, d]")
+    codes_t = {torch.bfloat16: ATTN_BF16, torch.float16: ATTN_FP16, torch.float32: ATTN_FP32}
+    if x.dtype not in codes_t:
+        raise TypeError(f"unsupported input dtype {x.dtype}")
+    B, N, H, d = x.shape
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.float8_e4m3fn, device=x.device)
+    if descale is None:
+        descale = torch.empty((B, H), dtype=torch.float32, device=x.device)
+    if signs is not None and not (signs.is_cuda and signs.dtype == torch.float32
+                                  and signs.numel() == d):
+        raise ValueError("signs must be a CUDA float32 tensor of d values")
+    st = lib().attn_quantize_e4m3(_ptr(x), codes_t[x.dtype], _ptr(codes), _ptr(descale), B, N,
+                                  H, d, _ptr(signs), _stream(stream, x.device))
+    _raise(st, "attn_quantize_e4m3")
+    return codes, descale
 
 
 def attn_splitkv_workspace_bytes(B, H, N_q, d, num_splits) -> int:

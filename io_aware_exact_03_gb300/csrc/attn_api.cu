@@ -153,6 +153,24 @@ attn_status_t attn_fwd_gqa(const void* q, const void* k, const void* v, void* o,
     return run_tc(p, static_cast<cudaStream_t>(stream));
 }
 
+attn_status_t attn_quantize_e4m3(const void* x, attn_dtype_t x_dtype, void* codes,
+                                 float* descale, int B, int N, int H, int d, const float* signs,
+                                 void* stream) {
+    if (B < 0 || N < 0 || H < 0) return ATTN_ERR_INVALID_ARG;
+    if (x_dtype != ATTN_BF16 && x_dtype != ATTN_FP16 && x_dtype != ATTN_FP32)
+        return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0) return ATTN_OK;
+    if (!descale || !aligned(descale, 4)) return ATTN_ERR_INVALID_ARG;
+    if (N > 0 && (!x || !codes || !aligned(codes, 16) || !aligned(x, 16)))
+        return ATTN_ERR_INVALID_ARG;
+    if (signs && !aligned(signs, 4)) return ATTN_ERR_INVALID_ARG;
+    cudaError_t e = attn::launch_quantize_e4m3(x, (int)x_dtype, signs, codes, descale, B, N, H, d,
+                                               static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    return from_cuda(e);
+}
+
 attn_status_t attn_selftest_wait(unsigned timeout_us, void* stream) {
     if (timeout_us == 0 || timeout_us > 10u * 1000u * 1000u) return ATTN_ERR_INVALID_ARG;
     cudaError_t e = attn::launch_wait_selftest(1000ull * timeout_us, static_cast<cudaStream_t>(stream));

@@ -7,7 +7,7 @@
 
 namespace attn {
 
-enum Dtype : int { kBF16 = 0, kFP16 = 1, kE4M3 = 2 };
+enum Dtype : int { kBF16 = 0, kFP16 = 1, kE4M3 = 2, kFP32 = 3 };
 
 // Device status bits, OR-ed into a per-kernel-file status word.
 enum : unsigned { kStatusTimeout = 1u };
@@ -36,6 +36,10 @@ cudaError_t simt_take_status(unsigned* out, cudaStream_t stream);
 // it does not take.
 cudaError_t launch_tc(const Problem& p, cudaStream_t stream);
 cudaError_t tc_take_status(unsigned* out, cudaStream_t stream);
+
+// Incoherent processing + per-head e4m3 quantisation (attn_quant.cu).
+cudaError_t launch_quantize_e4m3(const void* x, int dtype, const float* signs, void* codes,
+                                 float* descale, int B, int N, int H, int d, cudaStream_t stream);
 
 // Bounded-wait health check (attn_tc.cu).
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream);

@@ -32,6 +32,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("attn_fwd", "attn_fwd_fp8", "attn_fwd_simt", "attn_fwd_splitkv", "attn_fwd_gqa",
+              "attn_quantize_e4m3",
               "attn_splitkv_workspace_bytes", "attn_selftest_wait", "attn_check_status",
               "attn_status_string"):
         assert n in names
@@ -129,3 +130,15 @@ def test_gqa_rejects_bad_head_counts(L):
     args = (P, P, P, P, P, None, None, None, 1)
     assert L.attn_fwd_gqa(*args, 8, 3, 16, 16, 64, 0.125, 0, 0, None) == attn.ATTN_ERR_INVALID_ARG
     assert L.attn_fwd_gqa(*args, 8, 0, 16, 16, 64, 0.125, 0, 0, None) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_attention_rejects_the_quantiser_only_input_type(L):
+    assert call_fwd(L, dtype=attn.ATTN_FP32) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_quantiser_rejects_bad_arguments(L):
+    assert L.attn_quantize_e4m3(P, attn.ATTN_FP8_E4M3, P, P, 1, 4, 1, 64, None, None) == attn.ATTN_ERR_INVALID_ARG
+    assert L.attn_quantize_e4m3(P, attn.ATTN_FP32, P, P, 1, 4, 1, 96, None, None) == attn.ATTN_ERR_UNSUPPORTED
+    assert L.attn_quantize_e4m3(P, attn.ATTN_FP32, P + 4, P, 1, 4, 1, 64, None, None) == attn.ATTN_ERR_INVALID_ARG
+    assert L.attn_quantize_e4m3(P, attn.ATTN_FP32, P, None, 1, 4, 1, 64, None, None) == attn.ATTN_ERR_INVALID_ARG
+    assert L.attn_quantize_e4m3(None, attn.ATTN_FP32, None, None, 0, 4, 1, 64, None, None) == attn.ATTN_OK
