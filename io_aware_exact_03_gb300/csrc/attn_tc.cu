@@ -732,11 +732,16 @@ cudaError_t launch_t(const Problem& pr, cudaStream_t stream, int n_splits = 1,
     p.part_lse = part_lse;
     const long long n_bh = (long long)pr.B * pr.H;
     // heads scheduled together: their K/V (2 N_k d E bytes each) fill ~48 MiB of L2
-    // (a group of H / H_kv query heads shares one K/V head)
-    const long long kv_bytes = 2LL * (pr.N_k > 0 ? pr.N_k : 1) * D * C::E * pr.H_kv / pr.H + 1;
-    long long G = (48LL << 20) / kv_bytes;
+    // Heads scheduled together: their K/V (2 N_k d E bytes per K/V head, a
+    // K/V head shared by H / H_kv query heads) fill ~48 MiB of L2.  The groups
+    // are then evened out so the last one is not a lone small group that
+    // would run by itself at the end.
+    const long long kv_head_bytes = 2LL * (pr.N_k > 0 ? pr.N_k : 1) * D * C::E;
+    long long G = (48LL << 20) * (pr.H / pr.H_kv) / kv_head_bytes;
     if (G < 1) G = 1;
     if (G > n_bh) G = n_bh;
+    const long long n_groups = (n_bh + G - 1) / G;
+    G = (n_bh + n_groups - 1) / n_groups;
     p.heads_per_group = (int)G;
     const long long n_cta = (long long)p.n_pairs * n_bh;
     if (n_cta > 0x7fffffffLL) return cudaErrorNotSupported;
