@@ -76,6 +76,26 @@ def case_by_name(name):
     return synthetic.CASES.get(name) or synthetic.EXTRA_CASES[name]
 
 
+# ------------------------------------------------------- multi-rank helpers
+def shard_seed(case_seed: int, rank: int) -> int:
+    """Each rank draws its own shard of (batch, head) work: seed offset by rank."""
+    return case_seed + 100 * rank
+
+
+def max_over_ranks(torch, dist, ms: float, device) -> float:
+    """The slowest rank's time (the job is done when every rank is done)."""
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank_step: float, steps: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput: every rank's FLOPs over the slowest rank's time."""
+    return world * flops_per_rank_step * steps / (ms_max / 1e3) / 1e12
+
+
 def env_rank():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
@@ -237,7 +257,7 @@ def run_ours(args):
     cases = [case_by_name(n) for n in names]
     host, dev, outs = [], [], []
     for c in cases:
-        c_r = dataclasses.replace(c, seed=c.seed + 100 * rank)
+        c_r = dataclasses.replace(c, seed=shard_seed(c.seed, rank))
         inp = synthetic.make_inputs(c_r)
         host.append(inp)
         dev.append({k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()})
@@ -295,14 +315,10 @@ def run_ours(args):
         dist.barrier()
     clocks = sampler.stop()
     attn.attn_check_status()
-    ms_total = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(torch, dist, t_start.elapsed_time(t_end), "cuda")
     kern_ms = [statistics.fmean(a.elapsed_time(b) for a, b in ev[i]) for i in range(len(cases))]
     flops_step = sum(c.flops for c in cases)
-    value = world * flops_step * K / (ms_total / 1e3) / 1e12
+    value = job_tflops(flops_step, K, world, ms_total)
 
     # ---- end to end through the public API: pinned host -> device -> kernel -> host
     e2e = run_e2e(torch, attn, cases, host, outs, stream, args.e2e_steps, call, world)
@@ -394,14 +410,10 @@ def run_e2e(torch, attn, cases, host, outs, stream, steps, call, world):
     b.record(stream)
     torch.cuda.synchronize()
     attn.attn_check_status()
-    ms = a.elapsed_time(b)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    import torch.distributed as dist
+    ms = max_over_ranks(torch, dist, a.elapsed_time(b), "cuda")
     flops = sum(c.flops for c in cases)
-    return {"value": round(world * flops * steps / (ms / 1e3) / 1e12, 2), "unit": UNIT,
+    return {"value": round(job_tflops(flops, steps, world, ms), 2), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
             "ms_per_step": round(ms / steps, 4)}
 
