@@ -76,9 +76,14 @@ struct Cfg {
     static constexpr uint32_t IDESC_PV = instr_desc(FMT, FMT, 0, 1, BM, D);
     static constexpr uint32_t P_COLS = BN * E / 4;         // TMEM columns holding P
     // Rescale the running output only when the row maximum grew by more than
-    // this (log2 units).  bf16/fp16 P tolerate values up to 2^8; an e4m3 P
-    // must keep its largest weight exactly 1, so e4m3 rescales on every growth.
-    static constexpr float RESCALE_THRESHOLD = (KIND == kE4M3) ? 0.0f : 8.0f;
+    // this (log2 units): P values then stay <= 2^8, inside every P type's range.
+    static constexpr float RESCALE_THRESHOLD = 8.0f;
+    // e4m3 P carries 3 mantissa bits, and O/l divides by the sum of the
+    // unrounded P, so a weight above 1 (the row grew past the stale maximum)
+    // is off by up to 2^-4 of itself.  That is harmless while the weight is a
+    // small share of the row's mass: e4m3 also rescales once the tile's
+    // largest weight exceeds this fraction of the sum accumulated so far.
+    static constexpr float RESCALE_MASS = 0.125f;
     static_assert(SLOTS >= 2, "K/V ring needs two slots");
     static_assert(SMEM_USED <= (size_t)kSmemLimit, "shared memory budget");
 };
@@ -442,7 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float mx = max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]),
                                   fmaxf(mc[6], mc[7]));
             const float m_new = mx * c;
-            const bool need = m_new > m_used + C::RESCALE_THRESHOLD;
+            bool need = m_new > m_used + C::RESCALE_THRESHOLD;
+            if (KIND == kE4M3)
+                need = need || (m_new > m_used && ex2(m_new - m_used) > l * C::RESCALE_MASS);
             const bool any = __any_sync(0xffffffffu, need);
             float alpha = 1.f;
             if (any) {
