@@ -50,7 +50,6 @@ __device__ unsigned g_tc_status = 0;
 
 constexpr int BM = 128;        // query rows per tile (MMA M)
 constexpr int BN = 128;        // keys per tile (MMA N of Q K^T, K of P V)
-constexpr int kThreads = 320;  // 10 warps: producer, MMA, 2 x 4 softmax
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSmemLimit = 232448;  // max dynamic shared memory per CTA
 
@@ -62,13 +61,25 @@ struct Cfg {
     static constexpr int NC = RB / CB;                     // chunks per row
     static constexpr int TILE = BM * RB;                   // bytes per 128-row tile
     static constexpr int CHUNK = BM * CB;                  // bytes per chunk of a tile
-    static constexpr int NB_FIXED = 1 + 2 + 2 + 2 + 1;     // q_full, s_full, p_full, pv_done, drain
-    static constexpr int SLOTS_FIT = (kSmemLimit - 1024 - 2 * TILE - 512) / TILE;
+    // P_t in shared memory (K-major, 128-byte swizzle, like a Q tile of 128-byte
+    // rows) instead of over S_t in TMEM: S_t is free as soon as the softmax
+    // has loaded it, so the next Q K^T runs while the softmax works.
+    static constexpr bool P_SMEM = (KIND == kE4M3);
+    // Warps: 0 producer; 1 MMA issuer (with P_SMEM: 1 and 2, one per tile,
+    // each answering only its own tile's barriers); then 2 x 4 softmax warps.
+    static constexpr int ISSUERS = P_SMEM ? 2 : 1;
+    static constexpr int SOFTMAX_WARP0 = 1 + ISSUERS;
+    static constexpr int THREADS = 32 * (SOFTMAX_WARP0 + 8);
+    static constexpr int PT = P_SMEM ? BM * BN * E : 0;    // bytes of one P tile
+    static constexpr int P_CHUNK = BM * 128;               // bytes of a 128-byte-wide P chunk
+    // q_full, s_full x2, p_full x2, pv_done x2, drain, s_free x2, drain of issuer B
+    static constexpr int NB_FIXED = 1 + 2 + 2 + 2 + 1 + 2 + 1;
+    static constexpr int SLOTS_FIT = (kSmemLimit - 1024 - 2 * TILE - 2 * PT - 512) / TILE;
     static constexpr int SLOTS = SLOTS_FIT > 8 ? 8 : SLOTS_FIT;  // K/V ring depth
     static constexpr uint32_t LAYOUT = (CB == 128) ? 2u : 4u;  // 128B / 64B swizzle
     static constexpr int MMA_K = 32 / E;                   // K per MMA instruction
     static constexpr int NB = NB_FIXED + 2 * SLOTS;        // mbarriers
-    static constexpr size_t SMEM_USED = 1024 + (size_t)TILE * (2 + SLOTS) + NB * 8 + 16;
+    static constexpr size_t SMEM_USED = 1024 + (size_t)TILE * (2 + SLOTS) + 2 * PT + NB * 8 + 16;
     // at least ~120 KB so two CTAs never share an SM (each takes all of TMEM)
     static constexpr size_t SMEM = SMEM_USED > 122880 ? SMEM_USED : 122880;
     static constexpr uint32_t FMT = (KIND == kBF16) ? 1u : 0u;  // bf16 = 1, f16 / e4m3 = 0
@@ -84,7 +95,7 @@ struct Cfg {
     // small share of the row's mass: e4m3 also rescales once the tile's
     // largest weight exceeds this fraction of the sum accumulated so far.
     static constexpr float RESCALE_MASS = 0.125f;
-    static_assert(SLOTS >= 2, "K/V ring needs two slots");
+    static_assert(SLOTS >= 2, "K/V ring depth");
     static_assert(SMEM_USED <= (size_t)kSmemLimit, "shared memory budget");
 };
 
@@ -157,7 +168,7 @@ __device__ __forceinline__ int kv_tiles_for(int q0, const TcParams& p) {
 }
 
 template <int D, int KIND>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const TcParams p) {
     using C = Cfg<D, KIND>;
@@ -165,7 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sQ = smem;                      // two tiles: A then B
-    uint8_t* sKV = smem + 2 * C::TILE;       // SLOTS tiles
+    uint8_t* sP = smem + 2 * C::TILE;        // two P tiles (P_SMEM only)
+    uint8_t* sKV = sP + 2 * C::PT;           // SLOTS tiles
     uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + (size_t)C::SLOTS * C::TILE);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NB);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -175,8 +187,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t b_p_full = smem_u32(bars + 3);     // + 8 * tile
     const uint32_t b_pv_done = smem_u32(bars + 5);    // + 8 * tile
     const uint32_t b_drain = smem_u32(bars + 7);
-    const uint32_t b_kv_full = smem_u32(bars + 8);                // + 8 * slot
-    const uint32_t b_kv_empty = smem_u32(bars + 8 + C::SLOTS);    // + 8 * slot
+    const uint32_t b_s_free = smem_u32(bars + 8);     // + 8 * tile
+    const uint32_t b_drain_b = smem_u32(bars + 10);
+    const uint32_t b_kv_full = smem_u32(bars + 11);               // + 8 * slot
+    const uint32_t b_kv_empty = smem_u32(bars + 11 + C::SLOTS);   // + 8 * slot
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -228,11 +242,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(b_s_full + 8 * t, 1);
             mbar_init(b_p_full + 8 * t, 128);
             mbar_init(b_pv_done + 8 * t, 1);
+            mbar_init(b_s_free + 8 * t, 128);
         }
         mbar_init(b_drain, 1);
+        mbar_init(b_drain_b, 1);
         for (int s = 0; s < C::SLOTS; ++s) {
             mbar_init(b_kv_full + 8 * s, 1);
-            mbar_init(b_kv_empty + 8 * s, 1);
+            // one release per issuer that reads the ring
+            mbar_init(b_kv_empty + 8 * s, C::ISSUERS);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -288,8 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ----------------------------------------------------- MMA issuer
+    } else if (warp < C::SOFTMAX_WARP0) {
+        // ----------------------------------------------------- MMA issuer(s)
         if (lane == 0 && n_max > 0) {
             auto issue_qk = [&](int t, int slot) {
                 const uint32_t q_base = smem_u32(sQ + t * C::TILE);
@@ -316,27 +333,91 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // V is MN-major: 8-key groups 8*CB apart, d-chunks CHUNK apart
                     const uint64_t db = smem_desc(v_base + ks * C::MMA_K * C::CB, C::CHUNK,
                                                   8 * C::CB, C::LAYOUT);
-                    const uint32_t a_tmem = tmem + col_s(t) + ks * (C::MMA_K * C::E / 4);
                     const uint32_t acc = (!first || ks > 0) ? 1u : 0u;
-                    if constexpr (KIND == kE4M3)
-                        mma_f8_ts(tmem + col_o<D>(t), a_tmem, db, C::IDESC_PV, acc);
-                    else
-                        mma_f16_ts(tmem + col_o<D>(t), a_tmem, db, C::IDESC_PV, acc);
+                    if constexpr (C::P_SMEM) {
+                        // P K-major in 128-byte chunks; each MMA takes 32 bytes of K
+                        const uint32_t off = (ks * 32 / 128) * C::P_CHUNK + (ks * 32) % 128;
+                        const uint64_t da =
+                            smem_desc(smem_u32(sP + t * C::PT) + off, 16, 1024, 2u);
+                        if constexpr (KIND == kE4M3)
+                            mma_f8_ss(tmem + col_o<D>(t), da, db, C::IDESC_PV, acc);
+                        else
+                            mma_f16_ss(tmem + col_o<D>(t), da, db, C::IDESC_PV, acc);
+                    } else {
+                        const uint32_t a_tmem = tmem + col_s(t) + ks * (C::MMA_K * C::E / 4);
+                        if constexpr (KIND == kE4M3)
+                            mma_f8_ts(tmem + col_o<D>(t), a_tmem, db, C::IDESC_PV, acc);
+                        else
+                            mma_f16_ts(tmem + col_o<D>(t), a_tmem, db, C::IDESC_PV, acc);
+                    }
                 }
             };
             auto slot_of = [](int it) { return it % C::SLOTS; };
             auto par_of = [](int it) { return (uint32_t)(it / C::SLOTS) & 1u; };
 
-            bool ok = wait_bar(b_q_full, 0, abort_flag, lim);
-            if (ok) ok = wait_bar(b_kv_full + 8 * slot_of(0), par_of(0), abort_flag, lim);
-            if (ok) {
-                tc_fence_after();
-                for (int t = 0; t < 2; ++t) {
-                    if (n_kv[t] == 0) continue;
-                    issue_qk(t, slot_of(0));
-                    mma_commit(b_s_full + 8 * t);
+            bool ok = true;
+            if constexpr (C::P_SMEM) {
+                // One issuer per tile.  S_t is free once the softmax has loaded
+                // it, so the scores of K_{j+1} are issued as soon as that
+                // happens and run while the softmax works; P_t V_j follows when
+                // P_t is in shared memory.  Every ring item gets one release
+                // from each issuer: items this tile never reads (keys beyond
+                // its causal range) are released once they have landed, so a
+                // release never runs ahead of the item's own fill.
+                const int t = warp - 1;
+                const int nt = n_kv[t];
+                const uint32_t drain_t = t == 0 ? b_drain : b_drain_b;
+                ok = wait_bar(b_q_full, 0, abort_flag, lim);
+                if (ok && nt > 0) {
+                    ok = wait_bar(b_kv_full + 8 * slot_of(0), par_of(0), abort_flag, lim);
+                    if (ok) {
+                        tc_fence_after();
+                        issue_qk(t, slot_of(0));
+                        mma_commit(b_s_full + 8 * t);
+                        mma_commit(b_kv_empty + 8 * slot_of(0));
+                    }
                 }
-                mma_commit(b_kv_empty + 8 * slot_of(0));
+                for (int j = 0; j < nt && ok; ++j) {
+                    const int itV = 2 * j + 1, itK = 2 * j + 2;
+                    if (j + 1 < nt) {
+                        ok = wait_bar(b_kv_full + 8 * slot_of(itK), par_of(itK), abort_flag, lim);
+                        if (ok) ok = wait_bar(b_s_free + 8 * t, (uint32_t)j & 1u, abort_flag, lim);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_qk(t, slot_of(itK));
+                        mma_commit(b_s_full + 8 * t);
+                        mma_commit(b_kv_empty + 8 * slot_of(itK));
+                    }
+                    ok = wait_bar(b_kv_full + 8 * slot_of(itV), par_of(itV), abort_flag, lim);
+                    if (ok) ok = wait_bar(b_p_full + 8 * t, (uint32_t)j & 1u, abort_flag, lim);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(t, slot_of(itV), j == 0);
+                    mma_commit(b_pv_done + 8 * t);
+                    mma_commit(b_kv_empty + 8 * slot_of(itV));
+                }
+                // items of K/V tiles [nt, n_max): not read by this tile
+                for (int it = 2 * nt; it < 2 * n_max && ok; ++it) {
+                    ok = wait_bar(b_kv_full + 8 * slot_of(it), par_of(it), abort_flag, lim);
+                    if (ok) mbar_arrive(b_kv_empty + 8 * slot_of(it));
+                }
+                if (!ok) {
+                    // make sure none of this issuer's MMAs still runs when TMEM is freed
+                    mma_commit(drain_t);
+                    wait_drain(drain_t, 0, lim);
+                }
+            } else {
+                ok = wait_bar(b_q_full, 0, abort_flag, lim);
+                if (ok) ok = wait_bar(b_kv_full + 8 * slot_of(0), par_of(0), abort_flag, lim);
+                if (ok) {
+                    tc_fence_after();
+                    for (int t = 0; t < 2; ++t) {
+                        if (n_kv[t] == 0) continue;
+                        issue_qk(t, slot_of(0));
+                        mma_commit(b_s_full + 8 * t);
+                    }
+                    mma_commit(b_kv_empty + 8 * slot_of(0));
+                }
             }
             // Per tile: O_t += P_t V_j, then at once S_t = Q_t K_{j+1}^T into the
             // same TMEM columns.  One thread's tcgen05.mma operations execute in
@@ -344,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // MMA overwrites it; no completion wait is needed in between.
             // While softmax A works, the tensor core runs tile B's pair of MMAs
             // and the other way round.
-            for (int j = 0; j < n_max && ok; ++j) {
+            for (int j = 0; j < n_max && ok && !C::P_SMEM; ++j) {
                 const int itV = 2 * j + 1, itK = 2 * j + 2;
                 ok = wait_bar(b_kv_full + 8 * slot_of(itV), par_of(itV), abort_flag, lim);
                 bool k_ready = false;
@@ -376,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(b_kv_empty + 8 * slot_of(itK));
                 }
             }
-            if (!ok) {
+            if (!ok && !C::P_SMEM) {
                 // make sure no MMA is still reading or writing when TMEM is freed
                 mma_commit(b_drain);
                 wait_drain(b_drain, 0, lim);
@@ -385,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // --------------------------------------- softmax + epilogue (2 x 128 thr)
-        const int t = (warp - 2) >> 2;       // tile of this warp group
+        const int t = (warp - C::SOFTMAX_WARP0) >> 2;  // tile of this warp group
         const int quad = warp & 3;           // TMEM lane quadrant this warp may access
         const int r = quad * 32 + lane;
         const int row_g = q0[t] + r;
@@ -407,6 +488,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float c = p.scale * dq * dk * 1.4426950408889634f;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
+        // this thread's row of P_t in shared memory (P_SMEM only)
+        const uint32_t p_row = smem_u32(sP + t * C::PT) + (uint32_t)(r >> 3) * 1024u +
+                               (uint32_t)(r & 7) * 128u;
 
         for (int j = 0; j < nt; ++j) {
             if (!__all_sync(0xffffffffu, wait_bar(s_full, (uint32_t)j & 1u, abort_flag, lim))) {
@@ -424,6 +508,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < BN / 32; ++u)
                 reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[32 * u]));
+            if constexpr (C::P_SMEM) {
+                // S_t is in registers: the next scores may overwrite it
+                tc_fence_before();
+                mbar_arrive(b_s_free + 8 * t);
+            }
             float s[BN];
 #pragma unroll
             for (int x = 0; x < BN; ++x) s[x] = __uint_as_float(sr[x]);
@@ -495,8 +584,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pk[x / 2] = (KIND == kBF16) ? pack_bf16(p0, p1) : pack_f16(p0, p1);
                     }
                 }
-                tmem_st32(t_row + col_s(t) + 32 * u, pk);
+                if constexpr (C::P_SMEM) {
+                    // the buffer is free once P_{j-1} V_{j-1} has completed
+                    if (u == 0 && j > 0 &&
+                        !__all_sync(0xffffffffu, wait_bar(pv_done, (uint32_t)(j - 1) & 1u,
+                                                          abort_flag, lim))) {
+                        ok = false;
+                        break;
+                    }
+                    // row r of a 128-byte-swizzled K-major tile: 16-byte unit w
+                    // sits at unit w ^ (r % 8)
+                    const uint32_t row_base =
+                        p_row + (uint32_t)u * C::P_CHUNK;
+#pragma unroll
+                    for (int w = 0; w < 8; ++w)
+                        st_shared_v4(row_base + ((uint32_t)(w ^ (r & 7)) << 4), pk[4 * w],
+                                     pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+                } else {
+                    tmem_st32(t_row + col_s(t) + 32 * u, pk);
+                }
             }
+            if (!ok) break;
+            if constexpr (C::P_SMEM) fence_proxy_async_smem();
             const float sum =
                 ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));
             l = l * alpha + sum;
@@ -757,7 +866,7 @@ cudaError_t launch_t(const Problem& pr, cudaStream_t stream, int n_splits = 1,
     if (e != cudaSuccess) return e;
     if (n_splits < 1 || n_splits > 65535) return cudaErrorInvalidValue;
     dim3 grid((unsigned)n_cta, (unsigned)n_splits);
-    attn_tc_kernel<D, KIND><<<grid, kThreads, C::SMEM, stream>>>(mq, mk, mv, p);
+    attn_tc_kernel<D, KIND><<<grid, C::THREADS, C::SMEM, stream>>>(mq, mk, mv, p);
     return cudaGetLastError();
 }
 
