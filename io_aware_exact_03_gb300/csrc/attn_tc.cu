@@ -63,8 +63,13 @@ struct Cfg {
     static constexpr int CHUNK = BM * CB;                  // bytes per chunk of a tile
     // P_t in shared memory (K-major, 128-byte swizzle, like a Q tile of 128-byte
     // rows) instead of over S_t in TMEM: S_t is free as soon as the softmax
-    // has loaded it, so the next Q K^T runs while the softmax works.
-    static constexpr bool P_SMEM = (KIND == kE4M3);
+    // has loaded it, so the next Q K^T runs while the softmax works.  The
+    // cost is shared-memory bandwidth (128 B/clk per SM): the P V MMA then
+    // reads P from shared memory and the softmax writes it there.  For 16-bit
+    // types at d = 128 a step would move ~384 KB through shared memory, more
+    // than the MMAs' 2048 cycles allow (measured 14 % slower on the causal
+    // N = 16384 case), so they keep P over S in TMEM.
+    static constexpr bool P_SMEM = (KIND == kE4M3) || (D == 64);
     // Warps: 0 producer; 1 MMA issuer (with P_SMEM: 1 and 2, one per tile,
     // each answering only its own tile's barriers); then 2 x 4 softmax warps.
     static constexpr int ISSUERS = P_SMEM ? 2 : 1;
