@@ -137,7 +137,9 @@ def read_traffic():
 
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 20 ms, each with its own timestamp; only the
+    samples that fall inside the timed region are reported."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -145,16 +147,39 @@ class ClockSampler:
         self.gpu_id = gpu_id
         self.proc = None
         self.out_path = os.path.join("/tmp", f"bench_clocks_{os.getpid()}.csv")
+        self.window = None
 
     def start(self):
+        """Start sampling; returns once the first sample has been written."""
         try:
             self.fh = open(self.out_path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < 5.0:
+            time.sleep(0.02)
+            try:
+                if os.path.getsize(self.out_path) > 0:
+                    break
+            except OSError:
+                pass
+
+    def mark(self, t0: float, t1: float):
+        """Host wall-clock bounds of the timed region."""
+        self.window = (t0, t1)
+
+    @staticmethod
+    def _stamp(text):
+        import datetime
+        try:
+            return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
 
     def stop(self):
         if self.proc is None:
@@ -169,19 +194,27 @@ class ClockSampler:
         with open(self.out_path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 8:
+                if len(parts) >= 9:
                     rows.append(parts)
         os.remove(self.out_path)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
-        smax = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        if self.window is not None:
+            t0, t1 = self.window
+            inside = [r for r in rows if (ts := self._stamp(r[0])) is not None and t0 <= ts <= t1]
+        else:
+            inside = rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no sample inside the timed region"],
+                    "samples": 0}
+        num = lambda x: x.replace(".", "").isdigit()
+        sm = [float(r[1]) for r in inside if num(r[1])]
+        smax = [float(r[2]) for r in inside if num(r[2])]
+        power = [float(r[3]) for r in inside if num(r[3])]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
-        power = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(rows),
+                "reasons": reasons, "samples": len(inside),
+                "power_w_median": statistics.median(power) if power else None,
                 "power_w_max": max(power) if power else None}
 
 
@@ -225,7 +258,9 @@ def _allowed(case, i):
 
 
 def cpu_baseline(names, target_s=12.0):
-    base = {n: (32 if i == 0 else 16) for i, n in enumerate(names)}
+    # enough rows that every thread has several (a few rows per thread
+    # understate the rate, and the scaled run would fall short of target_s)
+    base = {n: (512 if i == 0 else 256) for i, n in enumerate(names)}
     for n in names:
         _f64_inputs(n)
     f, s, thr = oracle_rows_rate(base, seed=11)                # calibration
@@ -302,7 +337,7 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     sampler.start()
-    time.sleep(0.3)  # let the sampler come up before the timed region
+    wall0 = time.time()
     t_start.record(stream)
     for s in range(K):
         for i in range(len(cases)):
@@ -311,6 +346,7 @@ def run_ours(args):
             ev[i][s][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
+    sampler.mark(wall0, time.time())
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
