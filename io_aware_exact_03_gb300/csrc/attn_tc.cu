@@ -314,15 +314,17 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         // ----------------------------------------------------- MMA issuer(s)
         if (lane == 0 && n_max > 0) {
             auto issue_qk = [&](int t, int slot) {
-                const uint32_t q_base = smem_u32(sQ + t * C::TILE);
-                const uint32_t k_base = smem_u32(sKV + (size_t)slot * C::TILE);
+                // descriptors of the tile bases; each MMA adds its byte offset / 16
+                const uint64_t qd = smem_desc(smem_u32(sQ + t * C::TILE), 16, 8 * C::CB, C::LAYOUT);
+                const uint64_t kd =
+                    smem_desc(smem_u32(sKV + (size_t)slot * C::TILE), 16, 8 * C::CB, C::LAYOUT);
 #pragma unroll
                 for (int c = 0; c < C::NC; ++c) {
 #pragma unroll
                     for (int ks = 0; ks < C::CB / 32; ++ks) {
-                        const uint32_t off = c * C::CHUNK + ks * 32;
-                        const uint64_t da = smem_desc(q_base + off, 16, 8 * C::CB, C::LAYOUT);
-                        const uint64_t db = smem_desc(k_base + off, 16, 8 * C::CB, C::LAYOUT);
+                        const uint32_t off16 = (uint32_t)(c * C::CHUNK + ks * 32) >> 4;
+                        const uint64_t da = qd + off16;
+                        const uint64_t db = kd + off16;
                         const uint32_t acc = (c | ks) != 0;
                         if constexpr (KIND == kE4M3)
                             mma_f8_ss(tmem + col_s(t), da, db, C::IDESC_QK, acc);
@@ -332,12 +334,12 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                 }
             };
             auto issue_pv = [&](int t, int slot, bool first) {
-                const uint32_t v_base = smem_u32(sKV + (size_t)slot * C::TILE);
+                // V is MN-major: 8-key groups 8*CB apart, d-chunks CHUNK apart
+                const uint64_t vd =
+                    smem_desc(smem_u32(sKV + (size_t)slot * C::TILE), C::CHUNK, 8 * C::CB, C::LAYOUT);
 #pragma unroll
                 for (int ks = 0; ks < BN / C::MMA_K; ++ks) {
-                    // V is MN-major: 8-key groups 8*CB apart, d-chunks CHUNK apart
-                    const uint64_t db = smem_desc(v_base + ks * C::MMA_K * C::CB, C::CHUNK,
-                                                  8 * C::CB, C::LAYOUT);
+                    const uint64_t db = vd + ((uint32_t)(ks * C::MMA_K * C::CB) >> 4);
                     const uint32_t acc = (!first || ks > 0) ? 1u : 0u;
                     if constexpr (C::P_SMEM) {
                         // P K-major in 128-byte chunks; each MMA takes 32 bytes of K
