@@ -19,7 +19,10 @@
  * Layouts (all contiguous, row-major, device memory):
  *   q, o : [B, N_q, H, d]      k, v : [B, N_k, H, d]      lse : [B, H, N_q] fp32
  *   o is bf16 for bf16 and e4m3 inputs, fp16 for fp16 inputs.
- *   d (head dimension) must be 64 or 128.
+ *   d (head dimension) must be 64, 128 or 256 (head size 256 is named among
+ *   FlashAttention-2's extensions on the "FlashAttention (HI)" page, section
+ *   "Development and further research").  d = 256 runs a kernel with one 128-row query tile per CTA
+ *   (its 256-column fp32 output accumulator fills half of TMEM).
  *   q, k, v, o must be 16-byte aligned; lse 4-byte aligned.  lse may be NULL
  *   (then it is not written).
  *
@@ -110,7 +113,7 @@ ATTN_API attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v
  * +-448.  signs: device array of d values +1 / -1; NULL quantises without the
  * rotation (use that for V).  Apply the same signs to q and k: Q M (K M)^T =
  * Q K^T, so attn_fwd_fp8 on the outputs computes the same attention with
- * outliers spread over all coordinates.  d must be 64 or 128; codes 16-byte
+ * outliers spread over all coordinates.  d must be 64, 128 or 256; codes 16-byte
  * aligned.  Enqueued on `stream`; allocates nothing (descale also serves as
  * the amax accumulator). */
 ATTN_API attn_status_t attn_quantize_e4m3(const void* x, attn_dtype_t x_dtype, void* codes,

@@ -17,7 +17,7 @@ attn_status_t validate(const attn::Problem& p) {
     if (!(p.scale > 0.f) || !isfinite(p.scale)) return ATTN_ERR_INVALID_ARG;
     if (p.dtype != attn::kBF16 && p.dtype != attn::kFP16 && p.dtype != attn::kE4M3)
         return ATTN_ERR_INVALID_ARG;
-    if (p.d != 64 && p.d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (p.d != 64 && p.d != 128 && p.d != 256) return ATTN_ERR_UNSUPPORTED;
     const bool empty = p.B == 0 || p.H == 0 || p.N_q == 0;
     if (empty) return ATTN_OK;
     if (!p.q || !p.o) return ATTN_ERR_INVALID_ARG;
@@ -110,7 +110,7 @@ attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o
 }
 
 size_t attn_splitkv_workspace_bytes(int B, int H, int N_q, int d, int num_splits) {
-    if (B < 0 || H < 0 || N_q < 0 || (d != 64 && d != 128) || num_splits < 1 ||
+    if (B < 0 || H < 0 || N_q < 0 || (d != 64 && d != 128 && d != 256) || num_splits < 1 ||
         num_splits > attn::kMaxSplits)
         return 0;
     if (num_splits == 1) return 0;
@@ -159,7 +159,7 @@ attn_status_t attn_quantize_e4m3(const void* x, attn_dtype_t x_dtype, void* code
     if (B < 0 || N < 0 || H < 0) return ATTN_ERR_INVALID_ARG;
     if (x_dtype != ATTN_BF16 && x_dtype != ATTN_FP16 && x_dtype != ATTN_FP32)
         return ATTN_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
     if (B == 0 || H == 0) return ATTN_OK;
     if (!descale || !aligned(descale, 4)) return ATTN_ERR_INVALID_ARG;
     if (N > 0 && (!x || !codes || !aligned(codes, 16) || !aligned(x, 16)))
@@ -182,10 +182,11 @@ attn_status_t attn_check_status(void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return ATTN_ERR_CUDA;
-    unsigned a = 0, b = 0;
+    unsigned a = 0, b = 0, c = 0;
     if (attn::tc_take_status(&a, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (attn::tc256_take_status(&c, s) != cudaSuccess) return ATTN_ERR_CUDA;
     if (attn::simt_take_status(&b, s) != cudaSuccess) return ATTN_ERR_CUDA;
-    if ((a | b) & attn::kStatusTimeout) return ATTN_ERR_TIMEOUT;
+    if ((a | b | c) & attn::kStatusTimeout) return ATTN_ERR_TIMEOUT;
     return ATTN_OK;
 }
 

@@ -37,6 +37,12 @@ cudaError_t simt_take_status(unsigned* out, cudaStream_t stream);
 cudaError_t launch_tc(const Problem& p, cudaStream_t stream);
 cudaError_t tc_take_status(unsigned* out, cudaStream_t stream);
 
+// Tensor-core kernel for head dimension 256 (attn_tc256.cu): one 128-row
+// query tile per CTA.  n_splits > 1 writes fp32 partials as launch_tc_splitkv.
+cudaError_t launch_tc256(const Problem& p, cudaStream_t stream, int n_splits, float* part_o,
+                         float* part_lse);
+cudaError_t tc256_take_status(unsigned* out, cudaStream_t stream);
+
 // Incoherent processing + per-head e4m3 quantisation (attn_quant.cu).
 cudaError_t launch_quantize_e4m3(const void* x, int dtype, const float* signs, void* codes,
                                  float* descale, int B, int N, int H, int d, cudaStream_t stream);

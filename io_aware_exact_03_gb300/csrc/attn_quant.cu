@@ -160,6 +160,7 @@ cudaError_t launch_quantize_e4m3(const void* x, int dtype, const float* signs, v
                                  float* descale, int B, int N, int H, int d, cudaStream_t stream) {
     if (d == 64) return launch_quant<64>(x, dtype, signs, codes, descale, B, N, H, stream);
     if (d == 128) return launch_quant<128>(x, dtype, signs, codes, descale, B, N, H, stream);
+    if (d == 256) return launch_quant<256>(x, dtype, signs, codes, descale, B, N, H, stream);
     return cudaErrorNotSupported;
 }
 

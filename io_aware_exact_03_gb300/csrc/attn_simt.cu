@@ -179,6 +179,7 @@ cudaError_t launch_simt(const Problem& p, cudaStream_t stream) {
     if (p.H > 65535 || p.B > 65535) return cudaErrorNotSupported;
     if (p.d == 64) return launch_d<64>(p, stream);
     if (p.d == 128) return launch_d<128>(p, stream);
+    if (p.d == 256) return launch_d<256>(p, stream);
     return cudaErrorNotSupported;
 }
 

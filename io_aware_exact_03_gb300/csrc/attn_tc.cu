@@ -40,6 +40,7 @@
 
 #include "attn_internal.h"
 #include "tc_ptx.cuh"
+#include "tma_map.cuh"
 
 namespace attn {
 namespace {
@@ -781,59 +782,15 @@ __global__ void __launch_bounds__(256) splitkv_combine_kernel(const float* __res
 }
 
 // ------------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    }
-    return fn;
-}
-
-// [B, N, H, d] tensor seen as a 4-D map {d, H, N, B}; box = one swizzle chunk
-// of d x 1 head x 128 rows x 1 batch.
-bool encode_map(CUtensorMap* m, const void* base, int dtype, int B, int N, int H, int d,
-                int chunk_elems) {
-    EncodeTiledFn enc = get_encode();
-    if (!enc) return false;
-    const int E = dtype == kE4M3 ? 1 : 2;
-    const CUtensorMapDataType dt = dtype == kBF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                   : dtype == kFP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                    : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)(N > 0 ? N : 1),
-                                (cuuint64_t)B};
-    const cuuint64_t strides[3] = {(cuuint64_t)d * E, (cuuint64_t)H * d * E,
-                                   (cuuint64_t)(N > 0 ? N : 1) * H * d * E};
-    const cuuint32_t box[4] = {(cuuint32_t)chunk_elems, 1, (cuuint32_t)BM, 1};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    const CUtensorMapSwizzle sw =
-        chunk_elems * E == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    CUresult r = enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 template <int D, int KIND>
 cudaError_t launch_t(const Problem& pr, cudaStream_t stream, int n_splits = 1,
                      float* part_o = nullptr, float* part_lse = nullptr) {
     using C = Cfg<D, KIND>;
     CUtensorMap mq, mk, mv;
     const int ce = C::CB / C::E;
-    if (!encode_map(&mq, pr.q, KIND, pr.B, pr.N_q, pr.H, D, ce) ||
-        !encode_map(&mk, pr.N_k > 0 ? pr.k : pr.q, KIND, pr.B, pr.N_k, pr.H_kv, D, ce) ||
-        !encode_map(&mv, pr.N_k > 0 ? pr.v : pr.q, KIND, pr.B, pr.N_k, pr.H_kv, D, ce))
+    if (!tma::encode_map(&mq, pr.q, KIND, pr.B, pr.N_q, pr.H, D, ce, BM) ||
+        !tma::encode_map(&mk, pr.N_k > 0 ? pr.k : pr.q, KIND, pr.B, pr.N_k, pr.H_kv, D, ce, BN) ||
+        !tma::encode_map(&mv, pr.N_k > 0 ? pr.v : pr.q, KIND, pr.B, pr.N_k, pr.H_kv, D, ce, BN))
         return cudaErrorInvalidValue;
     TcParams p;
     p.B = pr.B;
@@ -880,6 +837,7 @@ cudaError_t launch_t(const Problem& pr, cudaStream_t stream, int n_splits = 1,
 }  // namespace
 
 cudaError_t launch_tc(const Problem& p, cudaStream_t stream) {
+    if (p.d == 256) return launch_tc256(p, stream, 1, nullptr, nullptr);
     switch (p.dtype) {
         case kBF16:
             if (p.d == 64) return launch_t<64, kBF16>(p, stream);
@@ -910,7 +868,8 @@ cudaError_t launch_tc_splitkv(const Problem& p, int n_splits, void* workspace,
     float* part_o = static_cast<float*>(workspace);
     float* part_lse = part_o + (size_t)n_splits * rows * p.d;
     cudaError_t e = cudaErrorNotSupported;
-    switch (p.dtype) {
+    if (p.d == 256) e = launch_tc256(p, stream, n_splits, part_o, part_lse);
+    switch (p.d == 256 ? -1 : p.dtype) {
         case kBF16:
             if (p.d == 64) e = launch_t<64, kBF16>(p, stream, n_splits, part_o, part_lse);
             if (p.d == 128) e = launch_t<128, kBF16>(p, stream, n_splits, part_o, part_lse);
@@ -930,6 +889,10 @@ cudaError_t launch_tc_splitkv(const Problem& p, int n_splits, void* workspace,
         splitkv_combine_kernel<64><<<blocks, 256, 0, stream>>>(part_o, part_lse, p.o, p.lse,
                                                               n_splits, p.H, p.N_q, rows,
                                                               p.dtype == kFP16);
+    else if (p.d == 256)
+        splitkv_combine_kernel<256><<<blocks, 256, 0, stream>>>(part_o, part_lse, p.o, p.lse,
+                                                               n_splits, p.H, p.N_q, rows,
+                                                               p.dtype == kFP16);
     else
         splitkv_combine_kernel<128><<<blocks, 256, 0, stream>>>(part_o, part_lse, p.o, p.lse,
                                                                n_splits, p.H, p.N_q, rows,

@@ -71,6 +71,8 @@ CASES = {
 # most SMs idle and the K/V range is split across CTAs.
 EXTRA_CASES = {
     "LKV": Case("LKV", 1, 8, 512, 65536, 128, False, "bf16", 1101),
+    # head dimension 256 (the largest head size the pages name), causal bf16
+    "D256": Case("D256", 2, 8, 8192, 8192, 256, True, "bf16", 1102),
 }
 
 

@@ -79,7 +79,8 @@ def test_rejects_bad_arguments(L):
     assert call_fwd(L, lse=P + 2) == attn.ATTN_ERR_INVALID_ARG
     assert call_fwd(L, dtype=7) == attn.ATTN_ERR_INVALID_ARG
     assert call_fwd(L, d=96) == attn.ATTN_ERR_UNSUPPORTED
-    assert call_fwd(L, d=256) == attn.ATTN_ERR_UNSUPPORTED
+    assert call_fwd(L, d=32) == attn.ATTN_ERR_UNSUPPORTED
+    assert call_fwd(L, d=512) == attn.ATTN_ERR_UNSUPPORTED
 
 
 def test_empty_problems_launch_nothing(L):

@@ -6,7 +6,8 @@ seconds (C1, C2) and on 256 seeded (b, h, i) rows otherwise (C3-C5, at their
 full sizes and in the launch configuration the benchmark times).  Edge cases
 cover ragged tiles, N_q != N_k under the causal mask (including rows with no
 allowed key), N_k = 1, N_k = 0, N_q = 0, several batches and heads, every
-dtype and both head dimensions.
+dtype and every head dimension (64, 128, 256).  The d = 256 workload D256
+(B2 H8 N8192, causal) is checked on sampled rows like C3-C5.
 """
 
 import zlib
@@ -43,6 +44,10 @@ def test_case_sampled(name, impl):
     check_sampled(synthetic.CASES[name], impl)
 
 
+def test_d256_workload_sampled():
+    check_sampled(synthetic.EXTRA_CASES["D256"], "tc")
+
+
 EDGE = [
     # B, H, N_q, N_k, d, causal, dtype
     (1, 1, 1, 1, 64, False, "bf16"),
@@ -57,6 +62,14 @@ EDGE = [
     (2, 2, 129, 383, 128, True, "e4m3"),
     (1, 3, 256, 256, 64, False, "e4m3"),
     (1, 2, 640, 640, 128, True, "e4m3"),
+    # head dimension 256: one query tile per CTA, half-tile K/V ring items
+    (1, 1, 1, 1, 256, False, "bf16"),
+    (1, 2, 300, 300, 256, True, "bf16"),
+    (2, 1, 129, 700, 256, False, "fp16"),
+    (1, 2, 100, 300, 256, True, "bf16"),
+    (1, 2, 300, 100, 256, True, "bf16"),     # first 200 rows see no key
+    (1, 2, 256, 640, 256, False, "e4m3"),
+    (1, 1, 640, 640, 256, True, "e4m3"),
 ]
 
 
@@ -130,6 +143,8 @@ SPLIT = [
     (1, 1, 200, 300, 64, True, "bf16", 8),      # more splits than K/V tiles: empty splits
     (1, 2, 300, 100, 128, True, "bf16", 2),     # rows with no key at all
     (2, 2, 513, 1537, 128, True, "bf16", 32),
+    (1, 2, 256, 3000, 256, True, "bf16", 4),
+    (1, 1, 130, 2000, 256, False, "e4m3", 3),
 ]
 
 
@@ -169,6 +184,7 @@ GQA = [
     (1, 6, 1, 257, 700, 64, False, "fp16"),     # multi-query
     (2, 4, 2, 384, 384, 128, False, "e4m3"),
     (1, 4, 4, 200, 200, 64, True, "bf16"),      # H_kv == H: plain multi-head
+    (2, 4, 1, 300, 300, 256, True, "bf16"),     # multi-query at d = 256
 ]
 
 
