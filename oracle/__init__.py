@@ -4,7 +4,8 @@ TEST INFRASTRUCTURE ONLY.  Only the tests, the package smoke check and the
 benchmark's CPU-baseline / reference legs may import this package.  The GPU
 product path never calls it and shares no code with it: the one-pass recurrence
 lives in attn_oracle.c (built here with gcc, no CUDA), the two-pass cross-check
-in two_pass.py (numpy).
+in two_pass.py (numpy), the gradients of the backward pass in backward.py
+(numpy), incoherent processing in incoherent.py (numpy).
 
 Definition followed: Attention(Q,K,V) = softmax(Q K^T / sqrt(d_k)) V from the
 "FlashAttention (HI)" page, section "Problems of standard attention"; the one-pass
