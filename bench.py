@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--case", choices=["C1", "C2", "C3", "C4", "C5", "LKV", "D256"], default=None,
+    ap.add_argument("--case", choices=["C1", "C2", "C3", "C4", "C5", "LKV", "D256", "BWD"], default=None,
                     help="measure one workload case alone instead of the C4 + C5 step")
     ap.add_argument("--splits", type=int, default=1,
                     help="with --case: split each query tile's K/V range over this many CTAs")
@@ -69,6 +69,16 @@ def workload(args):
         return (args.case,), (f"{c.name} {c.dtype} {'causal' if c.causal else 'non-causal'} "
                               f"B{c.B} H{c.H} N_q{c.N_q} N_k{c.N_k} d{c.d}{sp}; one attention call per step")
     return WORKLOAD, WORKLOAD_DESC
+
+
+# The backward pass does five matrix products per (query tile, key tile) pair
+# (S, dP, dV, dK, dQ; the usual count) against the forward's two.
+BWD_FLOP_FACTOR = 2.5
+
+
+def work_flops(c):
+    """Counted FLOPs of one call on case c (forward, or backward for BWD)."""
+    return c.flops * BWD_FLOP_FACTOR if c.name == "BWD" else c.flops
 
 
 def case_by_name(name):
@@ -291,14 +301,26 @@ def run_ours(args):
     names, desc = workload(args)
     cases = [case_by_name(n) for n in names]
     host, dev, outs = [], [], []
+    bwd_ws = None
     for c in cases:
         c_r = dataclasses.replace(c, seed=shard_seed(c.seed, rank))
         inp = synthetic.make_inputs(c_r)
-        host.append(inp)
-        dev.append({k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()})
+        d_in = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
         out_dtype = torch.float16 if c.dtype == "fp16" else torch.bfloat16
-        outs.append((torch.empty((c.B, c.N_q, c.H, c.d), dtype=out_dtype, device="cuda"),
-                     torch.empty((c.B, c.H, c.N_q), dtype=torch.float32, device="cuda")))
+        if c.name == "BWD":
+            # inputs of the backward pass: q, k, v, the forward's o and lse, dO
+            o, lse = attn.attn_fwd(d_in["q"], d_in["k"], d_in["v"], scale=c.scale, causal=c.causal)
+            d_in.update(o=o, lse=lse, dO=synthetic.make_grad(c_r).cuda())
+            inp = dict(inp, o=o.cpu(), lse=lse.cpu(), dO=d_in["dO"].cpu())
+            outs.append((torch.empty_like(d_in["q"]), torch.empty_like(d_in["k"]),
+                         torch.empty_like(d_in["v"])))
+            bwd_ws = torch.empty(attn.attn_bwd_workspace_bytes(c.B, c.H, c.N_q), dtype=torch.uint8,
+                                 device="cuda")
+        else:
+            outs.append((torch.empty((c.B, c.N_q, c.H, c.d), dtype=out_dtype, device="cuda"),
+                         torch.empty((c.B, c.H, c.N_q), dtype=torch.float32, device="cuda")))
+        host.append(inp)
+        dev.append(d_in)
     stream = torch.cuda.current_stream()
     ws = None
     if args.splits > 1:
@@ -307,6 +329,11 @@ def run_ours(args):
 
     def call(i, d):
         c = cases[i]
+        if c.name == "BWD":
+            dq, dk, dv = outs[i]
+            attn.attn_bwd(d["q"], d["k"], d["v"], d["o"], d["lse"], d["dO"], scale=c.scale,
+                          causal=c.causal, dq=dq, dk=dk, dv=dv, workspace=bwd_ws, stream=stream)
+            return
         o, lse = outs[i]
         if args.splits > 1:
             attn.attn_fwd_splitkv(d["q"], d["k"], d["v"], args.splits, o=o, lse=lse,
@@ -353,7 +380,7 @@ def run_ours(args):
     attn.attn_check_status()
     ms_total = max_over_ranks(torch, dist, t_start.elapsed_time(t_end), "cuda")
     kern_ms = [statistics.fmean(a.elapsed_time(b) for a, b in ev[i]) for i in range(len(cases))]
-    flops_step = sum(c.flops for c in cases)
+    flops_step = sum(work_flops(c) for c in cases)
     value = job_tflops(flops_step, K, world, ms_total)
 
     # ---- end to end through the public API: pinned host -> device -> kernel -> host
@@ -364,7 +391,7 @@ def run_ours(args):
     fp8_peak = bf16_peak * FP8_OVER_BF16
     per_kernel = {}
     for i, c in enumerate(cases):
-        ach = c.flops / (kern_ms[i] / 1e3) / 1e12
+        ach = work_flops(c) / (kern_ms[i] / 1e3) / 1e12
         pk = fp8_peak if c.dtype == "e4m3" else bf16_peak
         per_kernel[c.name] = {"dtype": c.dtype, "causal": c.causal, "ms": round(kern_ms[i], 4),
                               "tflops": round(ach, 1), "peak_tflops": round(pk, 1),
@@ -372,15 +399,16 @@ def run_ours(args):
     dom = max(range(len(cases)), key=lambda i: kern_ms[i])
     dc = cases[dom]
     dom_peak = fp8_peak if dc.dtype == "e4m3" else bf16_peak
-    dom_ach = dc.flops / (kern_ms[dom] / 1e3) / 1e12
+    dom_ach = work_flops(dc) / (kern_ms[dom] / 1e3) / 1e12
     traffic = read_traffic() if (dc.name == "C4" and len(cases) == 2) else None
     roofline = {"bound": "tensor", "achieved": round(dom_ach, 1), "peak": round(dom_peak, 1),
                 "unit": "TFLOP/s", "frac": round(dom_ach / dom_peak, 4), "traffic": traffic,
-                "kernel": f"attn_tc_kernel {dc.name} ({dc.dtype}, causal={dc.causal})",
+                "kernel": (f"attn_bwd: bwd_prep + bwd_dkdv + bwd_dq ({dc.dtype}, causal={dc.causal})"
+                           if dc.name == "BWD" else f"attn_tc_kernel {dc.name} ({dc.dtype}, causal={dc.causal})"),
                 "peak_source": f"{peak_src} bf16 burst" + (" x 2 (fp8/bf16 nominal)" if dc.dtype == "e4m3" else ""),
-                "algorithmic_flops_per_launch": dc.flops}
+                "algorithmic_flops_per_launch": work_flops(dc)}
     # mixed roofline of the whole step: time at peak for each kernel over actual time
-    t_peak = sum(c.flops / ((fp8_peak if c.dtype == "e4m3" else bf16_peak) * 1e12) for c in cases)
+    t_peak = sum(work_flops(c) / ((fp8_peak if c.dtype == "e4m3" else bf16_peak) * 1e12) for c in cases)
     step_frac = t_peak / (ms_total / K / 1e3)
 
     result = None
@@ -401,7 +429,7 @@ def run_ours(args):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": len(cases) * K,
+            "gpu_launches": sum(3 if c.name == "BWD" else 1 for c in cases) * K,
             "clocks": clocks,
         }
         print(json.dumps(result), flush=True)
@@ -419,22 +447,20 @@ def run_e2e(torch, attn, cases, host, outs, stream, steps, call, world):
         hp = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in host[i].items()}
         dd = {k: (torch.empty_like(v, device="cuda") if isinstance(v, torch.Tensor) else v)
               for k, v in hp.items()}
-        o, lse = outs[i]
-        ho, hl = torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()
-        pinned.append((hp, dd, ho, hl))
+        hout = [torch.empty_like(t, device="cpu").pin_memory() for t in outs[i]]
+        pinned.append((hp, dd, hout))
         h2d += sum(v.numel() * v.element_size() for v in hp.values() if isinstance(v, torch.Tensor))
-        d2h += o.numel() * o.element_size() + lse.numel() * lse.element_size()
+        d2h += sum(t.numel() * t.element_size() for t in outs[i])
 
     def e2e_step():
         for i in range(len(cases)):
-            hp, dd, ho, hl = pinned[i]
+            hp, dd, hout = pinned[i]
             for k, v in hp.items():
                 if isinstance(v, torch.Tensor):
                     dd[k].copy_(v, non_blocking=True)
             call(i, dd)
-            o, lse = outs[i]
-            ho.copy_(o, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
+            for h, t in zip(hout, outs[i]):
+                h.copy_(t, non_blocking=True)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -448,7 +474,7 @@ def run_e2e(torch, attn, cases, host, outs, stream, steps, call, world):
     attn.attn_check_status()
     import torch.distributed as dist
     ms = max_over_ranks(torch, dist, a.elapsed_time(b), "cuda")
-    flops = sum(c.flops for c in cases)
+    flops = sum(work_flops(c) for c in cases)
     return {"value": round(job_tflops(flops, steps, world, ms), 2), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
             "ms_per_step": round(ms / steps, 4)}

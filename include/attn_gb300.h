@@ -161,6 +161,34 @@ ATTN_API attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void
  * arguments). */
 ATTN_API size_t attn_splitkv_workspace_bytes(int B, int H, int N_q, int d, int num_splits);
 
+/* Backward pass: gradients of the forward's O with respect to q, k and v for an
+ * upstream gradient dO (the pages name training speedups, "FlashAttention
+ * (HI)" page, section "Empirical results", but do not write the backward pass
+ * out; this is the derivative of the formula above).  With P the forward's row
+ * softmax (P_ij = exp(scale q_i.k_j - lse_i), masked entries 0):
+ *   D_i = sum_t dO_it o_it,  dS = P (dO v^T - D),
+ *   dq = scale dS k,  dk = scale dS^T q,  dv = P^T dO.
+ * Inputs: q, o, dO [B, N_q, H, d]; k, v [B, N_k, H, d]; lse [B, H, N_q] fp32 as
+ * written by attn_fwd for the same q, k, v, scale and causal (o likewise).
+ * Outputs dq [B, N_q, H, d], dk, dv [B, N_k, H, d], in dtype (bf16 or fp16;
+ * ATTN_FP8_E4M3 gives ATTN_ERR_UNSUPPORTED), fp32 accumulation.  A key no
+ * query row may attend gets dk = dv = 0; a query row with no allowed key gets
+ * dq = 0.  d must be 64 or 128; H_kv = H.
+ * workspace: caller-allocated device memory of at least
+ * attn_bwd_workspace_bytes(B, H, N_q) bytes, 16-byte aligned, overwritten
+ * (fp32 lse * log2(e) and D per row, each padded to a multiple of 128 rows).
+ * Every output element is written by one CTA: the result is deterministic.
+ * Errors as attn_fwd, plus ATTN_ERR_INVALID_ARG for a missing, misaligned or
+ * too small workspace. */
+ATTN_API attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                                const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                                int B, int H, int N_q, int N_k, int d, float scale, int causal,
+                                attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/* Workspace bytes attn_bwd needs (0 for invalid arguments). */
+ATTN_API size_t attn_bwd_workspace_bytes(int B, int H, int N_q);
+
 /* Size of the fixed scratch array attn_fwd_splitkv_static uses (bytes). */
 #define ATTN_STATIC_SCRATCH_BYTES (32 * 1024 * 1024)
 

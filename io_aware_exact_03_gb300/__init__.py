@@ -23,6 +23,7 @@ from . import ext_build as _build
 __all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_simt", "attn_fwd_splitkv", "attn_fwd_gqa",
            "attn_quantize_e4m3",
            "attn_splitkv_workspace_bytes", "attn_check_status", "attn_status_string",
+           "attn_bwd", "attn_bwd_workspace_bytes",
            "AttnError", "lib", "build"]
 
 (ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT,
@@ -74,6 +75,11 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd_gqa.restype = i
         L.attn_quantize_e4m3.argtypes = [vp, i, vp, fp, i, i, i, i, fp, vp]
         L.attn_quantize_e4m3.restype = i
+        L.attn_bwd.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz,
+                               vp]
+        L.attn_bwd.restype = i
+        L.attn_bwd_workspace_bytes.argtypes = [i, i, i]
+        L.attn_bwd_workspace_bytes.restype = sz
         L.attn_selftest_wait.argtypes = [ctypes.c_uint, vp]
         L.attn_selftest_wait.restype = i
         L.attn_check_status.argtypes = [vp]
@@ -261,6 +267,35 @@ def attn_fwd_splitkv(q, k, v, num_splits, o=None, lse=None, scale=None, causal=F
                                 _ptr(workspace), ws_bytes, _stream(stream, q.device))
     _raise(st, "attn_fwd_splitkv")
     return o, lse
+
+
+def attn_bwd_workspace_bytes(B, H, N_q):
+    return int(lib().attn_bwd_workspace_bytes(int(B), int(H), int(N_q)))
+
+
+def attn_bwd(q, k, v, o, lse, dO, scale=None, causal=False, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """Backward pass: (dq, dk, dv) for upstream gradient dO; o and lse from attn_fwd."""
+    torch = _torch()
+    B, N_q, H, d, N_k = _check_inputs(q, k, v)
+    for name, t, shape in (("o", o, q.shape), ("dO", dO, q.shape)):
+        if tuple(t.shape) != tuple(shape) or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {q.dtype} tensor of shape {tuple(shape)}")
+    if tuple(lse.shape) != (B, H, N_q) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor [B, H, N_q]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    need = attn_bwd_workspace_bytes(B, H, N_q)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                        _ptr(dk), _ptr(dv), B, H, N_q, N_k, d, scale, int(bool(causal)),
+                        _dtype_code(q), _ptr(workspace), ws_bytes, _stream(stream, q.device))
+    _raise(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_selftest_wait(timeout_us=1000, stream=None, device=None):

@@ -171,6 +171,59 @@ attn_status_t attn_quantize_e4m3(const void* x, attn_dtype_t x_dtype, void* code
     return from_cuda(e);
 }
 
+size_t attn_bwd_workspace_bytes(int B, int H, int N_q) {
+    if (B < 0 || H < 0 || N_q < 0) return 0;
+    return attn::bwd_workspace_bytes(B, H, N_q);
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                       int H, int N_q, int N_k, int d, float scale, int causal,
+                       attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+    if (B < 0 || H < 0 || N_q < 0 || N_k < 0) return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_BF16 && dtype != ATTN_FP16) {
+        if (dtype == ATTN_FP8_E4M3) return ATTN_ERR_UNSUPPORTED;
+        return ATTN_ERR_INVALID_ARG;
+    }
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || (N_q == 0 && N_k == 0)) return ATTN_OK;
+    const void* need16[] = {q, k, v, o, dO, dq, dk, dv};
+    const bool has_q = N_q > 0, has_k = N_k > 0;
+    const bool present[] = {has_q, has_k, has_k, has_q, has_q, has_q, has_k, has_k};
+    for (int i = 0; i < 8; ++i) {
+        if (!present[i]) continue;
+        if (!need16[i] || !aligned(need16[i], 16)) return ATTN_ERR_INVALID_ARG;
+    }
+    if (has_q && (!lse || !aligned(lse, 4))) return ATTN_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 16) ||
+        workspace_bytes < attn::bwd_workspace_bytes(B, H, N_q))
+        return ATTN_ERR_INVALID_ARG;
+    attn::BwdArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.lse = lse;
+    a.dO = dO;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.B = B;
+    a.H = H;
+    a.N_q = N_q;
+    a.N_k = N_k;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.dtype = (int)dtype;
+    a.workspace = workspace;
+    cudaError_t e = attn::launch_bwd(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    return from_cuda(e);
+}
+
 attn_status_t attn_selftest_wait(unsigned timeout_us, void* stream) {
     if (timeout_us == 0 || timeout_us > 10u * 1000u * 1000u) return ATTN_ERR_INVALID_ARG;
     cudaError_t e = attn::launch_wait_selftest(1000ull * timeout_us, static_cast<cudaStream_t>(stream));
@@ -182,11 +235,12 @@ attn_status_t attn_check_status(void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return ATTN_ERR_CUDA;
-    unsigned a = 0, b = 0, c = 0;
+    unsigned a = 0, b = 0, c = 0, g = 0;
     if (attn::tc_take_status(&a, s) != cudaSuccess) return ATTN_ERR_CUDA;
     if (attn::tc256_take_status(&c, s) != cudaSuccess) return ATTN_ERR_CUDA;
     if (attn::simt_take_status(&b, s) != cudaSuccess) return ATTN_ERR_CUDA;
-    if ((a | b | c) & attn::kStatusTimeout) return ATTN_ERR_TIMEOUT;
+    if (attn::bwd_take_status(&g, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    if ((a | b | c | g) & attn::kStatusTimeout) return ATTN_ERR_TIMEOUT;
     return ATTN_OK;
 }
 

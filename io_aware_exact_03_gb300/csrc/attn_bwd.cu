@@ -1,0 +1,793 @@
+// Backward pass of exact attention on the fifth-generation tensor cores
+// (sm_103a): dQ, dK, dV from Q, K, V, the forward's O and lse, and the upstream
+// gradient dO.
+//
+// The pages motivate the backward pass only through training speedups
+// ("FlashAttention (HI)" page, section "Empirical results"); the arithmetic is
+// the derivative of the forward definition (same page, section "Problems of
+// standard attention"), organised like the forward: tiles in shared memory,
+// the scores recomputed on chip from Q, K and the forward's lse, nothing
+// N x N in HBM (same page, sections "Tiling and block processing" and
+// "Combining operations in one CUDA kernel"):
+//
+//   P_ij = exp(scale q_i.k_j - lse_i)            (lse from the forward)
+//   D_i  = sum_t dO_it O_it
+//   dV   = P^T dO,   dP = dO V^T,   dS = P (dP - D)
+//   dQ   = scale dS K,   dK = scale dS^T Q
+//
+// Three kernels, each using only MMA forms of the forward kernel:
+//   * bwd_prep: D_i and lse_i in base 2 into a padded workspace (one warp per
+//     row; rows with no key get lse2 = +inf so their P is exactly 0);
+//   * bwd_dkdv: one CTA per 128-key tile.  Per query tile: S^T = K Q^T and
+//     dP^T = V dO^T into TMEM (both K-major from shared memory, the forward's
+//     score form), one thread per key row turns them into P^T and dS^T (bf16 /
+//     fp16, over the same TMEM columns), then dV += P^T dO and dK += dS^T Q
+//     (A from TMEM, B MN-major from shared memory: the forward's P V form).
+//     The per-query vectors lse2 and D ride with each Q / dO tile;
+//   * bwd_dq: one CTA per 128-row query tile.  Per key tile: S = Q K^T and
+//     dP = dO V^T, one thread per query row forms dS, then dQ += dS K.
+// Every output element is written by one CTA: no atomics, deterministic.
+// Warps: 0 TMA producer, 1 MMA issuer (TMEM owner), 2-5 elementwise.  Every
+// mbarrier wait is bounded; on expiry the CTA drains, frees TMEM and exits
+// with the status word set.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "attn_internal.h"
+#include "tc_ptx.cuh"
+#include "tma_map.cuh"
+
+namespace attn {
+namespace {
+
+using namespace ptx;
+
+__device__ unsigned g_bwd_status = 0;
+
+constexpr int BM = 128;        // query rows per tile
+constexpr int BN = 128;        // keys per tile
+constexpr int kThreads = 192;  // producer, MMA issuer, 4 elementwise warps
+constexpr uint32_t kTmemCols = 512;
+constexpr int kSmemLimit = 232448;
+
+template <int D, int KIND>
+struct BCfg {
+    static constexpr int E = 2;                       // bytes per element (bf16 / fp16)
+    static constexpr int CB = 128;                    // bytes per swizzle chunk row
+    static constexpr int CE = CB / E;                 // 64 elements per chunk
+    static constexpr int NC = D * E / CB;             // chunks per row: 1 (d 64), 2 (d 128)
+    static constexpr int TILE = 128 * D * E;          // one 128-row tile
+    static constexpr int CHUNK = 128 * CB;            // one d-chunk of a tile
+    static constexpr int MMA_K = 16;
+    static constexpr uint32_t FMT = (KIND == kBF16) ? 1u : 0u;
+    // scores-like: A and B K-major, N = 128;  accumulate: A from TMEM, B MN-major, N = D
+    static constexpr uint32_t IDESC_S = instr_desc(FMT, FMT, 0, 0, 128, 128);
+    static constexpr uint32_t IDESC_ACC = instr_desc(FMT, FMT, 0, 1, 128, D);
+    // bwd_dkdv ring item: Q tile, dO tile, lse2[128], D[128]
+    static constexpr int ITEM_KV = 2 * TILE + 1024;
+    static constexpr int SLOTS_KV_FIT = (kSmemLimit - 1024 - 2 * TILE - 512) / ITEM_KV;
+    static constexpr int SLOTS_KV = SLOTS_KV_FIT > 6 ? 6 : SLOTS_KV_FIT;
+    static constexpr size_t SMEM_KV = 1024 + 2 * (size_t)TILE + (size_t)SLOTS_KV * ITEM_KV + 512;
+    // bwd_dq ring item: K tile, V tile
+    static constexpr int ITEM_Q = 2 * TILE;
+    static constexpr int SLOTS_Q_FIT = (kSmemLimit - 1024 - 2 * TILE - 512) / ITEM_Q;
+    static constexpr int SLOTS_Q = SLOTS_Q_FIT > 6 ? 6 : SLOTS_Q_FIT;
+    static constexpr size_t SMEM_Q = 1024 + 2 * (size_t)TILE + (size_t)SLOTS_Q * ITEM_Q + 512;
+    static_assert(SLOTS_KV >= 2 && SLOTS_Q >= 2, "ring depth");
+    static_assert(SMEM_KV <= (size_t)kSmemLimit && SMEM_Q <= (size_t)kSmemLimit, "smem");
+};
+
+// TMEM columns (both kernels): S or S^T [0,128), dP or dP^T [128,256),
+// accumulators from 256 (dV then dK, or dQ).
+constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256;
+
+struct BwdParams {
+    int B, H, N_q, N_k, N_pad;
+    int n_units_tiles;    // key tiles (dkdv) or query tiles (dq)
+    int heads_per_group;
+    int causal;
+    float scale;
+    const float* lse2;    // [B*H][N_pad]: lse * log2(e), +inf for padding / no key
+    const float* Dvec;    // [B*H][N_pad]
+    void* out_a;          // dkdv: dV; dq: dQ    [B, N, H, D]
+    void* out_b;          // dkdv: dK
+    unsigned long long timeout_ns;
+};
+
+__device__ __noinline__ bool wait_slow_b(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned long long limit_ns) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 31u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > limit_ns) {
+                *abort_flag = 1;
+                atomicOr(&g_bwd_status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow_b(bar, parity, abort_flag, limit_ns);
+}
+
+__device__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer() - t0 > limit_ns) return;
+    }
+}
+
+// unit L -> (b, h, tile rank) in groups of heads_per_group heads, the tile
+// rank the slow coordinate inside a group
+__device__ __forceinline__ void decode(long long L, const BwdParams& p, int* b, int* h, int* rank) {
+    const long long n_bh = (long long)p.B * p.H;
+    const long long G = p.heads_per_group;
+    const long long per_group = (long long)p.n_units_tiles * G;
+    const long long n_full = n_bh / G;
+    long long g, rem, Gg;
+    if (L < n_full * per_group) {
+        g = L / per_group;
+        rem = L % per_group;
+        Gg = G;
+    } else {
+        g = n_full;
+        rem = L - n_full * per_group;
+        Gg = n_bh - n_full * G;
+    }
+    *rank = (int)(rem / Gg);
+    const int bh = (int)(g * G + rem % Gg);
+    *b = bh / p.H;
+    *h = bh % p.H;
+}
+
+// ---------------------------------------------------------------- prep
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const void* o, const void* dO, const float* lse,
+                                                       float* lse2, float* Dvec, int B, int H, int N_q,
+                                                       int N_pad, int d, int fp16) {
+    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= (long long)B * H * N_pad) return;
+    const long long bh = row / N_pad;
+    const int i = (int)(row % N_pad);
+    float dsum = 0.f, l2 = INFINITY;
+    if (i < N_q) {
+        const int b = (int)(bh / H), h = (int)(bh % H);
+        const size_t base = (((size_t)b * N_q + i) * H + h) * d;
+        for (int t = lane; t < d; t += 32) {
+            float a, g;
+            if (fp16) {
+                a = __half2float(reinterpret_cast<const __half*>(o)[base + t]);
+                g = __half2float(reinterpret_cast<const __half*>(dO)[base + t]);
+            } else {
+                a = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(o)[base + t]);
+                g = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(dO)[base + t]);
+            }
+            dsum = fmaf(a, g, dsum);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+        const float ls = lse[bh * N_q + i];
+        l2 = ls == -INFINITY ? INFINITY : ls * 1.4426950408889634f;
+    }
+    if (lane == 0) {
+        Dvec[row] = dsum;
+        lse2[row] = l2;
+    }
+}
+
+// ---------------------------------------------------------------- dK, dV
+template <int D, int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                    const BwdParams p) {
+    using C = BCfg<D, KIND>;
+    constexpr int SLOTS = C::SLOTS_KV;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sK = smem;
+    uint8_t* sV = smem + C::TILE;
+    uint8_t* sRing = smem + 2 * C::TILE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + (size_t)SLOTS * C::ITEM_KV);
+    constexpr int NB = 6 + 2 * SLOTS;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + NB);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    const uint32_t b_kv_full = smem_u32(bars);
+    const uint32_t b_s_full = smem_u32(bars + 1);
+    const uint32_t b_p_full = smem_u32(bars + 2);
+    const uint32_t b_acc_done = smem_u32(bars + 3);
+    const uint32_t b_drain = smem_u32(bars + 4);
+    const uint32_t b_item_full = smem_u32(bars + 6);           // + 8 * slot
+    const uint32_t b_item_empty = smem_u32(bars + 6 + SLOTS);  // + 8 * slot
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int b, h, kt;
+    decode(blockIdx.x, p, &b, &h, &kt);  // key tiles: first (heaviest under causal) first
+    const int bh = b * p.H + h;
+    const int key0 = kt * BN;
+    const int shift = p.N_k - p.N_q;
+    // query tiles that see any key of this tile: rows qi >= key0 - shift
+    const int n_qt = (p.N_q + BM - 1) / BM;
+    int i_lo = 0;
+    if (p.causal) {
+        const int first_row = key0 - shift;
+        i_lo = first_row <= 0 ? 0 : first_row / BM;
+    }
+    const int n_steps = (key0 < p.N_k && i_lo < n_qt) ? n_qt - i_lo : 0;
+    const unsigned long long lim = p.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        mbar_init(b_kv_full, 1);
+        mbar_init(b_s_full, 1);
+        mbar_init(b_p_full, 128);
+        mbar_init(b_acc_done, 1);
+        mbar_init(b_drain, 1);
+        for (int s = 0; s < SLOTS; ++s) {
+            mbar_init(b_item_full + 8 * s, 1);
+            mbar_init(b_item_empty + 8 * s, 1);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0 && n_steps > 0) {
+            mbar_arrive_expect_tx(b_kv_full, 2u * C::TILE);
+            for (int c = 0; c < C::NC; ++c) {
+                tma_load_4d(smem_u32(sK + c * C::CHUNK), &tmK, b_kv_full, c * C::CE, h, key0, b);
+                tma_load_4d(smem_u32(sV + c * C::CHUNK), &tmV, b_kv_full, c * C::CE, h, key0, b);
+            }
+            bool ok = true;
+            int s = 0;
+            for (; s < n_steps; ++s) {
+                const int slot = s % SLOTS;
+                if (!wait_bar(b_item_empty + 8 * slot, ((uint32_t)(s / SLOTS) & 1u) ^ 1u, abort_flag, lim)) {
+                    ok = false;
+                    break;
+                }
+                const int q0 = (i_lo + s) * BM;
+                uint8_t* dst = sRing + (size_t)slot * C::ITEM_KV;
+                mbar_arrive_expect_tx(b_item_full + 8 * slot, (uint32_t)C::ITEM_KV);
+                for (int c = 0; c < C::NC; ++c) {
+                    tma_load_4d(smem_u32(dst + c * C::CHUNK), &tmQ, b_item_full + 8 * slot, c * C::CE, h, q0, b);
+                    tma_load_4d(smem_u32(dst + C::TILE + c * C::CHUNK), &tmG, b_item_full + 8 * slot,
+                                c * C::CE, h, q0, b);
+                }
+                const size_t vo = (size_t)bh * p.N_pad + q0;
+                bulk_load(smem_u32(dst + 2 * C::TILE), p.lse2 + vo, 512, b_item_full + 8 * slot);
+                bulk_load(smem_u32(dst + 2 * C::TILE + 512), p.Dvec + vo, 512, b_item_full + 8 * slot);
+            }
+            if (!ok) {
+                wait_drain(b_kv_full, 0, lim);
+                for (int k = (s > SLOTS ? s - SLOTS : 0); k < s; ++k)
+                    wait_drain(b_item_full + 8 * (k % SLOTS), (uint32_t)(k / SLOTS) & 1u, lim);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0 && n_steps > 0) {
+            const uint64_t kd = smem_desc(smem_u32(sK), 16, 8 * C::CB, 2u);
+            const uint64_t vd = smem_desc(smem_u32(sV), 16, 8 * C::CB, 2u);
+            bool ok = wait_bar(b_kv_full, 0, abort_flag, lim);
+            for (int s = 0; s < n_steps && ok; ++s) {
+                const int slot = s % SLOTS;
+                ok = wait_bar(b_item_full + 8 * slot, (uint32_t)(s / SLOTS) & 1u, abort_flag, lim);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t qa = smem_u32(sRing + (size_t)slot * C::ITEM_KV);
+                const uint32_t ga = qa + C::TILE;
+                const uint64_t qd = smem_desc(qa, 16, 8 * C::CB, 2u);
+                const uint64_t gd = smem_desc(ga, 16, 8 * C::CB, 2u);
+                // S^T = K Q^T and dP^T = V dO^T (K-major operands, N = 128 queries)
+#pragma unroll
+                for (int c = 0; c < C::NC; ++c) {
+#pragma unroll
+                    for (int ks = 0; ks < C::CB / 32; ++ks) {
+                        const uint32_t o16 = (uint32_t)(c * C::CHUNK + ks * 32) >> 4;
+                        const uint32_t acc = (c | ks) != 0;
+                        mma_f16_ss(tmem + kColS, kd + o16, qd + o16, C::IDESC_S, acc);
+                        mma_f16_ss(tmem + kColDP, vd + o16, gd + o16, C::IDESC_S, acc);
+                    }
+                }
+                mma_commit(b_s_full);
+                ok = wait_bar(b_p_full, (uint32_t)s & 1u, abort_flag, lim);
+                if (!ok) break;
+                tc_fence_after();
+                // dV += P^T dO, dK += dS^T Q: A from TMEM (K = 128 queries), B MN-major
+                const uint64_t gmn = smem_desc(ga, C::CHUNK, 8 * C::CB, 2u);
+                const uint64_t qmn = smem_desc(qa, C::CHUNK, 8 * C::CB, 2u);
+#pragma unroll
+                for (int ks = 0; ks < BM / C::MMA_K; ++ks) {
+                    const uint32_t o16 = (uint32_t)(ks * C::MMA_K * C::CB) >> 4;
+                    const uint32_t acc = (s > 0 || ks > 0) ? 1u : 0u;
+                    mma_f16_ts(tmem + kColAcc, tmem + kColS + ks * (C::MMA_K / 2), gmn + o16, C::IDESC_ACC, acc);
+                    mma_f16_ts(tmem + kColAcc + D, tmem + kColDP + ks * (C::MMA_K / 2), qmn + o16,
+                               C::IDESC_ACC, acc);
+                }
+                mma_commit(b_item_empty + 8 * slot);
+            }
+            if (ok) {
+                mma_commit(b_acc_done);
+            } else {
+                mma_commit(b_drain);
+                wait_drain(b_drain, 0, lim);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------- elementwise: one key row per thread
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;
+        const int kk = key0 + r;                 // this thread's key
+        const bool key_ok = kk < p.N_k;
+        const uint32_t t_row = tmem + ((uint32_t)(quad * 32) << 16);
+        const float cl = p.scale * 1.4426950408889634f;
+        bool ok = true;
+        for (int s = 0; s < n_steps; ++s) {
+            if (!__all_sync(0xffffffffu, wait_bar(b_s_full, (uint32_t)s & 1u, abort_flag, lim))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int q0 = (i_lo + s) * BM;
+            const float* vl = reinterpret_cast<const float*>(sRing + (size_t)(s % SLOTS) * C::ITEM_KV + 2 * C::TILE);
+            const float* vD = vl + 128;
+            // query column c is allowed for this key iff kk <= q0 + c + shift,
+            // i.e. c > kk - shift - q0 - 1
+            const int c_min = p.causal ? kk - shift - q0 - 1 : -1;
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+                uint32_t sr[64], dr[64];
+                tmem_ld32(t_row + kColS + 64 * v, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                tmem_ld32(t_row + kColS + 64 * v + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                tmem_ld32(t_row + kColDP + 64 * v, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+                tmem_ld32(t_row + kColDP + 64 * v + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+                tmem_ld_wait();
+                reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+                reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+                uint32_t pk[32], dk[32];
+#pragma unroll
+                for (int x = 0; x < 64; x += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4*>(vl + 64 * v + x);
+                    const float4 d4 = *reinterpret_cast<const float4*>(vD + 64 * v + x);
+                    float pv[4], dsv[4];
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                    const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int col = 64 * v + x + e;
+                        const bool allowed = key_ok && col > c_min;
+                        const float pe = allowed ? ex2(fmaf(__uint_as_float(sr[x + e]), cl, -lv[e])) : 0.f;
+                        pv[e] = pe;
+                        dsv[e] = pe * (__uint_as_float(dr[x + e]) - dv[e]);
+                    }
+                    if constexpr (KIND == kBF16) {
+                        pk[x / 2] = pack_bf16(pv[0], pv[1]);
+                        pk[x / 2 + 1] = pack_bf16(pv[2], pv[3]);
+                        dk[x / 2] = pack_bf16(dsv[0], dsv[1]);
+                        dk[x / 2 + 1] = pack_bf16(dsv[2], dsv[3]);
+                    } else {
+                        pk[x / 2] = pack_f16(pv[0], pv[1]);
+                        pk[x / 2 + 1] = pack_f16(pv[2], pv[3]);
+                        dk[x / 2] = pack_f16(dsv[0], dsv[1]);
+                        dk[x / 2 + 1] = pack_f16(dsv[2], dsv[3]);
+                    }
+                }
+                // 64 queries of P^T / dS^T = 32 columns, over columns this
+                // thread has already read
+                tmem_st32(t_row + kColS + 32 * v, pk);
+                tmem_st32(t_row + kColDP + 32 * v, dk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(b_p_full);
+        }
+        // ---- epilogue: dV and scale * dK for this key row
+        if (ok && n_steps > 0)
+            ok = __all_sync(0xffffffffu, wait_bar(b_acc_done, 0u, abort_flag, lim));
+        if (ok) {
+            tc_fence_after();
+            for (int which = 0; which < 2; ++which) {
+                uint16_t* dst = reinterpret_cast<uint16_t*>(which == 0 ? p.out_a : p.out_b) +
+                                (((size_t)b * p.N_k + (key_ok ? kk : 0)) * p.H + h) * D;
+                const float mul = which == 0 ? 1.f : p.scale;
+#pragma unroll 1
+                for (int u = 0; u < D / 32; ++u) {
+                    uint32_t oo[32];
+                    if (n_steps > 0) {
+                        tmem_ld32(t_row + kColAcc + which * D + 32 * u, oo);
+                        tmem_ld_wait();
+                        reg_fence32(oo);
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) oo[x] = 0u;
+                    }
+                    if (!key_ok) continue;
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        const float a0 = __uint_as_float(oo[2 * x]) * mul;
+                        const float a1 = __uint_as_float(oo[2 * x + 1]) * mul;
+                        packed[x] = (KIND == kFP16) ? pack_f16(a0, a1) : pack_bf16(a0, a1);
+                    }
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * u);
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+                        d4[x] = make_uint4(packed[4 * x], packed[4 * x + 1], packed[4 * x + 2], packed[4 * x + 3]);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- dQ
+template <int D, int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                  const BwdParams p) {
+    using C = BCfg<D, KIND>;
+    constexpr int SLOTS = C::SLOTS_Q;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sQ = smem;
+    uint8_t* sG = smem + C::TILE;
+    uint8_t* sRing = smem + 2 * C::TILE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + (size_t)SLOTS * C::ITEM_Q);
+    constexpr int NB = 6 + 2 * SLOTS;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + NB);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    const uint32_t b_q_full = smem_u32(bars);
+    const uint32_t b_s_full = smem_u32(bars + 1);
+    const uint32_t b_p_full = smem_u32(bars + 2);
+    const uint32_t b_acc_done = smem_u32(bars + 3);
+    const uint32_t b_drain = smem_u32(bars + 4);
+    const uint32_t b_item_full = smem_u32(bars + 6);
+    const uint32_t b_item_empty = smem_u32(bars + 6 + SLOTS);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int b, h, rank;
+    decode(blockIdx.x, p, &b, &h, &rank);
+    const int qt = p.causal ? (p.n_units_tiles - 1 - rank) : rank;  // heaviest first
+    const int bh = b * p.H + h;
+    const int q0 = qt * BM;
+    const int shift = p.N_k - p.N_q;
+    int n = 0;  // key tiles this query tile needs
+    if (q0 < p.N_q) {
+        const int last_row = min(q0 + BM - 1, p.N_q - 1);
+        int last_key = p.N_k - 1;
+        if (p.causal) last_key = min(last_key, last_row + shift);
+        n = last_key < 0 ? 0 : last_key / BN + 1;
+    }
+    const unsigned long long lim = p.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        mbar_init(b_q_full, 1);
+        mbar_init(b_s_full, 1);
+        mbar_init(b_p_full, 128);
+        mbar_init(b_acc_done, 1);
+        mbar_init(b_drain, 1);
+        for (int s = 0; s < SLOTS; ++s) {
+            mbar_init(b_item_full + 8 * s, 1);
+            mbar_init(b_item_empty + 8 * s, 1);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0 && n > 0) {
+            mbar_arrive_expect_tx(b_q_full, 2u * C::TILE);
+            for (int c = 0; c < C::NC; ++c) {
+                tma_load_4d(smem_u32(sQ + c * C::CHUNK), &tmQ, b_q_full, c * C::CE, h, q0, b);
+                tma_load_4d(smem_u32(sG + c * C::CHUNK), &tmG, b_q_full, c * C::CE, h, q0, b);
+            }
+            bool ok = true;
+            int j = 0;
+            for (; j < n; ++j) {
+                const int slot = j % SLOTS;
+                if (!wait_bar(b_item_empty + 8 * slot, ((uint32_t)(j / SLOTS) & 1u) ^ 1u, abort_flag, lim)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* dst = sRing + (size_t)slot * C::ITEM_Q;
+                mbar_arrive_expect_tx(b_item_full + 8 * slot, (uint32_t)C::ITEM_Q);
+                for (int c = 0; c < C::NC; ++c) {
+                    tma_load_4d(smem_u32(dst + c * C::CHUNK), &tmK, b_item_full + 8 * slot, c * C::CE, h, j * BN, b);
+                    tma_load_4d(smem_u32(dst + C::TILE + c * C::CHUNK), &tmV, b_item_full + 8 * slot,
+                                c * C::CE, h, j * BN, b);
+                }
+            }
+            if (!ok) {
+                wait_drain(b_q_full, 0, lim);
+                for (int k = (j > SLOTS ? j - SLOTS : 0); k < j; ++k)
+                    wait_drain(b_item_full + 8 * (k % SLOTS), (uint32_t)(k / SLOTS) & 1u, lim);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0 && n > 0) {
+            const uint64_t qd = smem_desc(smem_u32(sQ), 16, 8 * C::CB, 2u);
+            const uint64_t gd = smem_desc(smem_u32(sG), 16, 8 * C::CB, 2u);
+            bool ok = wait_bar(b_q_full, 0, abort_flag, lim);
+            for (int j = 0; j < n && ok; ++j) {
+                const int slot = j % SLOTS;
+                ok = wait_bar(b_item_full + 8 * slot, (uint32_t)(j / SLOTS) & 1u, abort_flag, lim);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t ka = smem_u32(sRing + (size_t)slot * C::ITEM_Q);
+                const uint32_t va = ka + C::TILE;
+                const uint64_t kd = smem_desc(ka, 16, 8 * C::CB, 2u);
+                const uint64_t vd = smem_desc(va, 16, 8 * C::CB, 2u);
+                // S = Q K^T and dP = dO V^T
+#pragma unroll
+                for (int c = 0; c < C::NC; ++c) {
+#pragma unroll
+                    for (int ks = 0; ks < C::CB / 32; ++ks) {
+                        const uint32_t o16 = (uint32_t)(c * C::CHUNK + ks * 32) >> 4;
+                        const uint32_t acc = (c | ks) != 0;
+                        mma_f16_ss(tmem + kColS, qd + o16, kd + o16, C::IDESC_S, acc);
+                        mma_f16_ss(tmem + kColDP, gd + o16, vd + o16, C::IDESC_S, acc);
+                    }
+                }
+                mma_commit(b_s_full);
+                ok = wait_bar(b_p_full, (uint32_t)j & 1u, abort_flag, lim);
+                if (!ok) break;
+                tc_fence_after();
+                // dQ += dS K: A = dS from TMEM (K = 128 keys), B = K MN-major
+                const uint64_t kmn = smem_desc(ka, C::CHUNK, 8 * C::CB, 2u);
+#pragma unroll
+                for (int ks = 0; ks < BN / C::MMA_K; ++ks) {
+                    const uint32_t o16 = (uint32_t)(ks * C::MMA_K * C::CB) >> 4;
+                    const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
+                    mma_f16_ts(tmem + kColAcc, tmem + kColDP + ks * (C::MMA_K / 2), kmn + o16, C::IDESC_ACC, acc);
+                }
+                mma_commit(b_item_empty + 8 * slot);
+            }
+            if (ok) {
+                mma_commit(b_acc_done);
+            } else {
+                mma_commit(b_drain);
+                wait_drain(b_drain, 0, lim);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------- elementwise: one query row per thread
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;
+        const int qi = q0 + r;
+        const bool row_ok = qi < p.N_q;
+        const uint32_t t_row = tmem + ((uint32_t)(quad * 32) << 16);
+        const float cl = p.scale * 1.4426950408889634f;
+        const size_t vo = (size_t)bh * p.N_pad + (row_ok ? qi : 0);
+        const float l2 = row_ok ? p.lse2[vo] : INFINITY;
+        const float Dr = row_ok ? p.Dvec[vo] : 0.f;
+        int row_lim = p.N_k - 1;  // last allowed key of this row
+        if (p.causal) row_lim = min(row_lim, qi + shift);
+        bool ok = true;
+        for (int j = 0; j < n; ++j) {
+            if (!__all_sync(0xffffffffu, wait_bar(b_s_full, (uint32_t)j & 1u, abort_flag, lim))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int cl_max = row_lim - j * BN;  // columns > cl_max are masked
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+                uint32_t sr[64], dr[64];
+                tmem_ld32(t_row + kColS + 64 * v, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                tmem_ld32(t_row + kColS + 64 * v + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                tmem_ld32(t_row + kColDP + 64 * v, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+                tmem_ld32(t_row + kColDP + 64 * v + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+                tmem_ld_wait();
+                reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+                reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+                uint32_t dk[32];
+#pragma unroll
+                for (int x = 0; x < 64; x += 2) {
+                    float ds[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int col = 64 * v + x + e;
+                        const float pe = (row_ok && col <= cl_max)
+                                             ? ex2(fmaf(__uint_as_float(sr[x + e]), cl, -l2))
+                                             : 0.f;
+                        ds[e] = pe * (__uint_as_float(dr[x + e]) - Dr);
+                    }
+                    dk[x / 2] = (KIND == kBF16) ? pack_bf16(ds[0], ds[1]) : pack_f16(ds[0], ds[1]);
+                }
+                tmem_st32(t_row + kColDP + 32 * v, dk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(b_p_full);
+        }
+        if (ok && n > 0) ok = __all_sync(0xffffffffu, wait_bar(b_acc_done, 0u, abort_flag, lim));
+        if (ok) {
+            tc_fence_after();
+            uint16_t* dst = reinterpret_cast<uint16_t*>(p.out_a) +
+                            (((size_t)b * p.N_q + (row_ok ? qi : 0)) * p.H + h) * D;
+#pragma unroll 1
+            for (int u = 0; u < D / 32; ++u) {
+                uint32_t oo[32];
+                if (n > 0) {
+                    tmem_ld32(t_row + kColAcc + 32 * u, oo);
+                    tmem_ld_wait();
+                    reg_fence32(oo);
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) oo[x] = 0u;
+                }
+                if (!row_ok) continue;
+                uint32_t packed[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const float a0 = __uint_as_float(oo[2 * x]) * p.scale;
+                    const float a1 = __uint_as_float(oo[2 * x + 1]) * p.scale;
+                    packed[x] = (KIND == kFP16) ? pack_f16(a0, a1) : pack_bf16(a0, a1);
+                }
+                uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * u);
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+                    d4[x] = make_uint4(packed[4 * x], packed[4 * x + 1], packed[4 * x + 2], packed[4 * x + 3]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// heads scheduled together so the tiles they stream (2 N d E bytes per head)
+// fill ~48 MiB of L2, group sizes evened out
+int heads_per_group(long long n_bh, long long stream_bytes_per_head) {
+    long long G = (48LL << 20) / (stream_bytes_per_head > 0 ? stream_bytes_per_head : 1);
+    if (G < 1) G = 1;
+    if (G > n_bh) G = n_bh;
+    const long long n_groups = (n_bh + G - 1) / G;
+    return (int)((n_bh + n_groups - 1) / n_groups);
+}
+
+template <int D, int KIND>
+cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
+    using C = BCfg<D, KIND>;
+    if (a.N_q == 0) {
+        // no query rows: every key and value gradient is zero
+        const size_t bytes = (size_t)a.B * a.N_k * a.H * D * 2;
+        cudaError_t e0 = cudaMemsetAsync(a.dk, 0, bytes, stream);
+        if (e0 != cudaSuccess) return e0;
+        return cudaMemsetAsync(a.dv, 0, bytes, stream);
+    }
+    const int N_pad = (a.N_q + BM - 1) / BM * BM;
+    float* lse2 = static_cast<float*>(a.workspace);
+    float* Dvec = lse2 + (size_t)a.B * a.H * N_pad;
+    const long long rows = (long long)a.B * a.H * N_pad;
+    bwd_prep_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(a.o, a.dO, a.lse, lse2, Dvec, a.B, a.H,
+                                                                   a.N_q, N_pad, D, KIND == kFP16);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    CUtensorMap mq, mk, mv, mg;
+    if (!tma::encode_map(&mq, a.q, KIND, a.B, a.N_q, a.H, D, C::CE, BM) ||
+        !tma::encode_map(&mk, a.N_k > 0 ? a.k : a.q, KIND, a.B, a.N_k, a.H, D, C::CE, BN) ||
+        !tma::encode_map(&mv, a.N_k > 0 ? a.v : a.q, KIND, a.B, a.N_k, a.H, D, C::CE, BN) ||
+        !tma::encode_map(&mg, a.dO, KIND, a.B, a.N_q, a.H, D, C::CE, BM))
+        return cudaErrorInvalidValue;
+    BwdParams p;
+    p.B = a.B;
+    p.H = a.H;
+    p.N_q = a.N_q;
+    p.N_k = a.N_k;
+    p.N_pad = N_pad;
+    p.causal = a.causal;
+    p.scale = a.scale;
+    p.lse2 = lse2;
+    p.Dvec = Dvec;
+    p.timeout_ns = 2000000000ull;
+    const long long n_bh = (long long)a.B * a.H;
+    // dK, dV: one CTA per key tile; the query side streams Q and dO
+    const int n_kt = (a.N_k + BN - 1) / BN;
+    if (n_kt > 0) {
+        p.n_units_tiles = n_kt;
+        p.heads_per_group = heads_per_group(n_bh, 2LL * a.N_q * D * 2);
+        p.out_a = a.dv;
+        p.out_b = a.dk;
+        const long long n_cta = (long long)n_kt * n_bh;
+        if (n_cta > 0x7fffffffLL) return cudaErrorNotSupported;
+        e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)C::SMEM_KV);
+        if (e != cudaSuccess) return e;
+        bwd_dkdv_kernel<D, KIND><<<(unsigned)n_cta, kThreads, C::SMEM_KV, stream>>>(mq, mk, mv, mg, p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    // dQ: one CTA per query tile; the key side streams K and V
+    const int n_qt = (a.N_q + BM - 1) / BM;
+    p.n_units_tiles = n_qt;
+    p.heads_per_group = heads_per_group(n_bh, 2LL * (a.N_k > 0 ? a.N_k : 1) * D * 2);
+    p.out_a = a.dq;
+    p.out_b = nullptr;
+    const long long n_cta = (long long)n_qt * n_bh;
+    if (n_cta > 0x7fffffffLL) return cudaErrorNotSupported;
+    e = cudaFuncSetAttribute(bwd_dq_kernel<D, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::SMEM_Q);
+    if (e != cudaSuccess) return e;
+    bwd_dq_kernel<D, KIND><<<(unsigned)n_cta, kThreads, C::SMEM_Q, stream>>>(mq, mk, mv, mg, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(long long B, long long H, long long N_q) {
+    const long long N_pad = (N_q + BM - 1) / BM * BM;
+    return (size_t)(2 * B * H * N_pad) * sizeof(float);
+}
+
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
+    if (a.dtype == kBF16) {
+        if (a.d == 64) return launch_bwd_t<64, kBF16>(a, stream);
+        if (a.d == 128) return launch_bwd_t<128, kBF16>(a, stream);
+    } else if (a.dtype == kFP16) {
+        if (a.d == 64) return launch_bwd_t<64, kFP16>(a, stream);
+        if (a.d == 128) return launch_bwd_t<128, kFP16>(a, stream);
+    }
+    return cudaErrorNotSupported;
+}
+
+cudaError_t bwd_take_status(unsigned* out, cudaStream_t stream) {
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_bwd_status, sizeof(unsigned), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyToSymbolAsync(g_bwd_status, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice,
+                                stream);
+    if (e != cudaSuccess) return e;
+    return cudaStreamSynchronize(stream);
+}
+
+}  // namespace attn

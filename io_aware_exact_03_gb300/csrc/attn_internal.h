@@ -43,6 +43,27 @@ cudaError_t launch_tc256(const Problem& p, cudaStream_t stream, int n_splits, fl
                          float* part_lse);
 cudaError_t tc256_take_status(unsigned* out, cudaStream_t stream);
 
+// Backward pass (attn_bwd.cu): dq, dk, dv from q, k, v, o, lse, dO.
+struct BwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* o;
+    const float* lse;
+    const void* dO;
+    void* dq;
+    void* dk;
+    void* dv;
+    int B, H, N_q, N_k, d;
+    float scale;
+    int causal;
+    int dtype;
+    void* workspace;  // bwd_workspace_bytes(B, H, N_q), 16-byte aligned
+};
+size_t bwd_workspace_bytes(long long B, long long H, long long N_q);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+cudaError_t bwd_take_status(unsigned* out, cudaStream_t stream);
+
 // Incoherent processing + per-head e4m3 quantisation (attn_quant.cu).
 cudaError_t launch_quantize_e4m3(const void* x, int dtype, const float* signs, void* codes,
                                  float* descale, int B, int N, int H, int d, cudaStream_t stream);

@@ -4,9 +4,8 @@ TEST INFRASTRUCTURE ONLY.  Only the tests and the benchmark's CPU legs may
 import this module; the GPU product path never calls it and shares no code
 with it.
 
-The pages name training speedups ("FlashAttention-3 (BN)" page, section
-"FlashAttention and FlashAttention-2"; "FlashAttention (HI)" page, section
-"Results") but never write the backward pass out, so this is the plain
+The pages name training speedups ("FlashAttention (HI)" page, section
+"Empirical results") but never write the backward pass out, so this is the plain
 derivative of the forward definition ("FlashAttention (HI)" page, section
 "Problems of standard attention"), O = softmax(scale Q K^T [mask]) V, for an
 upstream gradient dO of the same shape as O.  Per (batch, head), with the

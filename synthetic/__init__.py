@@ -73,6 +73,8 @@ EXTRA_CASES = {
     "LKV": Case("LKV", 1, 8, 512, 65536, 128, False, "bf16", 1101),
     # head dimension 256 (the largest head size the pages name), causal bf16
     "D256": Case("D256", 2, 8, 8192, 8192, 256, True, "bf16", 1102),
+    # backward pass: C3's shape (B2 H16 N4096 d128, causal bf16)
+    "BWD": Case("BWD", 2, 16, 4096, 4096, 128, True, "bf16", 1103),
 }
 
 
@@ -136,6 +138,17 @@ def make_raw_inputs(case: Case) -> dict:
               "k": (case.B, case.N_k, h_kv, case.d),
               "v": (case.B, case.N_k, h_kv, case.d)}
     return {n: _draw(g, shapes[n], case.outliers) for n in ("q", "k", "v")}
+
+
+def make_grad(case: Case) -> torch.Tensor:
+    """Seeded upstream gradient dO [B, N_q, H, d] for the backward pass: fp32
+    randn from its own generator (seed + 500 000, so the forward's q, k, v
+    draws are unchanged), rounded to the case's dtype."""
+    if case.dtype not in ("bf16", "fp16"):
+        raise ValueError("the backward pass takes bf16 or fp16")
+    g = torch.Generator().manual_seed(case.seed + 500_000)
+    x = torch.randn((case.B, case.N_q, case.H, case.d), generator=g, dtype=torch.float32)
+    return x.to(torch.bfloat16 if case.dtype == "bf16" else torch.float16)
 
 
 def random_signs(d: int, seed: int) -> torch.Tensor:
