@@ -149,9 +149,13 @@ __device__ __forceinline__ void decode(long long L, const BwdParams& p, int* b, 
 }
 
 // ---------------------------------------------------------------- prep
+// One warp per row; each lane loads its d / 32 consecutive elements of o and
+// dO with one vector load each (memory-bound: reads o and dO once).
+template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const void* o, const void* dO, const float* lse,
                                                        float* lse2, float* Dvec, int B, int H, int N_q,
-                                                       int N_pad, int d, int fp16) {
+                                                       int N_pad, int fp16) {
+    constexpr int PER = D / 32;  // elements per lane: 2 (d 64) or 4 (d 128)
     const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= (long long)B * H * N_pad) return;
@@ -160,17 +164,29 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const void* o, const void
     float dsum = 0.f, l2 = INFINITY;
     if (i < N_q) {
         const int b = (int)(bh / H), h = (int)(bh % H);
-        const size_t base = (((size_t)b * N_q + i) * H + h) * d;
-        for (int t = lane; t < d; t += 32) {
-            float a, g;
+        const size_t base = (((size_t)b * N_q + i) * H + h) * D + (size_t)lane * PER;
+        uint32_t ow[PER / 2], gw[PER / 2];
+        if constexpr (PER == 4) {
+            const uint2 a2 = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(o) + base);
+            const uint2 g2 = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(dO) + base);
+            ow[0] = a2.x; ow[1] = a2.y; gw[0] = g2.x; gw[1] = g2.y;
+        } else {
+            ow[0] = *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(o) + base);
+            gw[0] = *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(dO) + base);
+        }
+#pragma unroll
+        for (int w = 0; w < PER / 2; ++w) {
+            float a0, a1, g0, g1;
             if (fp16) {
-                a = __half2float(reinterpret_cast<const __half*>(o)[base + t]);
-                g = __half2float(reinterpret_cast<const __half*>(dO)[base + t]);
+                const float2 af = __half22float2(*reinterpret_cast<const __half2*>(&ow[w]));
+                const float2 gf = __half22float2(*reinterpret_cast<const __half2*>(&gw[w]));
+                a0 = af.x; a1 = af.y; g0 = gf.x; g1 = gf.y;
             } else {
-                a = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(o)[base + t]);
-                g = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(dO)[base + t]);
+                const float2 af = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[w]));
+                const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[w]));
+                a0 = af.x; a1 = af.y; g0 = gf.x; g1 = gf.y;
             }
-            dsum = fmaf(a, g, dsum);
+            dsum = fmaf(a0, g0, fmaf(a1, g1, dsum));
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
@@ -203,7 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     const uint32_t b_kv_full = smem_u32(bars);
     const uint32_t b_s_full = smem_u32(bars + 1);
-    const uint32_t b_p_full = smem_u32(bars + 2);
+    // P^T / dS^T of queries [0, 64) and [64, 128): the accumulating MMAs of
+    // the first half run while the elementwise warps form the second
+    const uint32_t b_p_half0 = smem_u32(bars + 2), b_p_half1 = smem_u32(bars + 5);
     const uint32_t b_acc_done = smem_u32(bars + 3);
     const uint32_t b_drain = smem_u32(bars + 4);
     const uint32_t b_item_full = smem_u32(bars + 6);           // + 8 * slot
@@ -228,7 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(b_kv_full, 1);
         mbar_init(b_s_full, 1);
-        mbar_init(b_p_full, 128);
+        mbar_init(b_p_half0, 128);
+        mbar_init(b_p_half1, 128);
         mbar_init(b_acc_done, 1);
         mbar_init(b_drain, 1);
         for (int s = 0; s < SLOTS; ++s) {
@@ -308,20 +327,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 mma_commit(b_s_full);
-                ok = wait_bar(b_p_full, (uint32_t)s & 1u, abort_flag, lim);
-                if (!ok) break;
-                tc_fence_after();
-                // dV += P^T dO, dK += dS^T Q: A from TMEM (K = 128 queries), B MN-major
+                // dV += P^T dO, dK += dS^T Q: A from TMEM (K = 128 queries, in two
+                // halves as the elementwise warps finish them), B MN-major
                 const uint64_t gmn = smem_desc(ga, C::CHUNK, 8 * C::CB, 2u);
                 const uint64_t qmn = smem_desc(qa, C::CHUNK, 8 * C::CB, 2u);
+                for (int half = 0; half < 2 && ok; ++half) {
+                    ok = wait_bar(half ? b_p_half1 : b_p_half0, (uint32_t)s & 1u, abort_flag, lim);
+                    if (!ok) break;
+                    tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < BM / C::MMA_K; ++ks) {
-                    const uint32_t o16 = (uint32_t)(ks * C::MMA_K * C::CB) >> 4;
-                    const uint32_t acc = (s > 0 || ks > 0) ? 1u : 0u;
-                    mma_f16_ts(tmem + kColAcc, tmem + kColS + ks * (C::MMA_K / 2), gmn + o16, C::IDESC_ACC, acc);
-                    mma_f16_ts(tmem + kColAcc + D, tmem + kColDP + ks * (C::MMA_K / 2), qmn + o16,
-                               C::IDESC_ACC, acc);
+                    for (int kh = 0; kh < BM / C::MMA_K / 2; ++kh) {
+                        const int ks = half * (BM / C::MMA_K / 2) + kh;
+                        const uint32_t o16 = (uint32_t)(ks * C::MMA_K * C::CB) >> 4;
+                        const uint32_t acc = (s > 0 || ks > 0) ? 1u : 0u;
+                        mma_f16_ts(tmem + kColAcc, tmem + kColS + ks * (C::MMA_K / 2), gmn + o16,
+                                   C::IDESC_ACC, acc);
+                        mma_f16_ts(tmem + kColAcc + D, tmem + kColDP + ks * (C::MMA_K / 2), qmn + o16,
+                                   C::IDESC_ACC, acc);
+                    }
                 }
+                if (!ok) break;
                 mma_commit(b_item_empty + 8 * slot);
             }
             if (ok) {
@@ -394,13 +419,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 // 64 queries of P^T / dS^T = 32 columns, over columns this
-                // thread has already read
+                // thread has already read; then this half may be consumed
                 tmem_st32(t_row + kColS + 32 * v, pk);
                 tmem_st32(t_row + kColDP + 32 * v, dk);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(v ? b_p_half1 : b_p_half0);
             }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(b_p_full);
         }
         // ---- epilogue: dV and scale * dK for this key row
         if (ok && n_steps > 0)
@@ -467,7 +492,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     const uint32_t b_q_full = smem_u32(bars);
     const uint32_t b_s_full = smem_u32(bars + 1);
-    const uint32_t b_p_full = smem_u32(bars + 2);
+    // dS of keys [0, 64) and [64, 128): the dQ MMAs of the first half run while
+    // the elementwise warps form the second
+    const uint32_t b_p_half0 = smem_u32(bars + 2), b_p_half1 = smem_u32(bars + 5);
     const uint32_t b_acc_done = smem_u32(bars + 3);
     const uint32_t b_drain = smem_u32(bars + 4);
     const uint32_t b_item_full = smem_u32(bars + 6);
@@ -492,7 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(b_q_full, 1);
         mbar_init(b_s_full, 1);
-        mbar_init(b_p_full, 128);
+        mbar_init(b_p_half0, 128);
+        mbar_init(b_p_half1, 128);
         mbar_init(b_acc_done, 1);
         mbar_init(b_drain, 1);
         for (int s = 0; s < SLOTS; ++s) {
@@ -568,17 +596,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 mma_commit(b_s_full);
-                ok = wait_bar(b_p_full, (uint32_t)j & 1u, abort_flag, lim);
-                if (!ok) break;
-                tc_fence_after();
-                // dQ += dS K: A = dS from TMEM (K = 128 keys), B = K MN-major
+                // dQ += dS K: A = dS from TMEM (K = 128 keys, in two halves), B = K MN-major
                 const uint64_t kmn = smem_desc(ka, C::CHUNK, 8 * C::CB, 2u);
+                for (int half = 0; half < 2 && ok; ++half) {
+                    ok = wait_bar(half ? b_p_half1 : b_p_half0, (uint32_t)j & 1u, abort_flag, lim);
+                    if (!ok) break;
+                    tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < BN / C::MMA_K; ++ks) {
-                    const uint32_t o16 = (uint32_t)(ks * C::MMA_K * C::CB) >> 4;
-                    const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
-                    mma_f16_ts(tmem + kColAcc, tmem + kColDP + ks * (C::MMA_K / 2), kmn + o16, C::IDESC_ACC, acc);
+                    for (int kh = 0; kh < BN / C::MMA_K / 2; ++kh) {
+                        const int ks = half * (BN / C::MMA_K / 2) + kh;
+                        const uint32_t o16 = (uint32_t)(ks * C::MMA_K * C::CB) >> 4;
+                        const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
+                        mma_f16_ts(tmem + kColAcc, tmem + kColDP + ks * (C::MMA_K / 2), kmn + o16,
+                                   C::IDESC_ACC, acc);
+                    }
                 }
+                if (!ok) break;
                 mma_commit(b_item_empty + 8 * slot);
             }
             if (ok) {
@@ -637,10 +670,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dk[x / 2] = (KIND == kBF16) ? pack_bf16(ds[0], ds[1]) : pack_f16(ds[0], ds[1]);
                 }
                 tmem_st32(t_row + kColDP + 32 * v, dk);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(v ? b_p_half1 : b_p_half0);
             }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(b_p_full);
         }
         if (ok && n > 0) ok = __all_sync(0xffffffffu, wait_bar(b_acc_done, 0u, abort_flag, lim));
         if (ok) {
@@ -706,8 +739,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
     float* lse2 = static_cast<float*>(a.workspace);
     float* Dvec = lse2 + (size_t)a.B * a.H * N_pad;
     const long long rows = (long long)a.B * a.H * N_pad;
-    bwd_prep_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(a.o, a.dO, a.lse, lse2, Dvec, a.B, a.H,
-                                                                   a.N_q, N_pad, D, KIND == kFP16);
+    bwd_prep_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(a.o, a.dO, a.lse, lse2, Dvec, a.B,
+                                                                      a.H, a.N_q, N_pad, KIND == kFP16);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mv, mg;
