@@ -74,6 +74,10 @@ struct Cfg {
     // Warps: 0 producer; 1 MMA issuer (with P_SMEM: 1 and 2, one per tile,
     // each answering only its own tile's barriers); then 2 x 4 softmax warps.
     static constexpr int ISSUERS = P_SMEM ? 2 : 1;
+    // 16-bit inputs: the O tile (bf16 / fp16) is exactly a Q tile, so the
+    // epilogue stages O in the tile's own Q buffer (free once its last P V is
+    // done) and writes it with one TMA store.
+    static constexpr bool TMA_O = (KIND != kE4M3);
     static constexpr int SOFTMAX_WARP0 = 1 + ISSUERS;
     static constexpr int THREADS = 32 * (SOFTMAX_WARP0 + 8);
     static constexpr int PT = P_SMEM ? BM * BN * E : 0;    // bytes of one P tile
@@ -176,7 +180,8 @@ __device__ __forceinline__ int kv_tiles_for(int q0, const TcParams& p) {
 template <int D, int KIND>
 __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                   const TcParams p) {
     using C = Cfg<D, KIND>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -677,6 +682,26 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
 #pragma unroll
                     for (int x = 0; x < 32; ++x) oo[x] = 0u;
                 }
+                if (C::TMA_O && !split) {
+                    // row r of the 128-byte-swizzled tile in Q_t's buffer: 16-byte
+                    // unit w of d-chunk c sits at unit w ^ (r % 8)
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        const float a0 = __uint_as_float(oo[2 * x]) * inv;
+                        const float a1 = __uint_as_float(oo[2 * x + 1]) * inv;
+                        packed[x] = (KIND == kFP16) ? pack_f16(a0, a1) : pack_bf16(a0, a1);
+                    }
+                    const uint32_t row_base = smem_u32(sQ + t * C::TILE + (u / 2) * C::CHUNK) +
+                                              (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u;
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const int w = (u % 2) * 4 + x;
+                        st_shared_v4(row_base + ((uint32_t)(w ^ (r & 7)) << 4), packed[4 * x],
+                                     packed[4 * x + 1], packed[4 * x + 2], packed[4 * x + 3]);
+                    }
+                    continue;
+                }
                 if (split) {
                     // partial of this split, normalised by its own row sum
                     if (valid) {
@@ -710,6 +735,22 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                 p.part_lse[prow_idx] = lse_row;
             else if (valid && p.lse)
                 p.lse[(size_t)bh * p.N_q + row_g] = lse_row;
+        }
+        if (C::TMA_O && p.n_splits == 1) {
+            // Every thread of the tile reaches this barrier, whether or not its
+            // waits succeeded (a barrier that an aborted warp skipped would
+            // never open).  Then one thread stores the tile from Q_t's buffer
+            // (rows past N_q are not written) and waits until the store has
+            // read shared memory.
+            fence_proxy_async_smem();
+            named_barrier(1 + t, 128);
+            if (r == 0 && ok && !*abort_flag && q0[t] < p.N_q) {
+                for (int c = 0; c < C::NC; ++c)
+                    tma_store_4d(&tmO, smem_u32(sQ + t * C::TILE + c * C::CHUNK), c * (C::CB / C::E),
+                                 h, q0[t], b);
+                bulk_commit_group();
+                bulk_wait_group_read0();
+            }
         }
     }
 
@@ -786,8 +827,13 @@ template <int D, int KIND>
 cudaError_t launch_t(const Problem& pr, cudaStream_t stream, int n_splits = 1,
                      float* part_o = nullptr, float* part_lse = nullptr) {
     using C = Cfg<D, KIND>;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     const int ce = C::CB / C::E;
+    // O has the layout of Q; for 16-bit inputs also its element size
+    if (C::TMA_O && n_splits == 1) {
+        if (!tma::encode_map(&mo, pr.o, KIND, pr.B, pr.N_q, pr.H, D, ce, BM))
+            return cudaErrorInvalidValue;
+    }
     if (!tma::encode_map(&mq, pr.q, KIND, pr.B, pr.N_q, pr.H, D, ce, BM) ||
         !tma::encode_map(&mk, pr.N_k > 0 ? pr.k : pr.q, KIND, pr.B, pr.N_k, pr.H_kv, D, ce, BN) ||
         !tma::encode_map(&mv, pr.N_k > 0 ? pr.v : pr.q, KIND, pr.B, pr.N_k, pr.H_kv, D, ce, BN))
@@ -830,7 +876,8 @@ cudaError_t launch_t(const Problem& pr, cudaStream_t stream, int n_splits = 1,
     if (e != cudaSuccess) return e;
     if (n_splits < 1 || n_splits > 65535) return cudaErrorInvalidValue;
     dim3 grid((unsigned)n_cta, (unsigned)n_splits);
-    attn_tc_kernel<D, KIND><<<grid, C::THREADS, C::SMEM, stream>>>(mq, mk, mv, p);
+    if (!(C::TMA_O && n_splits == 1)) mo = mq;  // not read
+    attn_tc_kernel<D, KIND><<<grid, C::THREADS, C::SMEM, stream>>>(mq, mk, mv, mo, p);
     return cudaGetLastError();
 }
 
