@@ -173,7 +173,7 @@ ATTN_API size_t attn_splitkv_workspace_bytes(int B, int H, int N_q, int d, int n
  * Outputs dq [B, N_q, H, d], dk, dv [B, N_k, H, d], in dtype (bf16 or fp16;
  * ATTN_FP8_E4M3 gives ATTN_ERR_UNSUPPORTED), fp32 accumulation.  A key no
  * query row may attend gets dk = dv = 0; a query row with no allowed key gets
- * dq = 0.  d must be 64 or 128; H_kv = H.
+ * dq = 0.  d must be 64 or 128; k, v have H heads (attn_bwd_gqa for fewer).
  * workspace: caller-allocated device memory of at least
  * attn_bwd_workspace_bytes(B, H, N_q) bytes, 16-byte aligned, overwritten
  * (fp32 lse * log2(e) and D per row, each padded to a multiple of 128 rows).
@@ -186,7 +186,18 @@ ATTN_API attn_status_t attn_bwd(const void* q, const void* k, const void* v, con
                                 attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
                                 void* stream);
 
-/* Workspace bytes attn_bwd needs (0 for invalid arguments). */
+/* attn_bwd for grouped-query / multi-query attention: k, v, dk, dv are
+ * [B, N_k, H_kv, d] with H % H_kv == 0; query head h uses K/V head
+ * h / (H / H_kv), and dk, dv of a K/V head sum the contributions of its
+ * H / H_kv query heads (each summed in one CTA: still deterministic).
+ * ATTN_ERR_INVALID_ARG if H_kv < 1 or H % H_kv != 0.  Otherwise as attn_bwd. */
+ATTN_API attn_status_t attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                                    const float* lse, const void* dO, void* dq, void* dk,
+                                    void* dv, int B, int H, int H_kv, int N_q, int N_k, int d,
+                                    float scale, int causal, attn_dtype_t dtype, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
+/* Workspace bytes attn_bwd and attn_bwd_gqa need (0 for invalid arguments). */
 ATTN_API size_t attn_bwd_workspace_bytes(int B, int H, int N_q);
 
 /* Size of the fixed scratch array attn_fwd_splitkv_static uses (bytes). */

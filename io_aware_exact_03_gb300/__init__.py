@@ -78,6 +78,9 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz,
                                vp]
         L.attn_bwd.restype = i
+        L.attn_bwd_gqa.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i,
+                                   vp, sz, vp]
+        L.attn_bwd_gqa.restype = i
         L.attn_bwd_workspace_bytes.argtypes = [i, i, i]
         L.attn_bwd_workspace_bytes.restype = sz
         L.attn_selftest_wait.argtypes = [ctypes.c_uint, vp]
@@ -275,9 +278,11 @@ def attn_bwd_workspace_bytes(B, H, N_q):
 
 def attn_bwd(q, k, v, o, lse, dO, scale=None, causal=False, dq=None, dk=None, dv=None,
              workspace=None, stream=None):
-    """Backward pass: (dq, dk, dv) for upstream gradient dO; o and lse from attn_fwd."""
+    """Backward pass: (dq, dk, dv) for upstream gradient dO; o and lse from attn_fwd
+    (or attn_fwd_gqa: k, v may have H_kv heads dividing H)."""
     torch = _torch()
-    B, N_q, H, d, N_k = _check_inputs(q, k, v)
+    B, N_q, H, d, N_k = _check_inputs(q, k, v, gqa=True)
+    H_kv = k.shape[2]
     for name, t, shape in (("o", o, q.shape), ("dO", dO, q.shape)):
         if tuple(t.shape) != tuple(shape) or t.dtype != q.dtype or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous {q.dtype} tensor of shape {tuple(shape)}")
@@ -291,9 +296,9 @@ def attn_bwd(q, k, v, o, lse, dO, scale=None, causal=False, dq=None, dk=None, dv
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()
-    st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
-                        _ptr(dk), _ptr(dv), B, H, N_q, N_k, d, scale, int(bool(causal)),
-                        _dtype_code(q), _ptr(workspace), ws_bytes, _stream(stream, q.device))
+    st = lib().attn_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                            _ptr(dk), _ptr(dv), B, H, H_kv, N_q, N_k, d, scale, int(bool(causal)),
+                            _dtype_code(q), _ptr(workspace), ws_bytes, _stream(stream, q.device))
     _raise(st, "attn_bwd")
     return dq, dk, dv
 

@@ -176,12 +176,13 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N_q) {
     return attn::bwd_workspace_bytes(B, H, N_q);
 }
 
-attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                       const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
-                       int H, int N_q, int N_k, int d, float scale, int causal,
-                       attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
-                       void* stream) {
+attn_status_t attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                           int B, int H, int H_kv, int N_q, int N_k, int d, float scale,
+                           int causal, attn_dtype_t dtype, void* workspace,
+                           size_t workspace_bytes, void* stream) {
     if (B < 0 || H < 0 || N_q < 0 || N_k < 0) return ATTN_ERR_INVALID_ARG;
+    if (H_kv < 1 || (H > 0 && H % H_kv != 0)) return ATTN_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     if (dtype != ATTN_BF16 && dtype != ATTN_FP16) {
         if (dtype == ATTN_FP8_E4M3) return ATTN_ERR_UNSUPPORTED;
@@ -215,6 +216,7 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
     a.N_q = N_q;
     a.N_k = N_k;
     a.d = d;
+    a.H_kv = H_kv;
     a.scale = scale;
     a.causal = causal ? 1 : 0;
     a.dtype = (int)dtype;
@@ -222,6 +224,15 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
     cudaError_t e = attn::launch_bwd(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) (void)cudaGetLastError();
     return from_cuda(e);
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                       int H, int N_q, int N_k, int d, float scale, int causal,
+                       attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+    return attn_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, B, H, H > 0 ? H : 1, N_q, N_k, d, scale,
+                        causal, dtype, workspace, workspace_bytes, stream);
 }
 
 attn_status_t attn_selftest_wait(unsigned timeout_us, void* stream) {

@@ -85,6 +85,8 @@ constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256;
 
 struct BwdParams {
     int B, H, N_q, N_k, N_pad;
+    int H_kv;             // K/V heads; query head h uses K/V head h / group
+    int group;            // H / H_kv
     int n_units_tiles;    // key tiles (dkdv) or query tiles (dq)
     int heads_per_group;
     int causal;
@@ -125,10 +127,11 @@ __device__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long lim
     }
 }
 
-// unit L -> (b, h, tile rank) in groups of heads_per_group heads, the tile
-// rank the slow coordinate inside a group
-__device__ __forceinline__ void decode(long long L, const BwdParams& p, int* b, int* h, int* rank) {
-    const long long n_bh = (long long)p.B * p.H;
+// unit L -> (b, head, tile rank) over n_heads heads per batch, in groups of
+// heads_per_group heads, the tile rank the slow coordinate inside a group
+__device__ __forceinline__ void decode(long long L, const BwdParams& p, int n_heads, int* b, int* h,
+                                       int* rank) {
+    const long long n_bh = (long long)p.B * n_heads;
     const long long G = p.heads_per_group;
     const long long per_group = (long long)p.n_units_tiles * G;
     const long long n_full = n_bh / G;
@@ -144,8 +147,8 @@ __device__ __forceinline__ void decode(long long L, const BwdParams& p, int* b, 
     }
     *rank = (int)(rem / Gg);
     const int bh = (int)(g * G + rem % Gg);
-    *b = bh / p.H;
-    *h = bh % p.H;
+    *b = bh / n_heads;
+    *h = bh % n_heads;
 }
 
 // ---------------------------------------------------------------- prep
@@ -228,9 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t b_item_empty = smem_u32(bars + 6 + SLOTS);  // + 8 * slot
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int b, h, kt;
-    decode(blockIdx.x, p, &b, &h, &kt);  // key tiles: first (heaviest under causal) first
-    const int bh = b * p.H + h;
+    int b, hk, kt;
+    decode(blockIdx.x, p, p.H_kv, &b, &hk, &kt);  // key tiles: first (heaviest under causal) first
     const int key0 = kt * BN;
     const int shift = p.N_k - p.N_q;
     // query tiles that see any key of this tile: rows qi >= key0 - shift
@@ -240,7 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int first_row = key0 - shift;
         i_lo = first_row <= 0 ? 0 : first_row / BM;
     }
-    const int n_steps = (key0 < p.N_k && i_lo < n_qt) ? n_qt - i_lo : 0;
+    // per query head of the K/V head's group: query tiles i_lo .. n_qt - 1
+    const int per_head = (key0 < p.N_k && i_lo < n_qt) ? n_qt - i_lo : 0;
+    const int n_steps = per_head * p.group;
     const unsigned long long lim = p.timeout_ns;
 
     if (threadIdx.x == 0) {
@@ -271,8 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && n_steps > 0) {
             mbar_arrive_expect_tx(b_kv_full, 2u * C::TILE);
             for (int c = 0; c < C::NC; ++c) {
-                tma_load_4d(smem_u32(sK + c * C::CHUNK), &tmK, b_kv_full, c * C::CE, h, key0, b);
-                tma_load_4d(smem_u32(sV + c * C::CHUNK), &tmV, b_kv_full, c * C::CE, h, key0, b);
+                tma_load_4d(smem_u32(sK + c * C::CHUNK), &tmK, b_kv_full, c * C::CE, hk, key0, b);
+                tma_load_4d(smem_u32(sV + c * C::CHUNK), &tmV, b_kv_full, c * C::CE, hk, key0, b);
             }
             bool ok = true;
             int s = 0;
@@ -282,7 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                const int q0 = (i_lo + s) * BM;
+                const int h = hk * p.group + s / per_head;  // query head of this step
+                const int q0 = (i_lo + s % per_head) * BM;
                 uint8_t* dst = sRing + (size_t)slot * C::ITEM_KV;
                 mbar_arrive_expect_tx(b_item_full + 8 * slot, (uint32_t)C::ITEM_KV);
                 for (int c = 0; c < C::NC; ++c) {
@@ -290,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_4d(smem_u32(dst + C::TILE + c * C::CHUNK), &tmG, b_item_full + 8 * slot,
                                 c * C::CE, h, q0, b);
                 }
-                const size_t vo = (size_t)bh * p.N_pad + q0;
+                const size_t vo = ((size_t)b * p.H + h) * p.N_pad + q0;
                 bulk_load(smem_u32(dst + 2 * C::TILE), p.lse2 + vo, 512, b_item_full + 8 * slot);
                 bulk_load(smem_u32(dst + 2 * C::TILE + 512), p.Dvec + vo, 512, b_item_full + 8 * slot);
             }
@@ -372,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const int q0 = (i_lo + s) * BM;
+            const int q0 = (i_lo + s % per_head) * BM;
             const float* vl = reinterpret_cast<const float*>(sRing + (size_t)(s % SLOTS) * C::ITEM_KV + 2 * C::TILE);
             const float* vD = vl + 128;
             // query column c is allowed for this key iff kk <= q0 + c + shift,
@@ -434,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             for (int which = 0; which < 2; ++which) {
                 uint16_t* dst = reinterpret_cast<uint16_t*>(which == 0 ? p.out_a : p.out_b) +
-                                (((size_t)b * p.N_k + (key_ok ? kk : 0)) * p.H + h) * D;
+                                (((size_t)b * p.N_k + (key_ok ? kk : 0)) * p.H_kv + hk) * D;
                 const float mul = which == 0 ? 1.f : p.scale;
 #pragma unroll 1
                 for (int u = 0; u < D / 32; ++u) {
@@ -502,7 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int b, h, rank;
-    decode(blockIdx.x, p, &b, &h, &rank);
+    decode(blockIdx.x, p, p.H, &b, &h, &rank);
+    const int hk = h / p.group;  // K/V head
     const int qt = p.causal ? (p.n_units_tiles - 1 - rank) : rank;  // heaviest first
     const int bh = b * p.H + h;
     const int q0 = qt * BM;
@@ -558,9 +564,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* dst = sRing + (size_t)slot * C::ITEM_Q;
                 mbar_arrive_expect_tx(b_item_full + 8 * slot, (uint32_t)C::ITEM_Q);
                 for (int c = 0; c < C::NC; ++c) {
-                    tma_load_4d(smem_u32(dst + c * C::CHUNK), &tmK, b_item_full + 8 * slot, c * C::CE, h, j * BN, b);
+                    tma_load_4d(smem_u32(dst + c * C::CHUNK), &tmK, b_item_full + 8 * slot, c * C::CE, hk, j * BN, b);
                     tma_load_4d(smem_u32(dst + C::TILE + c * C::CHUNK), &tmV, b_item_full + 8 * slot,
-                                c * C::CE, h, j * BN, b);
+                                c * C::CE, hk, j * BN, b);
                 }
             }
             if (!ok) {
@@ -730,7 +736,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
     using C = BCfg<D, KIND>;
     if (a.N_q == 0) {
         // no query rows: every key and value gradient is zero
-        const size_t bytes = (size_t)a.B * a.N_k * a.H * D * 2;
+        const size_t bytes = (size_t)a.B * a.N_k * a.H_kv * D * 2;
         cudaError_t e0 = cudaMemsetAsync(a.dk, 0, bytes, stream);
         if (e0 != cudaSuccess) return e0;
         return cudaMemsetAsync(a.dv, 0, bytes, stream);
@@ -745,13 +751,15 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mv, mg;
     if (!tma::encode_map(&mq, a.q, KIND, a.B, a.N_q, a.H, D, C::CE, BM) ||
-        !tma::encode_map(&mk, a.N_k > 0 ? a.k : a.q, KIND, a.B, a.N_k, a.H, D, C::CE, BN) ||
-        !tma::encode_map(&mv, a.N_k > 0 ? a.v : a.q, KIND, a.B, a.N_k, a.H, D, C::CE, BN) ||
+        !tma::encode_map(&mk, a.N_k > 0 ? a.k : a.q, KIND, a.B, a.N_k, a.H_kv, D, C::CE, BN) ||
+        !tma::encode_map(&mv, a.N_k > 0 ? a.v : a.q, KIND, a.B, a.N_k, a.H_kv, D, C::CE, BN) ||
         !tma::encode_map(&mg, a.dO, KIND, a.B, a.N_q, a.H, D, C::CE, BM))
         return cudaErrorInvalidValue;
     BwdParams p;
     p.B = a.B;
     p.H = a.H;
+    p.H_kv = a.H_kv;
+    p.group = a.H / a.H_kv;
     p.N_q = a.N_q;
     p.N_k = a.N_k;
     p.N_pad = N_pad;
@@ -761,14 +769,16 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
     p.Dvec = Dvec;
     p.timeout_ns = 2000000000ull;
     const long long n_bh = (long long)a.B * a.H;
-    // dK, dV: one CTA per key tile; the query side streams Q and dO
+    // dK, dV: one CTA per (K/V head, key tile); the query side streams Q and
+    // dO of the group's query heads
+    const long long n_bhk = (long long)a.B * a.H_kv;
     const int n_kt = (a.N_k + BN - 1) / BN;
     if (n_kt > 0) {
         p.n_units_tiles = n_kt;
-        p.heads_per_group = heads_per_group(n_bh, 2LL * a.N_q * D * 2);
+        p.heads_per_group = heads_per_group(n_bhk, 2LL * a.N_q * D * 2 * p.group);
         p.out_a = a.dv;
         p.out_b = a.dk;
-        const long long n_cta = (long long)n_kt * n_bh;
+        const long long n_cta = (long long)n_kt * n_bhk;
         if (n_cta > 0x7fffffffLL) return cudaErrorNotSupported;
         e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)C::SMEM_KV);
@@ -780,7 +790,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
     // dQ: one CTA per query tile; the key side streams K and V
     const int n_qt = (a.N_q + BM - 1) / BM;
     p.n_units_tiles = n_qt;
-    p.heads_per_group = heads_per_group(n_bh, 2LL * (a.N_k > 0 ? a.N_k : 1) * D * 2);
+    p.heads_per_group = heads_per_group(n_bh, 2LL * (a.N_k > 0 ? a.N_k : 1) * D * 2 / p.group);
     p.out_a = a.dq;
     p.out_b = nullptr;
     const long long n_cta = (long long)n_qt * n_bh;

@@ -55,6 +55,7 @@ struct BwdArgs {
     void* dk;
     void* dv;
     int B, H, N_q, N_k, d;
+    int H_kv;         // K/V heads (H % H_kv == 0): dk, dv sum over the group's query heads
     float scale;
     int causal;
     int dtype;

@@ -125,3 +125,36 @@ def test_fp8_backward_is_refused():
     st = attn.lib().attn_bwd(P(q), P(q), P(q), P(o), P(lse), P(o), P(o), P(o), P(o), 1, 1, 128, 128,
                              64, 0.125, 0, attn.ATTN_FP8_E4M3, P(ws), ws.numel(), None)
     assert st == attn.ATTN_ERR_UNSUPPORTED
+
+
+GQA = [
+    # B, H, H_kv, N_q, N_k, d, causal, dtype
+    (2, 8, 2, 300, 300, 128, True, "bf16"),
+    (1, 6, 1, 257, 500, 64, False, "fp16"),     # multi-query
+    (1, 4, 2, 200, 130, 64, True, "bf16"),      # rows with no key
+]
+
+
+@pytest.mark.parametrize("shape", GQA, ids=lambda s: "x".join(map(str, s)))
+def test_backward_gqa_matches_oracle(shape):
+    """K/V shared by H / H_kv query heads: the oracle differentiates the
+    expanded problem (each query head with its own copy of its K/V head) and
+    sums dk, dv over the copies, which is the gradient of the shared tensors."""
+    B, H, H_kv, N_q, N_k, d, causal, dtype = shape
+    case = synthetic.custom_case(B, H, N_q, N_k, d, causal, dtype, outliers=False, H_kv=H_kv,
+                                 seed=zlib.crc32(repr(shape).encode()) % 10000)
+    inputs = synthetic.make_inputs(case)
+    dO = synthetic.make_grad(case)
+    dev = {k: v.cuda() for k, v in inputs.items() if isinstance(v, torch.Tensor)}
+    o, lse = attn.attn_fwd_gqa(dev["q"], dev["k"], dev["v"], scale=case.scale, causal=causal)
+    dq, dk, dv = attn.attn_bwd(dev["q"], dev["k"], dev["v"], o, lse, dO.cuda(), scale=case.scale,
+                               causal=causal)
+    attn.attn_check_status()
+    got = [t.double().cpu().numpy() for t in (dq, dk, dv)]
+    q, k, v = oracle.case_inputs_f64(inputs)
+    g = H // H_kv
+    rq, rk, rv = backward.attention_backward(q, np.repeat(k, g, axis=2), np.repeat(v, g, axis=2),
+                                             oracle.to_f64(dO), case.scale, causal)
+    rk = rk.reshape(B, N_k, H_kv, g, d).sum(axis=3)
+    rv = rv.reshape(B, N_k, H_kv, g, d).sum(axis=3)
+    _compare(got, [rq, rk, rv], repr(shape))
