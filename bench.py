@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--case", choices=["C1", "C2", "C3", "C4", "C5", "LKV", "D256", "BWD"], default=None,
+    ap.add_argument("--case", choices=["C1", "C2", "C3", "C4", "C5", "LKV", "D256", "D256F", "BWD"], default=None,
                     help="measure one workload case alone instead of the C4 + C5 step")
     ap.add_argument("--splits", type=int, default=1,
                     help="with --case: split each query tile's K/V range over this many CTAs")

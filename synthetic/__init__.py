@@ -73,6 +73,8 @@ EXTRA_CASES = {
     "LKV": Case("LKV", 1, 8, 512, 65536, 128, False, "bf16", 1101),
     # head dimension 256 (the largest head size the pages name), causal bf16
     "D256": Case("D256", 2, 8, 8192, 8192, 256, True, "bf16", 1102),
+    # head dimension 256 in e4m3 (non-causal, 0.1 % x10 outliers like C5)
+    "D256F": Case("D256F", 2, 8, 8192, 8192, 256, False, "e4m3", 1104, outliers=True),
     # backward pass: C3's shape (B2 H16 N4096 d128, causal bf16)
     "BWD": Case("BWD", 2, 16, 4096, 4096, 128, True, "bf16", 1103),
 }

@@ -44,8 +44,9 @@ def test_case_sampled(name, impl):
     check_sampled(synthetic.CASES[name], impl)
 
 
-def test_d256_workload_sampled():
-    check_sampled(synthetic.EXTRA_CASES["D256"], "tc")
+@pytest.mark.parametrize("name", ["D256", "D256F"])
+def test_d256_workload_sampled(name):
+    check_sampled(synthetic.EXTRA_CASES[name], "tc")
 
 
 EDGE = [
