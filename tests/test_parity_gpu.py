@@ -198,3 +198,26 @@ def test_gqa_matches_oracle(shape):
     O, lse = run_gpu(case, to_device(inputs), "gqa")
     O_ref, lse_ref = oracle_full(case, inputs)
     compare(case, O, lse, O_ref, lse_ref)
+
+
+def test_c5_full_output_error_distribution():
+    """Every row of C5, not a sample: the e4m3 tensor-core kernel against the
+    CUDA-core kernel (fp32 scores and P, within 2.6e-2 of the oracle on C5's
+    worst rows).  e4m3 P carries 3 mantissa bits, so a weight is off by up to
+    2^-4 of itself, and with C5's x10 outliers |v| reaches ~42: on a row where
+    an outlier value carries a large weight the O error exceeds the 6e-2 that
+    holds on the seeded sample (measured: 80 of 262144 rows, max 0.31).  This
+    pins the distribution so it cannot silently widen."""
+    case = synthetic.CASES["C5"]
+    dev = to_device(synthetic.make_inputs(case))
+    o1, _ = attn.attn_fwd_fp8(dev["q"], dev["k"], dev["v"], dev["q_descale"], dev["k_descale"],
+                              dev["v_descale"], scale=case.scale)
+    o2, _ = attn.attn_fwd_simt(dev["q"], dev["k"], dev["v"], scale=case.scale,
+                               q_descale=dev["q_descale"], k_descale=dev["k_descale"],
+                               v_descale=dev["v_descale"])
+    attn.attn_check_status()
+    rowmax = (o1.float() - o2.float()).abs().amax(dim=3).flatten()
+    assert rowmax.median().item() <= 5e-3
+    assert torch.quantile(rowmax.cpu(), 0.999).item() <= 6e-2
+    assert (rowmax > 6e-2).float().mean().item() <= 1e-3
+    assert rowmax.max().item() <= 0.5
