@@ -200,6 +200,39 @@ ATTN_API attn_status_t attn_bwd_gqa(const void* q, const void* k, const void* v,
 /* Workspace bytes attn_bwd and attn_bwd_gqa need (0 for invalid arguments). */
 ATTN_API size_t attn_bwd_workspace_bytes(int B, int H, int N_q);
 
+/* Forward pass on HOST-resident tensors (the same operation and layouts as
+ * attn_fwd / attn_fwd_fp8, with q, k, v, o, lse and, for ATTN_FP8_E4M3, the
+ * three descale arrays of B*H floats in host memory; H_kv = H).  Host buffers
+ * should be page-locked (cudaHostAlloc / pinned), or the copies cannot overlap.
+ *
+ * The (batch, head) pairs are cut into about four chunks of whole heads of
+ * one batch row.  Over a ring of three device slots in `workspace`, the copy
+ * of chunk c + 1 to the device (an internal stream), the kernel on chunk c
+ * (on `stream`) and the copy of chunk c - 1 back to the host (a second
+ * internal stream) run at the same time.  Every (batch, head) is computed as
+ * attn_fwd computes it, so the results equal those of attn_fwd on device
+ * copies of the inputs bit for bit.
+ *
+ * workspace: device memory of attn_fwd_host_workspace_bytes(...) bytes,
+ *   256-byte aligned, owned by the caller, overwritten.  lse may be NULL.
+ * Ordering: the copies start after the work already queued on `stream`; work
+ *   queued on `stream` afterwards sees o and lse written in host memory (for
+ *   example a cudaStreamSynchronize(stream) before the host reads them).
+ * Threads: calls on one device from several host threads are enqueued one
+ *   after the other (an internal lock per device).
+ * Errors: as attn_fwd, plus ATTN_ERR_INVALID_ARG for a missing, misaligned or
+ *   short workspace; ATTN_ERR_CUDA if a copy or an internal stream or event
+ *   cannot be set up. */
+ATTN_API attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o,
+                                     float* lse, const float* q_descale, const float* k_descale,
+                                     const float* v_descale, int B, int H, int N_q, int N_k, int d,
+                                     float scale, int causal, attn_dtype_t dtype, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+/* Workspace bytes attn_fwd_host needs (0 for invalid or empty arguments). */
+ATTN_API size_t attn_fwd_host_workspace_bytes(int B, int H, int N_q, int N_k, int d,
+                                              attn_dtype_t dtype);
+
 /* Size of the fixed scratch array attn_fwd_splitkv_static uses (bytes). */
 #define ATTN_STATIC_SCRATCH_BYTES (32 * 1024 * 1024)
 

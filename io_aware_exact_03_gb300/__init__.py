@@ -23,7 +23,7 @@ from . import ext_build as _build
 __all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_simt", "attn_fwd_splitkv", "attn_fwd_gqa",
            "attn_quantize_e4m3",
            "attn_splitkv_workspace_bytes", "attn_check_status", "attn_status_string",
-           "attn_bwd", "attn_bwd_workspace_bytes",
+           "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_host", "attn_fwd_host_workspace_bytes",
            "AttnError", "lib", "build"]
 
 (ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT,
@@ -83,6 +83,10 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd_gqa.restype = i
         L.attn_bwd_workspace_bytes.argtypes = [i, i, i]
         L.attn_bwd_workspace_bytes.restype = sz
+        L.attn_fwd_host.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, i, i, i, i, i, f, i, i, vp, sz, vp]
+        L.attn_fwd_host.restype = i
+        L.attn_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        L.attn_fwd_host_workspace_bytes.restype = sz
         L.attn_selftest_wait.argtypes = [ctypes.c_uint, vp]
         L.attn_selftest_wait.restype = i
         L.attn_check_status.argtypes = [vp]
@@ -274,6 +278,64 @@ def attn_fwd_splitkv(q, k, v, num_splits, o=None, lse=None, scale=None, causal=F
 
 def attn_bwd_workspace_bytes(B, H, N_q):
     return int(lib().attn_bwd_workspace_bytes(int(B), int(H), int(N_q)))
+
+
+def attn_fwd_host_workspace_bytes(B, H, N_q, N_k, d, dtype_code) -> int:
+    return int(lib().attn_fwd_host_workspace_bytes(int(B), int(H), int(N_q), int(N_k), int(d),
+                                                   int(dtype_code)))
+
+
+def attn_fwd_host(q, k, v, o=None, lse=None, scale=None, causal=False, q_descale=None,
+                  k_descale=None, v_descale=None, workspace=None, stream=None, device=None):
+    """Forward pass on host (CPU) tensors, copies pipelined with the kernel.
+
+    q, k, v: contiguous CPU tensors [B, N, H, d] (pinned for overlap); for
+    float8_e4m3fn inputs the descales are CPU float32 tensors of B*H values.
+    o, lse: CPU outputs (allocated pinned when not given).  workspace: a CUDA
+    tensor of at least attn_fwd_host_workspace_bytes(...) bytes (allocated
+    when not given).  The call returns once the work is queued on `stream`;
+    synchronise that stream before reading o and lse.
+    """
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-D CPU tensor [B, N, H, d]")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    B, N_q, H, d = q.shape
+    N_k = k.shape[1]
+    if k.shape != v.shape or tuple(k.shape) != (B, N_k, H, d):
+        raise ValueError("k and v must be [B, N_k, H, d] matching q")
+    code = _dtype_code(q)
+    fp8 = code == ATTN_FP8_E4M3
+    if fp8:
+        for name, t in (("q_descale", q_descale), ("k_descale", k_descale), ("v_descale", v_descale)):
+            if t is None or t.is_cuda or t.dtype != torch.float32 or t.numel() != B * H or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous CPU float32 tensor of B*H values")
+    out_dtype = torch.float16 if q.dtype == torch.float16 else torch.bfloat16
+    if o is None:
+        o = torch.empty((B, N_q, H, d), dtype=out_dtype).pin_memory()
+    if lse is None:
+        lse = torch.empty((B, H, N_q), dtype=torch.float32).pin_memory()
+    if o.is_cuda or o.dtype != out_dtype or tuple(o.shape) != (B, N_q, H, d) or not o.is_contiguous():
+        raise ValueError("o must be a contiguous CPU [B, N_q, H, d] tensor of the output dtype")
+    if lse.is_cuda or lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N_q) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous CPU float32 [B, H, N_q] tensor")
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    ws_bytes = attn_fwd_host_workspace_bytes(B, H, N_q, N_k, d, code)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device)
+    elif workspace.numel() * workspace.element_size() < ws_bytes:
+        raise ValueError(f"workspace needs {ws_bytes} bytes")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    with torch.cuda.device(device):
+        st = lib().attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                 _ptr(q_descale if fp8 else None), _ptr(k_descale if fp8 else None),
+                                 _ptr(v_descale if fp8 else None), B, H, N_q, N_k, d, scale,
+                                 int(bool(causal)), code, _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream, device))
+    _raise(st, "attn_fwd_host")
+    return o, lse
 
 
 def attn_bwd(q, k, v, o, lse, dO, scale=None, causal=False, dq=None, dk=None, dv=None,

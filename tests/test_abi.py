@@ -143,3 +143,36 @@ def test_quantiser_rejects_bad_arguments(L):
     assert L.attn_quantize_e4m3(P, attn.ATTN_FP32, P + 4, P, 1, 4, 1, 64, None, None) == attn.ATTN_ERR_INVALID_ARG
     assert L.attn_quantize_e4m3(P, attn.ATTN_FP32, P, None, 1, 4, 1, 64, None, None) == attn.ATTN_ERR_INVALID_ARG
     assert L.attn_quantize_e4m3(None, attn.ATTN_FP32, None, None, 0, 4, 1, 64, None, None) == attn.ATTN_OK
+
+
+def test_host_forward_rejects_bad_arguments(L):
+    # every check below returns before any CUDA call (no GPU needed)
+    ws = 0x100000  # 256-byte aligned fake device address
+    big = 1 << 40
+
+    def call(q=P, k=P, v=P, o=P, lse=P, qd=None, kd=None, vd=None, B=1, H=4, N_q=64, N_k=64,
+             d=128, scale=0.125, dtype=0, w=ws, wb=big):
+        return L.attn_fwd_host(q, k, v, o, lse, qd, kd, vd, B, H, N_q, N_k, d, scale, 0, dtype, w,
+                               wb, None)
+
+    assert call(scale=0.0) == attn.ATTN_ERR_INVALID_ARG
+    assert call(scale=float("inf")) == attn.ATTN_ERR_INVALID_ARG
+    assert call(d=32) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(dtype=3) == attn.ATTN_ERR_INVALID_ARG
+    assert call(q=None) == attn.ATTN_ERR_INVALID_ARG
+    assert call(dtype=2) == attn.ATTN_ERR_INVALID_ARG          # e4m3 without descales
+    assert call(w=None) == attn.ATTN_ERR_INVALID_ARG
+    assert call(w=ws + 16) == attn.ATTN_ERR_INVALID_ARG        # workspace not 256-byte aligned
+    need = L.attn_fwd_host_workspace_bytes(1, 4, 64, 64, 128, 0)
+    assert call(wb=need - 1) == attn.ATTN_ERR_INVALID_ARG
+    assert call(B=0) == attn.ATTN_OK and call(N_q=0) == attn.ATTN_OK
+
+
+def test_host_forward_workspace_bytes(L):
+    f = L.attn_fwd_host_workspace_bytes
+    assert f(0, 4, 64, 64, 128, 0) == 0 and f(1, 4, 64, 64, 32, 0) == 0 and f(1, 4, 64, 64, 128, 3) == 0
+    # bf16, B1 H16 N16384 d128: four chunks of four heads, three slots of
+    # q, k, v, o (16 MiB each) + lse (256 KiB)
+    assert f(1, 16, 16384, 16384, 128, 0) == 3 * (4 * (16 << 20) + (256 << 10))
+    # one head, one chunk: a single slot
+    assert f(1, 1, 100, 100, 64, 0) == 12800 + 2 * 12800 + 12800 + 512
