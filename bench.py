@@ -42,7 +42,8 @@ WORKLOAD_DESC = ("C4 bf16 causal B1 H16 N16384 d128 + C5 e4m3 non-causal B2 H16 
                  "(per-(b,h) descales, 0.1% x10 outliers); one attention call each per step")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 4.5 / 2.25     # nominal dense ratio
-TC_SOURCES = ("io_aware_exact_03_gb300/csrc/attn_tc.cu", "io_aware_exact_03_gb300/csrc/tc_ptx.cuh")
+TC_SOURCES = ("io_aware_exact_03_gb300/csrc/attn_tc.cu", "io_aware_exact_03_gb300/csrc/tc_ptx.cuh",
+              "io_aware_exact_03_gb300/csrc/bounded_wait.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_attn_tc_bf16_causal_d128.txt")
 
 

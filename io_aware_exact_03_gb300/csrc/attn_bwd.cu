@@ -36,6 +36,7 @@
 #include <math.h>
 
 #include "attn_internal.h"
+#include "bounded_wait.cuh"
 #include "tc_ptx.cuh"
 #include "tma_map.cuh"
 
@@ -98,33 +99,14 @@ struct BwdParams {
     unsigned long long timeout_ns;
 };
 
-__device__ __noinline__ bool wait_slow_b(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                         unsigned long long limit_ns) {
-    const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 31u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > limit_ns) {
-                *abort_flag = 1;
-                atomicOr(&g_bwd_status, kStatusTimeout);
-                return false;
-            }
-        }
-    }
-}
-
+// Bounded waits (shared implementation) reporting to this file's status word.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          unsigned long long limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    return wait_slow_b(bar, parity, abort_flag, limit_ns);
+    return bounded_wait(bar, parity, abort_flag, limit_ns, &g_bwd_status);
 }
 
-__device__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer() - t0 > limit_ns) return;
-    }
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+    bounded_drain(bar, parity, limit_ns);
 }
 
 // unit L -> (b, head, tile rank) over n_heads heads per batch, in groups of

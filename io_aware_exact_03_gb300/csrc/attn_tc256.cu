@@ -33,6 +33,7 @@
 #include <math.h>
 
 #include "attn_internal.h"
+#include "bounded_wait.cuh"
 #include "tc_ptx.cuh"
 #include "tma_map.cuh"
 
@@ -105,33 +106,14 @@ struct Tc256Params {
     float* part_lse;  // [n_splits][B*H][N_q]
 };
 
-__device__ __noinline__ bool wait_slow256(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned long long limit_ns) {
-    const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 31u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > limit_ns) {
-                *abort_flag = 1;
-                atomicOr(&g_tc256_status, kStatusTimeout);
-                return false;
-            }
-        }
-    }
-}
-
+// Bounded waits (shared implementation) reporting to this file's status word.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          unsigned long long limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    return wait_slow256(bar, parity, abort_flag, limit_ns);
+    return bounded_wait(bar, parity, abort_flag, limit_ns, &g_tc256_status);
 }
 
-__device__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer() - t0 > limit_ns) return;
-    }
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+    bounded_drain(bar, parity, limit_ns);
 }
 
 __device__ __forceinline__ int kv_tiles_for(int q0, const Tc256Params& p) {
