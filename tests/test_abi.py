@@ -176,3 +176,18 @@ def test_host_forward_workspace_bytes(L):
     assert f(1, 16, 16384, 16384, 128, 0) == 3 * (4 * (16 << 20) + (256 << 10))
     # one head, one chunk: a single slot
     assert f(1, 1, 100, 100, 64, 0) == 12800 + 2 * 12800 + 12800 + 512
+
+
+def test_host_forward_binding_checks_arguments(L):
+    import torch
+    q = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        attn.attn_fwd_host(q, k, torch.zeros(1, 9, 2, 64, dtype=torch.bfloat16))   # v shape
+    with pytest.raises(TypeError):
+        attn.attn_fwd_host(q, k, k.to(torch.float16))                              # mixed dtypes
+    with pytest.raises(ValueError):
+        attn.attn_fwd_host(q[:, :, :1], k, k)                                       # q not contiguous
+    f8 = torch.zeros(1, 8, 2, 64).to(torch.float8_e4m3fn)
+    with pytest.raises(ValueError):
+        attn.attn_fwd_host(f8, f8, f8)                                              # e4m3 without descales
