@@ -195,10 +195,15 @@ attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o
                                 cudaMemcpyDeviceToHost, P.out);
         if (e == cudaSuccess) e = cudaEventRecord(P.drained[slot], P.out);
     }
-    // later work on the caller's stream sees every copy out
-    if (e == cudaSuccess) e = cudaEventRecord(P.end, P.out);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(us, P.end, 0);
-    if (e != cudaSuccess) {
+    // Later work on the caller's stream waits for every copy this call
+    // queued, in and out, also when the loop stopped early on an error (the
+    // caller may free the buffers as soon as that work runs).  `start` has
+    // been waited on already and is free to mark the copy-in tail.
+    cudaError_t ej = cudaEventRecord(P.end, P.out);
+    if (ej == cudaSuccess) ej = cudaStreamWaitEvent(us, P.end, 0);
+    if (ej == cudaSuccess) ej = cudaEventRecord(P.start, P.in);
+    if (ej == cudaSuccess) ej = cudaStreamWaitEvent(us, P.start, 0);
+    if (e != cudaSuccess || ej != cudaSuccess) {
         (void)cudaGetLastError();
         return ATTN_ERR_CUDA;
     }
