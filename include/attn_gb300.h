@@ -33,7 +33,9 @@
  *   arrays of B*H floats indexed b*H + h.
  *
  * Ownership: the caller allocates and owns every buffer.  The library
- *   allocates no device memory; inputs are never modified.
+ *   allocates no device memory; inputs are never modified.  (attn_fwd_host
+ *   creates two streams and a few events per device on its first call and
+ *   keeps them for the life of the process.)
  *
  * Asynchrony: calls are enqueued on `stream` (a cudaStream_t; NULL = legacy
  *   default stream) and return at once; results are valid once the stream has
