@@ -44,7 +44,7 @@
  * Errors: arguments are checked before anything is launched and give
  *   ATTN_ERR_INVALID_ARG (null pointer, negative size, misaligned pointer,
  *   non-finite or non-positive scale, bad dtype) or ATTN_ERR_UNSUPPORTED
- *   (d not 64/128, a grid dimension out of range).  ATTN_ERR_CUDA reports a
+ *   (d not 64, 128 or 256; a grid dimension out of range).  ATTN_ERR_CUDA reports a
  *   failed tensor-map encode or launch (cudaGetLastError is cleared).
  *   Kernels never trap: every wait inside them is bounded; a wait that runs
  *   out sets a device status word, the kernel returns, and attn_check_status
