@@ -12,7 +12,8 @@
 //     heads at a time so their K/V stay in L2, heaviest causal pairs first;
 //   * warp 0 (producer) streams Q_A, Q_B once and then K_0, V_0, K_1, V_1, ...
 //     through a ring of shared-memory slots with TMA, guarded by mbarriers;
-//   * warp 1 (one thread) issues the tcgen05 MMAs and owns TMEM:
+//   * warp 1 issues the tcgen05 MMAs and owns TMEM (the whole warp runs the
+//     issue loop on warp-uniform operands, one elected lane issues):
 //     S_t = Q_t K_j^T into the TMEM score buffer of tile t, and
 //     O_t += P_t V_j with P_t read from TMEM (P overwrites its own S buffer;
 //     the next S_t MMA is issued right behind that P V MMA: one thread's
@@ -297,7 +298,12 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         __syncwarp();
     } else if (warp < C::SOFTMAX_WARP0) {
         // ----------------------------------------------------- MMA issuer(s)
-        if (lane == 0 && n_max > 0) {
+        // The whole warp runs the issue loop (warp-uniform operands); one
+        // elected lane issues each MMA, commit and arrive.
+        auto wb = [&](uint32_t bar, uint32_t par) {
+            return __all_sync(0xffffffffu, wait_bar(bar, par, abort_flag, lim));
+        };
+        if (n_max > 0) {
             auto issue_qk = [&](int t, int slot) {
                 // descriptors of the tile bases; each MMA adds its byte offset / 16
                 const uint64_t qd = smem_desc(smem_u32(sQ + t * C::TILE), 16, 8 * C::CB, C::LAYOUT);
@@ -312,9 +318,9 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                         const uint64_t db = kd + off16;
                         const uint32_t acc = (c | ks) != 0;
                         if constexpr (KIND == kE4M3)
-                            mma_f8_ss(tmem + col_s(t), da, db, C::IDESC_QK, acc);
+                            mma_f8_ss_1(tmem + col_s(t), da, db, C::IDESC_QK, acc);
                         else
-                            mma_f16_ss(tmem + col_s(t), da, db, C::IDESC_QK, acc);
+                            mma_f16_ss_1(tmem + col_s(t), da, db, C::IDESC_QK, acc);
                     }
                 }
             };
@@ -332,15 +338,15 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                         const uint64_t da =
                             smem_desc(smem_u32(sP + t * C::PT) + off, 16, 1024, 2u);
                         if constexpr (KIND == kE4M3)
-                            mma_f8_ss(tmem + col_o<D>(t), da, db, C::IDESC_PV, acc);
+                            mma_f8_ss_1(tmem + col_o<D>(t), da, db, C::IDESC_PV, acc);
                         else
-                            mma_f16_ss(tmem + col_o<D>(t), da, db, C::IDESC_PV, acc);
+                            mma_f16_ss_1(tmem + col_o<D>(t), da, db, C::IDESC_PV, acc);
                     } else {
                         const uint32_t a_tmem = tmem + col_s(t) + ks * (C::MMA_K * C::E / 4);
                         if constexpr (KIND == kE4M3)
-                            mma_f8_ts(tmem + col_o<D>(t), a_tmem, db, C::IDESC_PV, acc);
+                            mma_f8_ts_1(tmem + col_o<D>(t), a_tmem, db, C::IDESC_PV, acc);
                         else
-                            mma_f16_ts(tmem + col_o<D>(t), a_tmem, db, C::IDESC_PV, acc);
+                            mma_f16_ts_1(tmem + col_o<D>(t), a_tmem, db, C::IDESC_PV, acc);
                     }
                 }
             };
@@ -356,59 +362,59 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                 // from each issuer: items this tile never reads (keys beyond
                 // its causal range) are released once they have landed, so a
                 // release never runs ahead of the item's own fill.
-                const int t = warp - 1;
+                const int t = __shfl_sync(0xffffffffu, warp, 0) - 1;
                 const int nt = n_kv[t];
                 const uint32_t drain_t = t == 0 ? b_drain : b_drain_b;
-                ok = wait_bar(b_q_full, 0, abort_flag, lim);
+                ok = wb(b_q_full, 0);
                 if (ok && nt > 0) {
-                    ok = wait_bar(b_kv_full + 8 * slot_of(0), par_of(0), abort_flag, lim);
+                    ok = wb(b_kv_full + 8 * slot_of(0), par_of(0));
                     if (ok) {
                         tc_fence_after();
                         issue_qk(t, slot_of(0));
-                        mma_commit(b_s_full + 8 * t);
-                        mma_commit(b_kv_empty + 8 * slot_of(0));
+                        mma_commit_1(b_s_full + 8 * t);
+                        mma_commit_1(b_kv_empty + 8 * slot_of(0));
                     }
                 }
                 for (int j = 0; j < nt && ok; ++j) {
                     const int itV = 2 * j + 1, itK = 2 * j + 2;
                     if (j + 1 < nt) {
-                        ok = wait_bar(b_kv_full + 8 * slot_of(itK), par_of(itK), abort_flag, lim);
-                        if (ok) ok = wait_bar(b_s_free + 8 * t, (uint32_t)j & 1u, abort_flag, lim);
+                        ok = wb(b_kv_full + 8 * slot_of(itK), par_of(itK));
+                        if (ok) ok = wb(b_s_free + 8 * t, (uint32_t)j & 1u);
                         if (!ok) break;
                         tc_fence_after();
                         issue_qk(t, slot_of(itK));
-                        mma_commit(b_s_full + 8 * t);
-                        mma_commit(b_kv_empty + 8 * slot_of(itK));
+                        mma_commit_1(b_s_full + 8 * t);
+                        mma_commit_1(b_kv_empty + 8 * slot_of(itK));
                     }
-                    ok = wait_bar(b_kv_full + 8 * slot_of(itV), par_of(itV), abort_flag, lim);
-                    if (ok) ok = wait_bar(b_p_full + 8 * t, (uint32_t)j & 1u, abort_flag, lim);
+                    ok = wb(b_kv_full + 8 * slot_of(itV), par_of(itV));
+                    if (ok) ok = wb(b_p_full + 8 * t, (uint32_t)j & 1u);
                     if (!ok) break;
                     tc_fence_after();
                     issue_pv(t, slot_of(itV), j == 0);
-                    mma_commit(b_pv_done + 8 * t);
-                    mma_commit(b_kv_empty + 8 * slot_of(itV));
+                    mma_commit_1(b_pv_done + 8 * t);
+                    mma_commit_1(b_kv_empty + 8 * slot_of(itV));
                 }
                 // items of K/V tiles [nt, n_max): not read by this tile
                 for (int it = 2 * nt; it < 2 * n_max && ok; ++it) {
-                    ok = wait_bar(b_kv_full + 8 * slot_of(it), par_of(it), abort_flag, lim);
-                    if (ok) mbar_arrive(b_kv_empty + 8 * slot_of(it));
+                    ok = wb(b_kv_full + 8 * slot_of(it), par_of(it));
+                    if (ok) mbar_arrive_1(b_kv_empty + 8 * slot_of(it));
                 }
                 if (!ok) {
                     // make sure none of this issuer's MMAs still runs when TMEM is freed
-                    mma_commit(drain_t);
+                    mma_commit_1(drain_t);
                     wait_drain(drain_t, 0, lim);
                 }
             } else {
-                ok = wait_bar(b_q_full, 0, abort_flag, lim);
-                if (ok) ok = wait_bar(b_kv_full + 8 * slot_of(0), par_of(0), abort_flag, lim);
+                ok = wb(b_q_full, 0);
+                if (ok) ok = wb(b_kv_full + 8 * slot_of(0), par_of(0));
                 if (ok) {
                     tc_fence_after();
                     for (int t = 0; t < 2; ++t) {
                         if (n_kv[t] == 0) continue;
                         issue_qk(t, slot_of(0));
-                        mma_commit(b_s_full + 8 * t);
+                        mma_commit_1(b_s_full + 8 * t);
                     }
-                    mma_commit(b_kv_empty + 8 * slot_of(0));
+                    mma_commit_1(b_kv_empty + 8 * slot_of(0));
                 }
             }
             // Per tile: O_t += P_t V_j, then at once S_t = Q_t K_{j+1}^T into the
@@ -419,39 +425,38 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             // and the other way round.
             for (int j = 0; j < n_max && ok && !C::P_SMEM; ++j) {
                 const int itV = 2 * j + 1, itK = 2 * j + 2;
-                ok = wait_bar(b_kv_full + 8 * slot_of(itV), par_of(itV), abort_flag, lim);
+                ok = wb(b_kv_full + 8 * slot_of(itV), par_of(itV));
                 bool k_ready = false;
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (j < n_kv[t]) {
-                        ok = wait_bar(b_p_full + 8 * t, (uint32_t)j & 1u, abort_flag, lim);
+                        ok = wb(b_p_full + 8 * t, (uint32_t)j & 1u);
                         if (!ok) break;
                         tc_fence_after();
                         issue_pv(t, slot_of(itV), j == 0);
-                        mma_commit(b_pv_done + 8 * t);
+                        mma_commit_1(b_pv_done + 8 * t);
                     }
                     if (j + 1 < n_kv[t]) {
                         if (!k_ready) {
-                            ok = wait_bar(b_kv_full + 8 * slot_of(itK), par_of(itK), abort_flag,
-                                          lim);
+                            ok = wb(b_kv_full + 8 * slot_of(itK), par_of(itK));
                             k_ready = true;
                         }
                         if (!ok) break;
                         tc_fence_after();
                         issue_qk(t, slot_of(itK));
-                        mma_commit(b_s_full + 8 * t);
+                        mma_commit_1(b_s_full + 8 * t);
                     }
                 }
                 if (!ok) break;
                 // release V_j (every P V of it is issued) and K_{j+1}; the last
                 // V's release is not needed (nothing is loaded after it)
                 if (j + 1 < n_max) {
-                    mma_commit(b_kv_empty + 8 * slot_of(itV));
-                    mma_commit(b_kv_empty + 8 * slot_of(itK));
+                    mma_commit_1(b_kv_empty + 8 * slot_of(itV));
+                    mma_commit_1(b_kv_empty + 8 * slot_of(itK));
                 }
             }
             if (!ok && !C::P_SMEM) {
                 // make sure no MMA is still reading or writing when TMEM is freed
-                mma_commit(b_drain);
+                mma_commit_1(b_drain);
                 wait_drain(b_drain, 0, lim);
             }
         }

@@ -176,6 +176,52 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t d, uint32_t a_tmem, uint64_t 
         : "memory");
 }
 
+// Warp-converged forms: every lane of the warp executes the instruction with
+// the same operands and an elect.sync predicate lets exactly one lane issue
+// it.  The operands are then computed by the whole warp (warp-uniform values)
+// instead of inside a one-lane branch.
+#define ATTN_ELECT_MMA(KIND_STR, A_FORM)                                              \
+    asm volatile("{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\t"              \
+                 "elect.sync _|e, 0xffffffff;\n\t"                                       \
+                 "@e tcgen05.mma.cta_group::1.kind::" KIND_STR " [%0], " A_FORM ", %2, %3, p;\n\t}\n"
+
+__device__ __forceinline__ void mma_f16_ss_1(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                             uint32_t acc) {
+    ATTN_ELECT_MMA("f16", "%1")::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+__device__ __forceinline__ void mma_f16_ts_1(uint32_t d, uint32_t a_tmem, uint64_t b,
+                                             uint32_t idesc, uint32_t acc) {
+    ATTN_ELECT_MMA("f16", "[%1]")::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+__device__ __forceinline__ void mma_f8_ss_1(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t acc) {
+    ATTN_ELECT_MMA("f8f6f4", "%1")::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+__device__ __forceinline__ void mma_f8_ts_1(uint32_t d, uint32_t a_tmem, uint64_t b,
+                                            uint32_t idesc, uint32_t acc) {
+    ATTN_ELECT_MMA("f8f6f4", "[%1]")::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+#undef ATTN_ELECT_MMA
+
+// Commit / arrive from one elected lane of a converged warp.
+__device__ __forceinline__ void mma_commit_1(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
+            bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_1(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}\n" ::"r"(bar)
+        : "memory");
+}
+
 // Arrive once on an mbarrier when every tcgen05 op issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
