@@ -289,13 +289,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0 && n_steps > 0) {
+        // The whole warp runs the issue loop (warp-uniform operands); one
+        // elected lane issues each MMA and commit.
+        auto wb = [&](uint32_t bar, uint32_t par) {
+            return __all_sync(0xffffffffu, wait_bar(bar, par, abort_flag, lim));
+        };
+        if (n_steps > 0) {
             const uint64_t kd = smem_desc(smem_u32(sK), 16, 8 * C::CB, 2u);
             const uint64_t vd = smem_desc(smem_u32(sV), 16, 8 * C::CB, 2u);
-            bool ok = wait_bar(b_kv_full, 0, abort_flag, lim);
+            bool ok = wb(b_kv_full, 0);
             for (int s = 0; s < n_steps && ok; ++s) {
                 const int slot = s % SLOTS;
-                ok = wait_bar(b_item_full + 8 * slot, (uint32_t)(s / SLOTS) & 1u, abort_flag, lim);
+                ok = wb(b_item_full + 8 * slot, (uint32_t)(s / SLOTS) & 1u);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t qa = smem_u32(sRing + (size_t)slot * C::ITEM_KV);
@@ -309,17 +314,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int ks = 0; ks < C::CB / 32; ++ks) {
                         const uint32_t o16 = (uint32_t)(c * C::CHUNK + ks * 32) >> 4;
                         const uint32_t acc = (c | ks) != 0;
-                        mma_f16_ss(tmem + kColS, kd + o16, qd + o16, C::IDESC_S, acc);
-                        mma_f16_ss(tmem + kColDP, vd + o16, gd + o16, C::IDESC_S, acc);
+                        mma_f16_ss_1(tmem + kColS, kd + o16, qd + o16, C::IDESC_S, acc);
+                        mma_f16_ss_1(tmem + kColDP, vd + o16, gd + o16, C::IDESC_S, acc);
                     }
                 }
-                mma_commit(b_s_full);
+                mma_commit_1(b_s_full);
                 // dV += P^T dO, dK += dS^T Q: A from TMEM (K = 128 queries, in two
                 // halves as the elementwise warps finish them), B MN-major
                 const uint64_t gmn = smem_desc(ga, C::CHUNK, 8 * C::CB, 2u);
                 const uint64_t qmn = smem_desc(qa, C::CHUNK, 8 * C::CB, 2u);
                 for (int half = 0; half < 2 && ok; ++half) {
-                    ok = wait_bar(half ? b_p_half1 : b_p_half0, (uint32_t)s & 1u, abort_flag, lim);
+                    ok = wb(half ? b_p_half1 : b_p_half0, (uint32_t)s & 1u);
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll
@@ -327,19 +332,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int ks = half * (BM / C::MMA_K / 2) + kh;
                         const uint32_t o16 = (uint32_t)(ks * C::MMA_K * C::CB) >> 4;
                         const uint32_t acc = (s > 0 || ks > 0) ? 1u : 0u;
-                        mma_f16_ts(tmem + kColAcc, tmem + kColS + ks * (C::MMA_K / 2), gmn + o16,
+                        mma_f16_ts_1(tmem + kColAcc, tmem + kColS + ks * (C::MMA_K / 2), gmn + o16,
                                    C::IDESC_ACC, acc);
-                        mma_f16_ts(tmem + kColAcc + D, tmem + kColDP + ks * (C::MMA_K / 2), qmn + o16,
+                        mma_f16_ts_1(tmem + kColAcc + D, tmem + kColDP + ks * (C::MMA_K / 2), qmn + o16,
                                    C::IDESC_ACC, acc);
                     }
                 }
                 if (!ok) break;
-                mma_commit(b_item_empty + 8 * slot);
+                mma_commit_1(b_item_empty + 8 * slot);
             }
             if (ok) {
-                mma_commit(b_acc_done);
+                mma_commit_1(b_acc_done);
             } else {
-                mma_commit(b_drain);
+                mma_commit_1(b_drain);
                 wait_drain(b_drain, 0, lim);
             }
         }
@@ -559,13 +564,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0 && n > 0) {
+        // The whole warp runs the issue loop (warp-uniform operands); one
+        // elected lane issues each MMA and commit.
+        auto wb = [&](uint32_t bar, uint32_t par) {
+            return __all_sync(0xffffffffu, wait_bar(bar, par, abort_flag, lim));
+        };
+        if (n > 0) {
             const uint64_t qd = smem_desc(smem_u32(sQ), 16, 8 * C::CB, 2u);
             const uint64_t gd = smem_desc(smem_u32(sG), 16, 8 * C::CB, 2u);
-            bool ok = wait_bar(b_q_full, 0, abort_flag, lim);
+            bool ok = wb(b_q_full, 0);
             for (int j = 0; j < n && ok; ++j) {
                 const int slot = j % SLOTS;
-                ok = wait_bar(b_item_full + 8 * slot, (uint32_t)(j / SLOTS) & 1u, abort_flag, lim);
+                ok = wb(b_item_full + 8 * slot, (uint32_t)(j / SLOTS) & 1u);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t ka = smem_u32(sRing + (size_t)slot * C::ITEM_Q);
@@ -579,15 +589,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int ks = 0; ks < C::CB / 32; ++ks) {
                         const uint32_t o16 = (uint32_t)(c * C::CHUNK + ks * 32) >> 4;
                         const uint32_t acc = (c | ks) != 0;
-                        mma_f16_ss(tmem + kColS, qd + o16, kd + o16, C::IDESC_S, acc);
-                        mma_f16_ss(tmem + kColDP, gd + o16, vd + o16, C::IDESC_S, acc);
+                        mma_f16_ss_1(tmem + kColS, qd + o16, kd + o16, C::IDESC_S, acc);
+                        mma_f16_ss_1(tmem + kColDP, gd + o16, vd + o16, C::IDESC_S, acc);
                     }
                 }
-                mma_commit(b_s_full);
+                mma_commit_1(b_s_full);
                 // dQ += dS K: A = dS from TMEM (K = 128 keys, in two halves), B = K MN-major
                 const uint64_t kmn = smem_desc(ka, C::CHUNK, 8 * C::CB, 2u);
                 for (int half = 0; half < 2 && ok; ++half) {
-                    ok = wait_bar(half ? b_p_half1 : b_p_half0, (uint32_t)j & 1u, abort_flag, lim);
+                    ok = wb(half ? b_p_half1 : b_p_half0, (uint32_t)j & 1u);
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll
@@ -595,17 +605,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int ks = half * (BN / C::MMA_K / 2) + kh;
                         const uint32_t o16 = (uint32_t)(ks * C::MMA_K * C::CB) >> 4;
                         const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
-                        mma_f16_ts(tmem + kColAcc, tmem + kColDP + ks * (C::MMA_K / 2), kmn + o16,
+                        mma_f16_ts_1(tmem + kColAcc, tmem + kColDP + ks * (C::MMA_K / 2), kmn + o16,
                                    C::IDESC_ACC, acc);
                     }
                 }
                 if (!ok) break;
-                mma_commit(b_item_empty + 8 * slot);
+                mma_commit_1(b_item_empty + 8 * slot);
             }
             if (ok) {
-                mma_commit(b_acc_done);
+                mma_commit_1(b_acc_done);
             } else {
-                mma_commit(b_drain);
+                mma_commit_1(b_drain);
                 wait_drain(b_drain, 0, lim);
             }
         }

@@ -288,7 +288,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ----------------------------------------------------- MMA issuer
-        if (lane == 0 && n > 0) {
+        // The whole warp runs the issue loop (warp-uniform operands); one
+        // elected lane issues each MMA and commit.
+        auto wb = [&](uint32_t bar, uint32_t par) {
+            return __all_sync(0xffffffffu, wait_bar(bar, par, abort_flag, lim));
+        };
+        if (n > 0) {
             // S_{buf} = Q K^T from the two K items at ring positions it, it + 1
             auto issue_qk = [&](int buf, int it) {
                 const uint64_t qd = smem_desc(smem_u32(sQ), 16, 8 * C::CB, 2u);
@@ -304,9 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t b16 = (uint32_t)(ks * 32) >> 4;
                         const uint32_t acc = (c | ks) != 0;
                         if constexpr (KIND == kE4M3)
-                            mma_f8_ss(tmem + 128u * buf, qd + a16, kd + b16, C::IDESC_QK, acc);
+                            mma_f8_ss_1(tmem + 128u * buf, qd + a16, kd + b16, C::IDESC_QK, acc);
                         else
-                            mma_f16_ss(tmem + 128u * buf, qd + a16, kd + b16, C::IDESC_QK, acc);
+                            mma_f16_ss_1(tmem + 128u * buf, qd + a16, kd + b16, C::IDESC_QK, acc);
                     }
                 }
             };
@@ -323,29 +328,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t a_tmem = tmem + 128u * buf + ks * (C::MMA_K * C::E / 4);
                     const uint32_t acc = (!first || ks > 0) ? 1u : 0u;
                     if constexpr (KIND == kE4M3)
-                        mma_f8_ts(tmem + kColO, a_tmem, vd, C::IDESC_PV, acc);
+                        mma_f8_ts_1(tmem + kColO, a_tmem, vd, C::IDESC_PV, acc);
                     else
-                        mma_f16_ts(tmem + kColO, a_tmem, vd, C::IDESC_PV, acc);
+                        mma_f16_ts_1(tmem + kColO, a_tmem, vd, C::IDESC_PV, acc);
                 }
             };
             auto wait_items = [&](int it) {
-                return wait_bar(b_kv_full + 8 * slot_of(it), par_of(it), abort_flag, lim) &&
-                       wait_bar(b_kv_full + 8 * slot_of(it + 1), par_of(it + 1), abort_flag, lim);
+                return wb(b_kv_full + 8 * slot_of(it), par_of(it)) &&
+                       wb(b_kv_full + 8 * slot_of(it + 1), par_of(it + 1));
             };
             auto release_items = [&](int it) {
-                mma_commit(b_kv_empty + 8 * slot_of(it));
-                mma_commit(b_kv_empty + 8 * slot_of(it + 1));
+                mma_commit_1(b_kv_empty + 8 * slot_of(it));
+                mma_commit_1(b_kv_empty + 8 * slot_of(it + 1));
             };
 
             int it = 0;
-            bool ok = wait_bar(b_q_full, 0, abort_flag, lim);
+            bool ok = wb(b_q_full, 0);
             // scores of K_0 and K_1 into S_0 and S_1
             for (int t = 0; t < 2 && t < n && ok; ++t) {
                 ok = wait_items(it);
                 if (!ok) break;
                 tc_fence_after();
                 issue_qk(t, it);
-                mma_commit(b_s_full + 8 * t);
+                mma_commit_1(b_s_full + 8 * t);
                 release_items(it);
                 it += 2;
             }
@@ -354,12 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < n && ok; ++j) {
                 const int buf = j & 1;
                 ok = wait_items(it);
-                if (ok) ok = wait_bar(b_p_full + 8 * buf, (uint32_t)(j >> 1) & 1u, abort_flag, lim);
+                if (ok) ok = wb(b_p_full + 8 * buf, (uint32_t)(j >> 1) & 1u);
                 if (!ok) break;
                 tc_fence_after();
                 issue_pv(buf, it, j == 0);
-                mma_commit(b_pv_done);
-                if (j + 1 == n) mma_commit(b_o_done);
+                mma_commit_1(b_pv_done);
+                if (j + 1 == n) mma_commit_1(b_o_done);
                 release_items(it);
                 it += 2;
                 if (j + 2 < n) {
@@ -367,13 +372,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     tc_fence_after();
                     issue_qk(buf, it);
-                    mma_commit(b_s_full + 8 * buf);
+                    mma_commit_1(b_s_full + 8 * buf);
                     release_items(it);
                     it += 2;
                 }
             }
             if (!ok) {
-                mma_commit(b_drain);
+                mma_commit_1(b_drain);
                 wait_drain(b_drain, 0, lim);
             }
         }
