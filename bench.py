@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--sustained-s", type=float, default=1.5,
+                    help="seconds of back-to-back steps for the sustained clock record (0: skip)")
     ap.add_argument("--case", choices=["C1", "C2", "C3", "C4", "C5", "LKV", "D256", "D256F", "BWD"], default=None,
                     help="measure one workload case alone instead of the C4 + C5 step")
     ap.add_argument("--splits", type=int, default=1,
@@ -384,6 +386,15 @@ def run_ours(args):
     flops_step = sum(work_flops(c) for c in cases)
     value = job_tflops(flops_step, K, world, ms_total)
 
+    # ---- the same step back to back for a sustained period (>= 1.5 s), with
+    # its own clock record: the short timed region above cannot show the
+    # power draw and the clock a long run settles at.
+    sustained = None
+    if args.sustained_s > 0:
+        sustained = run_sustained(torch, cases, dev, call, stream, gpu_id, ms_total / K,
+                                  work_flops_step=sum(work_flops(c) for c in cases),
+                                  seconds=args.sustained_s)
+
     # ---- end to end through the public API: pinned host -> device -> kernel -> host
     e2e = run_e2e(torch, attn, cases, host, outs, stream, args.e2e_steps, call, world,
                   host_api=args.splits <= 1)
@@ -431,6 +442,7 @@ def run_ours(args):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "sustained": sustained,
             "gpu_launches": sum(3 if c.name == "BWD" else 1 for c in cases) * K,
             "clocks": clocks,
         }
@@ -439,6 +451,32 @@ def run_ours(args):
         dist.barrier()
         dist.destroy_process_group()
     return result
+
+
+def run_sustained(torch, cases, dev, call, stream, gpu_id, ms_step, work_flops_step,
+                  seconds=1.5):
+    """Back-to-back steps for about `seconds`, timed with CUDA events, with
+    nvidia-smi clock / power samples taken inside that window.  Reported
+    beside the short timed region; it does not replace `value`."""
+    n = max(20, int(seconds * 1e3 / max(ms_step, 1e-3)) + 1)
+    sampler = ClockSampler(gpu_id)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    sampler.start()
+    wall0 = time.time()
+    a.record(stream)
+    for _ in range(n):
+        for i in range(len(cases)):
+            call(i, dev[i])
+    b.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark(wall0, time.time())
+    clocks = sampler.stop()
+    ms = a.elapsed_time(b)
+    return {"steps": n, "seconds": round(ms / 1e3, 3), "ms_per_step": round(ms / n, 4),
+            "value": round(work_flops_step * n / (ms / 1e3) / 1e12, 2), "unit": UNIT,
+            "clocks": clocks}
 
 
 def run_e2e(torch, attn, cases, host, outs, stream, steps, call, world, host_api=True):

@@ -253,7 +253,13 @@ ATTN_API size_t attn_fwd_host_workspace_bytes(int B, int H, int N_q, int N_k, in
  * num_splits: 2..32.  Other arguments, layouts and errors as attn_fwd_splitkv.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  All calls share the one array, so calls whose
+ * before any stream capture.  With lazy module loading (CUDA's default,
+ * CUDA_MODULE_LOADING=LAZY) the library's device code, and the array with it,
+ * is loaded on a device by the first library call that needs it there: that
+ * load reserves the array's memory and may synchronise.  Callers that cannot
+ * afford either make their first call on each device outside the region where
+ * allocation is not allowed (for example at start-up); later calls reserve
+ * nothing.  All calls share the one array, so calls whose
  * work overlaps on the GPU (other streams, other host threads) race: order
  * them on one stream or synchronise between them.  No state carries over from
  * one call to the next that the result depends on. */

@@ -66,6 +66,9 @@ extern "C" ATTN_API attn_status_t attn_fwd_splitkv_static(
     if (!aligned16(q) || !aligned16(o) || (k && !aligned16(k)) || (v && !aligned16(v)) ||
         (reinterpret_cast<uintptr_t>(lse) & 3u))
         return ATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q_descale) & 3u) || (reinterpret_cast<uintptr_t>(k_descale) & 3u) ||
+        (reinterpret_cast<uintptr_t>(v_descale) & 3u))
+        return ATTN_ERR_INVALID_ARG;
     // the fixed array must hold every split's partial outputs and lse
     const size_t need = attn::splitkv_workspace_bytes(B, H, N_q, d, num_splits);
     if (need > (size_t)ATTN_STATIC_SCRATCH_BYTES) return ATTN_ERR_SCRATCH_LIMIT;
