@@ -277,6 +277,25 @@ ATTN_API attn_status_t attn_fwd_splitkv_static(const void* q, const void* k, con
  * ATTN_ERR_TIMEOUT and the context stays usable.  Nothing traps or hangs. */
 ATTN_API attn_status_t attn_selftest_wait(unsigned timeout_us, void* stream);
 
+/* Health check of the attention kernels' own abort path (the failure
+ * detection of the tensor-core kernels: every wait bounded, then drain, free
+ * TMEM, exit).  Runs the kernel attn_fwd / attn_fwd_fp8 would run for these
+ * arguments (same layouts, dtypes, head dimensions 64 / 128 / 256), except that
+ * the K/V loader stops after the first ring item and every bounded wait gives
+ * up after timeout_us microseconds (1 .. 10^7; normal calls use 2 s).  The
+ * waits for the withheld tiles run out, each role drains what it issued (those
+ * drains keep the 2 s limit), TMEM is freed and the CTAs exit; the next
+ * attn_check_status returns ATTN_ERR_TIMEOUT and clears the status, and the
+ * context stays usable.  o and lse are left with undefined contents.  Needs
+ * N_q > 0 and N_k > 0 (else ATTN_ERR_INVALID_ARG); other errors as attn_fwd.
+ * Not part of the method: a diagnostic of the failure-detection path. */
+ATTN_API attn_status_t attn_selftest_abort(const void* q, const void* k, const void* v, void* o,
+                                           float* lse, const float* q_descale,
+                                           const float* k_descale, const float* v_descale,
+                                           int B, int H, int N_q, int N_k, int d, float scale,
+                                           int causal, attn_dtype_t dtype, unsigned timeout_us,
+                                           void* stream);
+
 /* Synchronises `stream`, then returns and clears the device status word:
  * ATTN_ERR_TIMEOUT if a bounded wait inside a kernel ran out since the last
  * call, ATTN_ERR_CUDA if the stream reports an error, else ATTN_OK. */

@@ -24,6 +24,7 @@ __all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_simt", "attn_fwd_splitkv", "att
            "attn_quantize_e4m3",
            "attn_splitkv_workspace_bytes", "attn_check_status", "attn_status_string",
            "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_host", "attn_fwd_host_workspace_bytes",
+           "attn_selftest_wait", "attn_selftest_abort",
            "AttnError", "lib", "build"]
 
 (ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT,
@@ -89,6 +90,9 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd_host_workspace_bytes.restype = sz
         L.attn_selftest_wait.argtypes = [ctypes.c_uint, vp]
         L.attn_selftest_wait.restype = i
+        L.attn_selftest_abort.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, i, i, i, i, i, f, i, i,
+                                          ctypes.c_uint, vp]
+        L.attn_selftest_abort.restype = i
         L.attn_check_status.argtypes = [vp]
         L.attn_check_status.restype = i
         L.attn_status_string.argtypes = [i]
@@ -371,6 +375,21 @@ def attn_selftest_wait(timeout_us=1000, stream=None, device=None):
     dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
     st = lib().attn_selftest_wait(int(timeout_us), _stream(stream, dev))
     _raise(st, "attn_selftest_wait")
+
+
+def attn_selftest_abort(q, k, v, q_descale=None, k_descale=None, v_descale=None, scale=None,
+                        causal=False, timeout_us=500, stream=None):
+    """Run the attention kernel with its K/V loader stopped after the first
+    tile and every wait limited to timeout_us: the abort path's health check.
+    The next attn_check_status raises AttnError(ATTN_ERR_TIMEOUT)."""
+    B, N_q, H, d, N_k = _check_inputs(q, k, v)
+    o, lse = _outputs(q, None, None, B, N_q, H, d)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib().attn_selftest_abort(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(q_descale),
+                                   _ptr(k_descale), _ptr(v_descale), B, H, N_q, N_k, d, scale,
+                                   int(bool(causal)), _dtype_code(q), int(timeout_us),
+                                   _stream(stream, q.device))
+    _raise(st, "attn_selftest_abort")
 
 
 def attn_check_status(stream=None, device=None):

@@ -242,6 +242,25 @@ attn_status_t attn_selftest_wait(unsigned timeout_us, void* stream) {
     return from_cuda(e);
 }
 
+attn_status_t attn_selftest_abort(const void* q, const void* k, const void* v, void* o,
+                                  float* lse, const float* q_descale, const float* k_descale,
+                                  const float* v_descale, int B, int H, int N_q, int N_k, int d,
+                                  float scale, int causal, attn_dtype_t dtype, unsigned timeout_us,
+                                  void* stream) {
+    if (timeout_us == 0 || timeout_us > 10u * 1000u * 1000u) return ATTN_ERR_INVALID_ARG;
+    attn::Problem p = make_problem(q, k, v, o, lse, q_descale, k_descale, v_descale, B, H, N_q,
+                                   N_k, d, scale, causal, (int)dtype);
+    attn_status_t st = validate(p);
+    if (st != ATTN_OK) return st;
+    // the check needs work to cut short: at least one query row and one key
+    if (is_empty(p) || N_k == 0) return ATTN_ERR_INVALID_ARG;
+    p.selftest_wait_ns = 1000ull * timeout_us;
+    p.selftest_items = 1;  // the loader stops after the first K/V ring item
+    cudaError_t e = attn::launch_tc(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    return from_cuda(e);
+}
+
 attn_status_t attn_check_status(void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaStreamSynchronize(s);

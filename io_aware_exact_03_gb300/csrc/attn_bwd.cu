@@ -282,9 +282,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bulk_load(smem_u32(dst + 2 * C::TILE + 512), p.Dvec + vo, 512, b_item_full + 8 * slot);
             }
             if (!ok) {
-                wait_drain(b_kv_full, 0, lim);
+                wait_drain(b_kv_full, 0, kWaitLimitNs);
                 for (int k = (s > SLOTS ? s - SLOTS : 0); k < s; ++k)
-                    wait_drain(b_item_full + 8 * (k % SLOTS), (uint32_t)(k / SLOTS) & 1u, lim);
+                    wait_drain(b_item_full + 8 * (k % SLOTS), (uint32_t)(k / SLOTS) & 1u, kWaitLimitNs);
             }
         }
         __syncwarp();
@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit_1(b_acc_done);
             } else {
                 mma_commit_1(b_drain);
-                wait_drain(b_drain, 0, lim);
+                wait_drain(b_drain, 0, kWaitLimitNs);
             }
         }
         __syncwarp();
@@ -557,9 +557,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) {
-                wait_drain(b_q_full, 0, lim);
+                wait_drain(b_q_full, 0, kWaitLimitNs);
                 for (int k = (j > SLOTS ? j - SLOTS : 0); k < j; ++k)
-                    wait_drain(b_item_full + 8 * (k % SLOTS), (uint32_t)(k / SLOTS) & 1u, lim);
+                    wait_drain(b_item_full + 8 * (k % SLOTS), (uint32_t)(k / SLOTS) & 1u, kWaitLimitNs);
             }
         }
         __syncwarp();
@@ -616,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit_1(b_acc_done);
             } else {
                 mma_commit_1(b_drain);
-                wait_drain(b_drain, 0, lim);
+                wait_drain(b_drain, 0, kWaitLimitNs);
             }
         }
         __syncwarp();
@@ -759,7 +759,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
     p.scale = a.scale;
     p.lse2 = lse2;
     p.Dvec = Dvec;
-    p.timeout_ns = 2000000000ull;
+    p.timeout_ns = kWaitLimitNs;
     const long long n_bh = (long long)a.B * a.H;
     // dK, dV: one CTA per (K/V head, key tile); the query side streams Q and
     // dO of the group's query heads

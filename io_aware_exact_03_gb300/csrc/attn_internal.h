@@ -26,7 +26,16 @@ struct Problem {
     float scale;
     int causal;
     int dtype;
+    // Health check of the abort path only (attn_selftest_abort); 0 in normal
+    // calls.  Every bounded wait then gives up after selftest_wait_ns, and the
+    // K/V loader stops after selftest_items ring items.
+    unsigned long long selftest_wait_ns = 0;
+    int selftest_items = 0;
 };
+
+// Time limit of every bounded wait in a normal call; waits that only drain
+// what a role already issued (on the abort path) always get at least this.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 // CUDA-core kernel (attn_simt.cu).
 cudaError_t launch_simt(const Problem& p, cudaStream_t stream);

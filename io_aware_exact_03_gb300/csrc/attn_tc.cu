@@ -129,7 +129,9 @@ struct TcParams {
     const float* q_descale;
     const float* k_descale;
     const float* v_descale;
-    unsigned long long timeout_ns;
+    unsigned long long timeout_ns;  // limit of every bounded wait
+    unsigned long long drain_ns;    // limit of the abort path's drains (>= 2 s)
+    int items_limit;                // K/V ring items the loader issues (abort-path check)
     // split-KV: grid.y = n_splits CTAs share one query-tile pair's K/V range;
     // each writes its partial (O normalised within the split, fp32) and lse
     int n_splits;
@@ -274,7 +276,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             // item 2j = K_j, item 2j+1 = V_j (the order the MMAs first use them)
             int it = 0;
             bool ok = true;
-            for (; it < 2 * n_max; ++it) {
+            for (; it < 2 * n_max && it < p.items_limit; ++it) {
                 const int slot = it % C::SLOTS;
                 const uint32_t ph = (uint32_t)(it / C::SLOTS) & 1u;
                 if (!wait_bar(b_kv_empty + 8 * slot, ph ^ 1u, abort_flag, lim)) {
@@ -290,9 +292,9 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             }
             if (!ok) {
                 // let every load already issued land before the CTA can exit
-                wait_drain(b_q_full, 0, lim);
+                wait_drain(b_q_full, 0, p.drain_ns);
                 for (int k = (it > C::SLOTS ? it - C::SLOTS : 0); k < it; ++k)
-                    wait_drain(b_kv_full + 8 * (k % C::SLOTS), (uint32_t)(k / C::SLOTS) & 1u, lim);
+                    wait_drain(b_kv_full + 8 * (k % C::SLOTS), (uint32_t)(k / C::SLOTS) & 1u, p.drain_ns);
             }
         }
         __syncwarp();
@@ -402,7 +404,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                 if (!ok) {
                     // make sure none of this issuer's MMAs still runs when TMEM is freed
                     mma_commit_1(drain_t);
-                    wait_drain(drain_t, 0, lim);
+                    wait_drain(drain_t, 0, p.drain_ns);
                 }
             } else {
                 ok = wb(b_q_full, 0);
@@ -457,7 +459,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             if (!ok && !C::P_SMEM) {
                 // make sure no MMA is still reading or writing when TMEM is freed
                 mma_commit_1(b_drain);
-                wait_drain(b_drain, 0, lim);
+                wait_drain(b_drain, 0, p.drain_ns);
             }
         }
         __syncwarp();
@@ -836,7 +838,9 @@ cudaError_t launch_t(const Problem& pr, cudaStream_t stream, int n_splits = 1,
     p.q_descale = pr.q_descale;
     p.k_descale = pr.k_descale;
     p.v_descale = pr.v_descale;
-    p.timeout_ns = 2000000000ull;
+    p.timeout_ns = pr.selftest_wait_ns ? pr.selftest_wait_ns : kWaitLimitNs;
+    p.drain_ns = kWaitLimitNs;
+    p.items_limit = pr.selftest_items > 0 ? pr.selftest_items : 0x7fffffff;
     p.n_splits = n_splits;
     p.part_o = part_o;
     p.part_lse = part_lse;

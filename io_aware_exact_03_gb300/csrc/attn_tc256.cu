@@ -100,7 +100,9 @@ struct Tc256Params {
     const float* q_descale;
     const float* k_descale;
     const float* v_descale;
-    unsigned long long timeout_ns;
+    unsigned long long timeout_ns;  // limit of every bounded wait
+    unsigned long long drain_ns;    // limit of the abort path's drains (>= 2 s)
+    int items_limit;                // K/V ring items the loader issues (abort-path check)
     int n_splits;
     float* part_o;    // [n_splits][B*H][N_q][256]
     float* part_lse;  // [n_splits][B*H][N_q]
@@ -259,6 +261,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int grp = 0; ok && group_of(grp, n, &is_v, &t_kv); ++grp) {
                 const int key0 = (j0 + t_kv) * BN;
                 for (int half = 0; half < 2; ++half, ++it) {
+                    if (it >= p.items_limit) {
+                        ok = false;  // stop loading; nothing issued needs a drain beyond the usual
+                        break;
+                    }
                     const int slot = slot_of(it);
                     if (!wait_bar(b_kv_empty + 8 * slot, par_of(it) ^ 1u, abort_flag, lim)) {
                         ok = false;
@@ -280,9 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) {
-                wait_drain(b_q_full, 0, lim);
+                wait_drain(b_q_full, 0, p.drain_ns);
                 for (int k = (it > C::SLOTS ? it - C::SLOTS : 0); k < it; ++k)
-                    wait_drain(b_kv_full + 8 * slot_of(k), par_of(k), lim);
+                    wait_drain(b_kv_full + 8 * slot_of(k), par_of(k), p.drain_ns);
             }
         }
         __syncwarp();
@@ -379,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) {
                 mma_commit_1(b_drain);
-                wait_drain(b_drain, 0, lim);
+                wait_drain(b_drain, 0, p.drain_ns);
             }
         }
         __syncwarp();
@@ -613,7 +619,9 @@ cudaError_t launch_k(const Problem& pr, cudaStream_t stream, int n_splits, float
     p.q_descale = pr.q_descale;
     p.k_descale = pr.k_descale;
     p.v_descale = pr.v_descale;
-    p.timeout_ns = 2000000000ull;
+    p.timeout_ns = pr.selftest_wait_ns ? pr.selftest_wait_ns : kWaitLimitNs;
+    p.drain_ns = kWaitLimitNs;
+    p.items_limit = pr.selftest_items > 0 ? pr.selftest_items : 0x7fffffff;
     p.n_splits = n_splits;
     p.part_o = part_o;
     p.part_lse = part_lse;

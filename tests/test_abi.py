@@ -123,6 +123,14 @@ def test_splitkv_rejects_bad_workspace(L):
 
 
 def test_selftest_wait_rejects_bad_limits(L):
+    # the abort-path check: limit out of range, or nothing to cut short
+    fp = ctypes.c_void_p(P)
+    assert L.attn_selftest_abort(fp, fp, fp, fp, None, None, None, None, 1, 1, 128, 128, 64,
+                                 0.125, 0, attn.ATTN_BF16, 0, None) == attn.ATTN_ERR_INVALID_ARG
+    assert L.attn_selftest_abort(fp, fp, fp, fp, None, None, None, None, 1, 1, 128, 0, 64,
+                                 0.125, 0, attn.ATTN_BF16, 500, None) == attn.ATTN_ERR_INVALID_ARG
+    assert L.attn_selftest_abort(fp, fp, fp, fp, None, None, None, None, 1, 1, 128, 128, 96,
+                                 0.125, 0, attn.ATTN_BF16, 500, None) == attn.ATTN_ERR_UNSUPPORTED
     assert L.attn_selftest_wait(0, None) == attn.ATTN_ERR_INVALID_ARG
     assert L.attn_selftest_wait(20 * 1000 * 1000, None) == attn.ATTN_ERR_INVALID_ARG
 

@@ -179,6 +179,38 @@ def test_bounded_wait_times_out_and_context_stays_usable():
     check_full(synthetic.CASES["C1"], "tc")  # and the context still computes correctly
 
 
+ABORT = [
+    # B, H, N_q, N_k, d, causal, dtype: one per kernel form
+    (1, 2, 300, 300, 64, True, "bf16"),     # P in shared memory, two issuers, 16-bit
+    (1, 2, 300, 300, 128, True, "bf16"),    # P over S in TMEM, one issuer
+    (1, 2, 300, 300, 128, False, "e4m3"),   # P in shared memory, e4m3 with descales
+    (1, 2, 300, 300, 256, True, "bf16"),    # head dimension 256, one tile per CTA
+]
+
+
+@pytest.mark.parametrize("shape", ABORT, ids=lambda s: "x".join(map(str, s)))
+def test_attention_kernel_abort_path(shape):
+    """The attention kernel's own abort path: its K/V loader stops after the
+    first tile and every wait is limited to 500 us, so the waits for the
+    missing tiles run out; every role drains what it issued and frees TMEM.
+    The timeout is reported, cleared, and the next call is correct."""
+    B, H, N_q, N_k, d, causal, dtype = shape
+    case = synthetic.custom_case(B, H, N_q, N_k, d, causal, dtype, outliers=False,
+                                 seed=zlib.crc32(repr(shape).encode()) % 10000)
+    inputs = synthetic.make_inputs(case)
+    dev = to_device(inputs)
+    attn.attn_selftest_abort(dev["q"], dev["k"], dev["v"], dev.get("q_descale"),
+                             dev.get("k_descale"), dev.get("v_descale"), scale=case.scale,
+                             causal=causal, timeout_us=500)
+    with pytest.raises(attn.AttnError) as err:
+        attn.attn_check_status()
+    assert err.value.status == attn.ATTN_ERR_TIMEOUT
+    assert attn.attn_check_status() == attn.ATTN_OK
+    O, lse = run_gpu(case, dev, "tc")
+    O_ref, lse_ref = oracle_full(case, inputs)
+    compare(case, O, lse, O_ref, lse_ref)
+
+
 GQA = [
     # B, H, H_kv, N_q, N_k, d, causal, dtype
     (2, 8, 2, 300, 300, 128, True, "bf16"),
