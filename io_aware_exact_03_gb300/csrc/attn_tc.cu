@@ -64,56 +64,79 @@ struct Cfg {
     static constexpr int NC = RB / CB;                     // chunks per row
     static constexpr int TILE = BM * RB;                   // bytes per 128-row tile
     static constexpr int CHUNK = BM * CB;                  // bytes per chunk of a tile
-    // P_t in shared memory (K-major, 128-byte swizzle, like a Q tile of 128-byte
-    // rows) instead of over S_t in TMEM: S_t is free as soon as the softmax
-    // has loaded it, so the next Q K^T runs while the softmax works.  The
-    // cost is shared-memory bandwidth (128 B/clk per SM): the P V MMA then
-    // reads P from shared memory and the softmax writes it there.  For 16-bit
-    // types at d = 128 a step would move ~384 KB through shared memory, more
-    // than the MMAs' 2048 cycles allow (measured 14 % slower on the causal
-    // N = 16384 case), so they keep P over S in TMEM.
-    static constexpr bool P_SMEM = (KIND == kE4M3) || (D == 64);
-    // Warps: 0 producer; 1 MMA issuer (with P_SMEM: 1 and 2, one per tile,
-    // each answering only its own tile's barriers); then 2 x 4 softmax warps.
-    static constexpr int ISSUERS = P_SMEM ? 2 : 1;
+    // e4m3 inputs: P goes to the P V product as fp16, not e4m3.  An e4m3 P
+    // keeps 3 mantissa bits, so a weight that is a sizeable share of its row
+    // but not the row maximum is off by up to 2^-4 of itself, and with V
+    // values of a few tens (the 0.1 % x10 outliers) that is an O error of
+    // several 1e-2 to a few 1e-1 on rare rows; fp16 P (10 bits) keeps every
+    // row within about 1e-3 of exact.  The P V MMA is then kind::f16 with
+    // A = P in TMEM and B = V widened from e4m3 to fp16 in shared memory by
+    // the eight softmax warps, 64 bytes each, at the end of the previous step
+    // (every e4m3 value is exact in fp16).  TMEM: one score
+    // buffer S shared by the two tiles (each tile's softmax frees it as soon as
+    // it has loaded its scores, and the two issuers take turns), P_A, P_B
+    // (64 columns each) and O_A, O_B.
+    static constexpr bool F16P = (KIND == kE4M3);
+    // P_t in shared memory (K-major, 128-byte swizzle) instead of over S_t in
+    // TMEM (16-bit types at d = 64): S_t is free as soon as the softmax has
+    // loaded it, so the next Q K^T runs while the softmax works.  The cost is
+    // shared-memory bandwidth (128 B/clk per SM): for 16-bit types at d = 128
+    // a step would move ~384 KB through shared memory, more than the MMAs'
+    // 2048 cycles allow (measured 14 % slower on the causal N = 16384 case),
+    // so they keep P over S in TMEM.
+    static constexpr bool P_SMEM = !F16P && (D == 64);
+    // Warps: 0 producer; with P_SMEM or F16P, 1 and 2 are MMA issuers, one
+    // per tile, each answering only its own tile's barriers (without them
+    // warp 1 issues for both tiles); then 2 x 4 softmax warps.
+    static constexpr int ISSUERS = (P_SMEM || F16P) ? 2 : 1;
     // 16-bit inputs: the O tile (bf16 / fp16) is exactly a Q tile, so the
     // epilogue stages O in the tile's own Q buffer (free once its last P V is
     // done) and writes it with one TMA store.
     static constexpr bool TMA_O = (KIND != kE4M3);
     static constexpr int SOFTMAX_WARP0 = 1 + ISSUERS;
     static constexpr int THREADS = 32 * (SOFTMAX_WARP0 + 8);
-    static constexpr int PT = P_SMEM ? BM * BN * E : 0;    // bytes of one P tile
+    static constexpr int PT = P_SMEM ? BM * BN * E : 0;    // bytes of one P tile in smem
     static constexpr int P_CHUNK = BM * 128;               // bytes of a 128-byte-wide P chunk
-    // q_full, s_full x2, p_full x2, pv_done x2, drain, s_free x2, drain of issuer B
-    static constexpr int NB_FIXED = 1 + 2 + 2 + 2 + 1 + 2 + 1;
-    static constexpr int SLOTS_FIT = (kSmemLimit - 1024 - 2 * TILE - 2 * PT - 512) / TILE;
-    static constexpr int SLOTS = SLOTS_FIT > 8 ? 8 : SLOTS_FIT;  // K/V ring depth
+    // fp16 copy of one V tile (F16P): 128 keys x D, 128-byte swizzled chunks
+    // of 64 values, like a 16-bit V tile loaded by TMA
+    static constexpr int V16_CB = 2 * D >= 128 ? 128 : 2 * D;
+    static constexpr int V16_CHUNK = BN * V16_CB;
+    static constexpr int V16T = F16P ? BN * 2 * D : 0;
+    // q_full, s_full x2, p_full x2, pv_done x2, drain, s_free x2, drain of
+    // issuer B, v16_full x2, v16_empty x2
+    static constexpr int NB_FIXED = 1 + 2 + 2 + 2 + 1 + 2 + 1 + 4;
+    static constexpr int SLOTS_FIT =
+        (kSmemLimit - 1024 - 2 * TILE - 2 * PT - 2 * V16T - 512) / TILE;
+    // K/V ring depth; F16P needs it even (K items in even slots, V in odd)
+    static constexpr int SLOTS = (SLOTS_FIT > 8 ? 8 : SLOTS_FIT) & (F16P ? ~1 : ~0);
     static constexpr uint32_t LAYOUT = (CB == 128) ? 2u : 4u;  // 128B / 64B swizzle
-    static constexpr int MMA_K = 32 / E;                   // K per MMA instruction
+    static constexpr int MMA_K = 32 / E;                   // K per Q K^T MMA instruction
     static constexpr int NB = NB_FIXED + 2 * SLOTS;        // mbarriers
-    static constexpr size_t SMEM_USED = 1024 + (size_t)TILE * (2 + SLOTS) + 2 * PT + NB * 8 + 16;
+    static constexpr size_t SMEM_USED =
+        1024 + (size_t)TILE * (2 + SLOTS) + 2 * PT + 2 * (size_t)V16T + NB * 8 + 16;
     // at least ~120 KB so two CTAs never share an SM (each takes all of TMEM)
     static constexpr size_t SMEM = SMEM_USED > 122880 ? SMEM_USED : 122880;
     static constexpr uint32_t FMT = (KIND == kBF16) ? 1u : 0u;  // bf16 = 1, f16 / e4m3 = 0
     static constexpr uint32_t IDESC_QK = instr_desc(FMT, FMT, 0, 0, BM, BN);
-    static constexpr uint32_t IDESC_PV = instr_desc(FMT, FMT, 0, 1, BM, D);
-    static constexpr uint32_t P_COLS = BN * E / 4;         // TMEM columns holding P
+    // P V: 16-bit operands (F16P: fp16 P and fp16 V)
+    static constexpr uint32_t IDESC_PV = instr_desc(F16P ? 0u : FMT, F16P ? 0u : FMT, 0, 1, BM, D);
+    static constexpr int PV_K = 16;                        // keys per P V MMA instruction
+    static constexpr int PE = F16P ? 2 : E;                // bytes per P element
+    static constexpr uint32_t P_COLS = BN * PE / 4;        // TMEM columns holding P
     // Rescale the running output only when the row maximum grew by more than
     // this (log2 units): P values then stay <= 2^8, inside every P type's range.
     static constexpr float RESCALE_THRESHOLD = 8.0f;
-    // e4m3 P carries 3 mantissa bits, and O/l divides by the sum of the
-    // unrounded P, so a weight above 1 (the row grew past the stale maximum)
-    // is off by up to 2^-4 of itself.  That is harmless while the weight is a
-    // small share of the row's mass: e4m3 also rescales once the tile's
-    // largest weight exceeds this fraction of the sum accumulated so far.
-    static constexpr float RESCALE_MASS = 0.125f;
     static_assert(SLOTS >= 2, "K/V ring depth");
     static_assert(SMEM_USED <= (size_t)kSmemLimit, "shared memory budget");
 };
 
-// TMEM columns: S_A [0,128), S_B [128,256) (P_t overwrites the start of S_t),
-// O_A [256, 256+D), O_B [256+D, 256+2D).
-__device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
+// TMEM columns.  bf16 / fp16: S_A [0,128), S_B [128,256), P_t over the start
+// of S_t.  e4m3 (F16P): one S [0,128) for both tiles, P_A [128,192),
+// P_B [192,256).  O_A [256, 256+D), O_B [256+D, 256+2D).
+template <bool F16P>
+__device__ __forceinline__ uint32_t col_s(int t) { return F16P ? 0u : 128u * t; }
+template <bool F16P>
+__device__ __forceinline__ uint32_t col_p(int t) { return F16P ? 128u + 64u * t : 128u * t; }
 template <int D>
 __device__ __forceinline__ uint32_t col_o(int t) { return 256u + (uint32_t)(D * t); }
 
@@ -170,7 +193,8 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sQ = smem;                      // two tiles: A then B
     uint8_t* sP = smem + 2 * C::TILE;        // two P tiles (P_SMEM only)
-    uint8_t* sKV = sP + 2 * C::PT;           // SLOTS tiles
+    uint8_t* sV16 = sP + 2 * C::PT;          // two fp16 V tiles (F16P only)
+    uint8_t* sKV = sV16 + 2 * C::V16T;       // SLOTS tiles
     uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + (size_t)C::SLOTS * C::TILE);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NB);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -182,8 +206,10 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
     const uint32_t b_drain = smem_u32(bars + 7);
     const uint32_t b_s_free = smem_u32(bars + 8);     // + 8 * tile
     const uint32_t b_drain_b = smem_u32(bars + 10);
-    const uint32_t b_kv_full = smem_u32(bars + 11);               // + 8 * slot
-    const uint32_t b_kv_empty = smem_u32(bars + 11 + C::SLOTS);   // + 8 * slot
+    const uint32_t b_v16_full = smem_u32(bars + 11);  // + 8 * buffer (F16P)
+    const uint32_t b_v16_empty = smem_u32(bars + 13); // + 8 * buffer (F16P)
+    const uint32_t b_kv_full = smem_u32(bars + 15);               // + 8 * slot
+    const uint32_t b_kv_empty = smem_u32(bars + 15 + C::SLOTS);   // + 8 * slot
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -239,10 +265,15 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         }
         mbar_init(b_drain, 1);
         mbar_init(b_drain_b, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(b_v16_full + 8 * t, 256);  // every softmax thread converts a slice
+            mbar_init(b_v16_empty + 8 * t, 2);   // one release per tile's issuer
+        }
         for (int s = 0; s < C::SLOTS; ++s) {
             mbar_init(b_kv_full + 8 * s, 1);
-            // one release per issuer that reads the ring
-            mbar_init(b_kv_empty + 8 * s, C::ISSUERS);
+            // one release per issuer that reads the ring; F16P: V items (odd
+            // slots) are read by the eight softmax warps, one release each
+            mbar_init(b_kv_empty + 8 * s, (C::F16P && (s & 1)) ? 8 : C::ISSUERS);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -320,13 +351,28 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                         const uint64_t db = kd + off16;
                         const uint32_t acc = (c | ks) != 0;
                         if constexpr (KIND == kE4M3)
-                            mma_f8_ss_1(tmem + col_s(t), da, db, C::IDESC_QK, acc);
+                            mma_f8_ss_1(tmem + col_s<C::F16P>(t), da, db, C::IDESC_QK, acc);
                         else
-                            mma_f16_ss_1(tmem + col_s(t), da, db, C::IDESC_QK, acc);
+                            mma_f16_ss_1(tmem + col_s<C::F16P>(t), da, db, C::IDESC_QK, acc);
                     }
                 }
             };
             auto issue_pv = [&](int t, int slot, bool first) {
+                if constexpr (C::F16P) {
+                    // A = fp16 P_t in TMEM (8 columns per 16 keys); B = the fp16
+                    // V tile in buffer `slot`, MN-major: 8-key groups 8*128
+                    // bytes apart, 64-value d-chunks V16_CHUNK apart
+                    const uint64_t vd = smem_desc(smem_u32(sV16 + (size_t)slot * C::V16T),
+                                                  C::V16_CHUNK, 8 * C::V16_CB, 2u);
+#pragma unroll
+                    for (int ks = 0; ks < BN / C::PV_K; ++ks) {
+                        const uint64_t db = vd + ((uint32_t)(ks * C::PV_K * C::V16_CB) >> 4);
+                        const uint32_t acc = (!first || ks > 0) ? 1u : 0u;
+                        mma_f16_ts_1(tmem + col_o<D>(t), tmem + col_p<true>(t) + ks * (C::PV_K * 2 / 4),
+                                     db, C::IDESC_PV, acc);
+                    }
+                    return;
+                }
                 // V is MN-major: 8-key groups 8*CB apart, d-chunks CHUNK apart
                 const uint64_t vd =
                     smem_desc(smem_u32(sKV + (size_t)slot * C::TILE), C::CHUNK, 8 * C::CB, C::LAYOUT);
@@ -339,16 +385,10 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                         const uint32_t off = (ks * 32 / 128) * C::P_CHUNK + (ks * 32) % 128;
                         const uint64_t da =
                             smem_desc(smem_u32(sP + t * C::PT) + off, 16, 1024, 2u);
-                        if constexpr (KIND == kE4M3)
-                            mma_f8_ss_1(tmem + col_o<D>(t), da, db, C::IDESC_PV, acc);
-                        else
-                            mma_f16_ss_1(tmem + col_o<D>(t), da, db, C::IDESC_PV, acc);
+                        mma_f16_ss_1(tmem + col_o<D>(t), da, db, C::IDESC_PV, acc);
                     } else {
-                        const uint32_t a_tmem = tmem + col_s(t) + ks * (C::MMA_K * C::E / 4);
-                        if constexpr (KIND == kE4M3)
-                            mma_f8_ts_1(tmem + col_o<D>(t), a_tmem, db, C::IDESC_PV, acc);
-                        else
-                            mma_f16_ts_1(tmem + col_o<D>(t), a_tmem, db, C::IDESC_PV, acc);
+                        const uint32_t a_tmem = tmem + col_p<false>(t) + ks * (C::MMA_K * C::E / 4);
+                        mma_f16_ts_1(tmem + col_o<D>(t), a_tmem, db, C::IDESC_PV, acc);
                     }
                 }
             };
@@ -356,7 +396,76 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             auto par_of = [](int it) { return (uint32_t)(it / C::SLOTS) & 1u; };
 
             bool ok = true;
-            if constexpr (C::P_SMEM) {
+            if constexpr (C::F16P) {
+                // One issuer per tile; the two share one TMEM score buffer S.
+                // The score MMAs into S run in the order A_0 B_0 A_1 B_1 ...
+                // (a tile past its own key range drops out), and each waits
+                // until the softmax of the one before it has loaded its scores
+                // (s_free).  P_t V_j reads fp16 P_t from TMEM and the fp16 copy
+                // of V_j the softmax warps wrote into buffer j % 2; the buffer is
+                // released when the MMA has read it.  Key tiles this tile
+                // never reads release their K slot and V buffer once filled.
+                const int t = __shfl_sync(0xffffffffu, warp, 0) - 1;
+                const int nt = n_kv[t], nt_o = n_kv[1 - t];
+                const uint32_t drain_t = t == 0 ? b_drain : b_drain_b;
+                auto s_ready = [&](int j) -> bool {
+                    int pt = -1, pj = 0;  // the score MMA before tile t's j-th
+                    if (t == 0) {
+                        if (j >= 1) {
+                            pt = (j - 1 < nt_o) ? 1 : 0;
+                            pj = j - 1;
+                        }
+                    } else if (j < nt_o) {
+                        pt = 0;
+                        pj = j;
+                    } else if (j >= 1) {
+                        pt = 1;
+                        pj = j - 1;
+                    }
+                    return pt < 0 || wb(b_s_free + 8 * pt, (uint32_t)pj & 1u);
+                };
+                ok = wb(b_q_full, 0);
+                if (ok && nt > 0) {
+                    ok = wb(b_kv_full + 8 * slot_of(0), par_of(0));
+                    if (ok) ok = s_ready(0);
+                    if (ok) {
+                        tc_fence_after();
+                        issue_qk(t, slot_of(0));
+                        mma_commit_1(b_s_full + 8 * t);
+                        mma_commit_1(b_kv_empty + 8 * slot_of(0));
+                    }
+                }
+                for (int j = 0; j < nt && ok; ++j) {
+                    const int itK = 2 * j + 2;
+                    if (j + 1 < nt) {
+                        ok = wb(b_kv_full + 8 * slot_of(itK), par_of(itK));
+                        if (ok) ok = s_ready(j + 1);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_qk(t, slot_of(itK));
+                        mma_commit_1(b_s_full + 8 * t);
+                        mma_commit_1(b_kv_empty + 8 * slot_of(itK));
+                    }
+                    ok = wb(b_v16_full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u);
+                    if (ok) ok = wb(b_p_full + 8 * t, (uint32_t)j & 1u);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(t, j & 1, j == 0);
+                    mma_commit_1(b_pv_done + 8 * t);
+                    mma_commit_1(b_v16_empty + 8 * (j & 1));
+                }
+                for (int j = nt; j < n_max && ok; ++j) {
+                    ok = wb(b_kv_full + 8 * slot_of(2 * j), par_of(2 * j));
+                    if (ok) mbar_arrive_1(b_kv_empty + 8 * slot_of(2 * j));
+                    if (ok) ok = wb(b_v16_full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u);
+                    if (ok) mbar_arrive_1(b_v16_empty + 8 * (j & 1));
+                }
+                if (!ok) {
+                    // make sure none of this issuer's MMAs still runs when TMEM is freed
+                    mma_commit_1(drain_t);
+                    wait_drain(drain_t, 0, p.drain_ns);
+                }
+            } else if constexpr (C::P_SMEM) {
                 // One issuer per tile.  S_t is free once the softmax has loaded
                 // it, so the scores of K_{j+1} are issued as soon as that
                 // happens and run while the softmax works; P_t V_j follows when
@@ -425,7 +534,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             // MMA overwrites it; no completion wait is needed in between.
             // While softmax A works, the tensor core runs tile B's pair of MMAs
             // and the other way round.
-            for (int j = 0; j < n_max && ok && !C::P_SMEM; ++j) {
+            for (int j = 0; j < n_max && ok && !C::P_SMEM && !C::F16P; ++j) {
                 const int itV = 2 * j + 1, itK = 2 * j + 2;
                 ok = wb(b_kv_full + 8 * slot_of(itV), par_of(itV));
                 bool k_ready = false;
@@ -456,7 +565,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                     mma_commit_1(b_kv_empty + 8 * slot_of(itK));
                 }
             }
-            if (!ok && !C::P_SMEM) {
+            if (!ok && !C::P_SMEM && !C::F16P) {
                 // make sure no MMA is still reading or writing when TMEM is freed
                 mma_commit_1(b_drain);
                 wait_drain(b_drain, 0, p.drain_ns);
@@ -491,7 +600,63 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         const uint32_t p_row = smem_u32(sP + t * C::PT) + (uint32_t)(r >> 3) * 1024u +
                                (uint32_t)(r & 7) * 128u;
 
-        for (int j = 0; j < nt; ++j) {
+        // F16P: every softmax thread (both tiles' warps, whichever key tiles
+        // its own tile reads) widens a 64-byte share of each e4m3 V tile into
+        // the fp16 buffer jv % 2: 16-byte units g, g + 256, ... of the tile.
+        // V_0 before the first step, V_{j+1} at the end of step j (where the
+        // softmax would otherwise wait for its next scores), and the V tiles
+        // past this tile's own key range after its last step.  The ring slot
+        // is released by one lane of each of the eight warps, the buffer is
+        // full when all 256 threads have arrived.
+        const int gv = (warp - C::SOFTMAX_WARP0) * 32 + lane;
+        auto convert_v = [&](int jv) -> bool {
+            const int itV = 2 * jv + 1;
+            const int slot = itV % C::SLOTS;
+            bool okc = __all_sync(0xffffffffu, wait_bar(b_kv_full + 8 * slot,
+                                                        (uint32_t)(itV / C::SLOTS) & 1u, abort_flag, lim));
+            if (okc)
+                okc = __all_sync(0xffffffffu, wait_bar(b_v16_empty + 8 * (jv & 1),
+                                                       ((uint32_t)(jv >> 1) & 1u) ^ 1u, abort_flag, lim));
+            if (!okc) return false;
+            const uint32_t src = smem_u32(sKV + (size_t)slot * C::TILE);
+            const uint32_t dst = smem_u32(sV16 + (size_t)(jv & 1) * C::V16T);
+            constexpr int UNITS = C::CB / 16;        // 16-byte units per e4m3 row
+            constexpr int PER = BN * UNITS / 256;    // units per thread
+            uint32_t x[PER][4];
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int u = gv + 256 * k, rr = u / UNITS, w = u % UNITS;
+                // e4m3 row rr: 128-byte swizzle (w ^ rr%8) or 64-byte (w ^ (rr/2)%4)
+                const int wp = (C::CB == 128) ? (w ^ (rr & 7)) : (w ^ ((rr >> 1) & 3));
+                ld_shared_v4(src + (uint32_t)(rr * C::CB + wp * 16), x[k]);
+            }
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int u = gv + 256 * k, rr = u / UNITS, w = u % UNITS;
+                uint32_t hv[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    hv[2 * e] = e4m3x2_to_f16x2((uint16_t)(x[k][e] & 0xffffu));
+                    hv[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(x[k][e] >> 16));
+                }
+                // values d = 16 w .. 16 w + 15: fp16 chunk w / 4, units 2 (w % 4), +1
+                const uint32_t row = dst + (uint32_t)((w >> 2) * C::V16_CHUNK + rr * C::V16_CB);
+                const int u0 = 2 * (w & 3);
+                st_shared_v4(row + (uint32_t)((u0 ^ (rr & 7)) << 4), hv[0], hv[1], hv[2], hv[3]);
+                st_shared_v4(row + (uint32_t)(((u0 + 1) ^ (rr & 7)) << 4), hv[4], hv[5], hv[6],
+                             hv[7]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(b_v16_full + 8 * (jv & 1));
+            __syncwarp();
+            mbar_arrive_1(b_kv_empty + 8 * slot);
+            return true;
+        };
+        if constexpr (C::F16P) {
+            if (n_max > 0) ok = convert_v(0);
+        }
+
+        for (int j = 0; j < nt && ok; ++j) {
             if (!__all_sync(0xffffffffu, wait_bar(s_full, (uint32_t)j & 1u, abort_flag, lim))) {
                 ok = false;
                 break;
@@ -501,14 +666,14 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             uint32_t sr[BN];
 #pragma unroll
             for (int u = 0; u < BN / 32; ++u)
-                tmem_ld32(t_row + col_s(t) + 32 * u,
+                tmem_ld32(t_row + col_s<C::F16P>(t) + 32 * u,
                           *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * u]));
             tmem_ld_wait();
 #pragma unroll
             for (int u = 0; u < BN / 32; ++u)
                 reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[32 * u]));
-            if constexpr (C::P_SMEM) {
-                // S_t is in registers: the next scores may overwrite it
+            if constexpr (C::P_SMEM || C::F16P) {
+                // the scores are in registers: the next score MMA may overwrite them
                 tc_fence_before();
                 mbar_arrive(b_s_free + 8 * t);
             }
@@ -535,9 +700,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             const float mx = max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]),
                                   fmaxf(mc[6], mc[7]));
             const float m_new = mx * c;
-            bool need = m_new > m_used + C::RESCALE_THRESHOLD;
-            if (KIND == kE4M3)
-                need = need || (m_new > m_used && ex2(m_new - m_used) > l * C::RESCALE_MASS);
+            const bool need = m_new > m_used + C::RESCALE_THRESHOLD;
             const bool any = __any_sync(0xffffffffu, need);
             float alpha = 1.f;
             if (any) {
@@ -549,48 +712,36 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             float sc[8];  // independent partial row sums (four packed pairs)
 #pragma unroll
             for (int k = 0; k < 8; ++k) sc[k] = 0.f;
-            // P_t goes over the first P_COLS columns of S_t (already read above;
-            // the previous P_t V MMA read P before this S_t was written), 32
-            // columns at a time so only one chunk of packed P is live.  The
-            // scale-and-subtract and the sums use packed f32x2 instructions:
-            // this loop is bound by instruction issue, not by ex2 throughput.
-            constexpr int PER_CHUNK = 32 * 4 / C::E;  // score columns per 32 TMEM columns
+            // P_t as bf16 / fp16 (e4m3 inputs: fp16), 32 TMEM columns (64
+            // scores) at a time so only one chunk of packed P is live.  P over
+            // S: the first P_COLS columns of S_t, already read above (the
+            // previous P_t V MMA read P before this S_t was written).  P in
+            // shared memory or in its own TMEM buffer (F16P): the buffer is
+            // free once P_{j-1} V_{j-1} has completed.  The scale-and-subtract
+            // and the sums use packed f32x2 instructions.
+            constexpr int PER_CHUNK = 32 * 4 / C::PE;  // score columns per 32 TMEM columns
 #pragma unroll
             for (int u = 0; u < (int)C::P_COLS / 32; ++u) {
                 uint32_t pk[32];
-                if constexpr (KIND == kE4M3) {
 #pragma unroll
-                    for (int x = 0; x < PER_CHUNK; x += 4) {
-                        const int y = u * PER_CHUNK + x;
-                        float a0, a1, a2, a3;
-                        ffma2(a0, a1, s[y], s[y + 1], c, c, -m_ref, -m_ref);
-                        ffma2(a2, a3, s[y + 2], s[y + 3], c, c, -m_ref, -m_ref);
-                        const float p0 = ex2(a0), p1 = ex2(a1), p2 = ex2(a2), p3 = ex2(a3);
-                        const int k = ((x / 4) & 3) * 2;
-                        fadd2(sc[k], sc[k + 1], sc[k], sc[k + 1], p0, p1);
-                        fadd2(sc[k], sc[k + 1], sc[k], sc[k + 1], p2, p3);
-                        pk[x / 4] = pack_e4m3(p0, p1, p2, p3);
-                    }
-                } else {
-#pragma unroll
-                    for (int x = 0; x < PER_CHUNK; x += 2) {
-                        const int y = u * PER_CHUNK + x;
-                        float a0, a1;
-                        ffma2(a0, a1, s[y], s[y + 1], c, c, -m_ref, -m_ref);
-                        const float p0 = ex2(a0), p1 = ex2(a1);
-                        const int k = ((x / 2) & 3) * 2;
-                        fadd2(sc[k], sc[k + 1], sc[k], sc[k + 1], p0, p1);
-                        pk[x / 2] = (KIND == kBF16) ? pack_bf16(p0, p1) : pack_f16(p0, p1);
-                    }
+                for (int x = 0; x < PER_CHUNK; x += 2) {
+                    const int y = u * PER_CHUNK + x;
+                    float a0, a1;
+                    ffma2(a0, a1, s[y], s[y + 1], c, c, -m_ref, -m_ref);
+                    const float p0 = ex2(a0), p1 = ex2(a1);
+                    const int k = ((x / 2) & 3) * 2;
+                    fadd2(sc[k], sc[k + 1], sc[k], sc[k + 1], p0, p1);
+                    pk[x / 2] = (KIND == kBF16) ? pack_bf16(p0, p1) : pack_f16(p0, p1);
                 }
-                if constexpr (C::P_SMEM) {
-                    // the buffer is free once P_{j-1} V_{j-1} has completed
+                if constexpr (C::P_SMEM || C::F16P) {
                     if (u == 0 && j > 0 &&
                         !__all_sync(0xffffffffu, wait_bar(pv_done, (uint32_t)(j - 1) & 1u,
                                                           abort_flag, lim))) {
                         ok = false;
                         break;
                     }
+                }
+                if constexpr (C::P_SMEM) {
                     // row r of a 128-byte-swizzled K-major tile: 16-byte unit w
                     // sits at unit w ^ (r % 8)
                     const uint32_t row_base =
@@ -600,7 +751,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                         st_shared_v4(row_base + ((uint32_t)(w ^ (r & 7)) << 4), pk[4 * w],
                                      pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
                 } else {
-                    tmem_st32(t_row + col_s(t) + 32 * u, pk);
+                    tmem_st32(t_row + col_p<C::F16P>(t) + 32 * u, pk);
                 }
             }
             if (!ok) break;
@@ -642,6 +793,16 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(p_full);
+            if constexpr (C::F16P) {
+                if (j + 1 < n_max && !convert_v(j + 1)) {
+                    ok = false;
+                    break;
+                }
+            }
+        }
+        if constexpr (C::F16P) {
+            // V tiles past this tile's key range (the other tile reads them)
+            for (int jv = nt + 1; jv < n_max && ok; ++jv) ok = convert_v(jv);
         }
 
         if (ok && nt > 0)

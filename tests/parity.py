@@ -11,11 +11,21 @@ import oracle
 import synthetic
 
 # Tolerances stated for this path (O max / mean absolute error, lse absolute error).
+# e4m3: O is written as bf16, whose spacing is 0.125 for |O| in [16, 32) and
+# 0.25 in [32, 64) (C5's x10 outliers put |O| near 40 on some rows), so the
+# 6e-2 bound is read as a bound on the computation: each element may also be
+# off by half a bf16 ulp of the exact value, its own output rounding.
 TOL = {
     "bf16": dict(o_max=1e-2, o_mean=1e-3, lse=1e-3),
     "fp16": dict(o_max=1e-2, o_mean=1e-3, lse=1e-3),
-    "e4m3": dict(o_max=6e-2, o_mean=None, lse=1e-3),
+    "e4m3": dict(o_max=6e-2, o_mean=None, lse=1e-3, out_half_ulp=True),
 }
+
+
+def bf16_half_ulp(x):
+    """Half the spacing of bf16 values (8 significant bits) at |x|."""
+    ax = np.maximum(np.abs(np.asarray(x, dtype=np.float64)), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(ax)) - 8.0)
 
 
 def to_device(inputs: dict) -> dict:
@@ -68,8 +78,10 @@ def compare(case, O_gpu, lse_gpu, O_ref, lse_ref, tol=None):
     assert O_gpu.shape == O_ref.shape
     assert np.all(np.isfinite(O_gpu)), "non-finite output"
     err = np.abs(O_gpu - O_ref)
-    msg = f"{case.name}: O max err {err.max():.3e} mean {err.mean():.3e}"
-    assert err.max() <= tol["o_max"], msg
+    bound = tol["o_max"] + (bf16_half_ulp(O_ref) if tol.get("out_half_ulp") else 0.0)
+    msg = (f"{case.name}: O max err {err.max():.3e} mean {err.mean():.3e}, "
+           f"worst excess over the bound {(err - bound).max():.3e}")
+    assert np.all(err <= bound), msg
     if tol["o_mean"] is not None:
         assert err.mean() <= tol["o_mean"], msg
     lse_gpu = np.asarray(lse_gpu)

@@ -18,7 +18,8 @@ import torch
 
 import io_aware_exact_03_gb300 as attn
 import synthetic
-from parity import check_full, check_sampled, compare, oracle_full, run_gpu, to_device
+import oracle
+from parity import TOL, check_full, check_sampled, compare, oracle_full, run_gpu, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -232,24 +233,40 @@ def test_gqa_matches_oracle(shape):
     compare(case, O, lse, O_ref, lse_ref)
 
 
-def test_c5_full_output_error_distribution():
-    """Every row of C5, not a sample: the e4m3 tensor-core kernel against the
-    CUDA-core kernel (fp32 scores and P, within 2.6e-2 of the oracle on C5's
-    worst rows).  e4m3 P carries 3 mantissa bits, so a weight is off by up to
-    2^-4 of itself, and with C5's x10 outliers |v| reaches ~42: on a row where
-    an outlier value carries a large weight the O error exceeds the 6e-2 that
-    holds on the seeded sample (measured: 80 of 262144 rows, max 0.31).  This
-    pins the distribution so it cannot silently widen."""
+def test_c5_every_row_within_the_fp8_tolerance():
+    """C5 (B2 H16 N8192 d128, e4m3 with 0.1 % x10 outliers) against the fp64
+    oracle at the stated FP8 bound (O max abs error <= 6e-2 beyond the bf16
+    output's own rounding, lse <= 1e-3) on 4096 seeded rows plus the 256 rows
+    where the tensor-core kernel and the CUDA-core kernel (fp32 scores, fp32
+    P) differ most, out of all 262 144.  Over every row the two kernels agree
+    within 1e-2 beyond one bf16 ulp (each output is rounded on its own), and
+    the CUDA-core kernel is within 1e-3 (plus its rounding) of the oracle on
+    the checked rows."""
     case = synthetic.CASES["C5"]
-    dev = to_device(synthetic.make_inputs(case))
-    o1, _ = attn.attn_fwd_fp8(dev["q"], dev["k"], dev["v"], dev["q_descale"], dev["k_descale"],
-                              dev["v_descale"], scale=case.scale)
-    o2, _ = attn.attn_fwd_simt(dev["q"], dev["k"], dev["v"], scale=case.scale,
-                               q_descale=dev["q_descale"], k_descale=dev["k_descale"],
-                               v_descale=dev["v_descale"])
+    inputs = synthetic.make_inputs(case)
+    dev = to_device(inputs)
+    o1, l1 = attn.attn_fwd_fp8(dev["q"], dev["k"], dev["v"], dev["q_descale"], dev["k_descale"],
+                               dev["v_descale"], scale=case.scale)
+    o2, l2 = attn.attn_fwd_simt(dev["q"], dev["k"], dev["v"], scale=case.scale,
+                                q_descale=dev["q_descale"], k_descale=dev["k_descale"],
+                                v_descale=dev["v_descale"])
     attn.attn_check_status()
-    rowmax = (o1.float() - o2.float()).abs().amax(dim=3).flatten()
-    assert rowmax.median().item() <= 5e-3
-    assert torch.quantile(rowmax.cpu(), 0.999).item() <= 6e-2
-    assert (rowmax > 6e-2).float().mean().item() <= 1e-3
-    assert rowmax.max().item() <= 0.5
+    tol = TOL["e4m3"]
+    a1, a2 = o1.float(), o2.float()
+    big = torch.maximum(a1.abs(), a2.abs()).clamp_min(2.0 ** -126)
+    ulp = torch.exp2(torch.floor(torch.log2(big)) - 7.0)             # one bf16 ulp
+    excess = (a1 - a2).abs() - ulp
+    assert excess.max().item() <= 1e-2
+    rowmax = excess.amax(dim=3)                                      # [B, N, H]
+    worst = torch.topk(rowmax.flatten(), 256).indices.cpu().numpy()
+    B, N, H = rowmax.shape
+    wb, rem = np.divmod(worst, N * H)
+    wi, wh = np.divmod(rem, H)
+    rows = np.concatenate([np.stack([wb, wh, wi], axis=1),
+                           synthetic.sample_rows(case, 4096, seed=case.seed + 500)]).astype(np.int64)
+    q, k, v = oracle.case_inputs_f64(inputs)
+    O_ref, lse_ref = oracle.attention_rows(q, k, v, case.scale, False, rows)
+    for o, lse, t in ((o1, l1, tol), (o2, l2, dict(tol, o_max=1e-3))):
+        O_s = o.double().cpu().numpy()[rows[:, 0], rows[:, 2], rows[:, 1]]
+        lse_s = lse.double().cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
+        compare(case, O_s, lse_s, O_ref, lse_ref, tol=t)
