@@ -70,9 +70,9 @@ struct Cfg {
     // values of a few tens (the 0.1 % x10 outliers) that is an O error of
     // several 1e-2 to a few 1e-1 on rare rows; fp16 P (10 bits) keeps every
     // row within about 1e-3 of exact.  The P V MMA is then kind::f16 with
-    // A = P in TMEM and B = V widened from e4m3 to fp16 in shared memory by
-    // the eight softmax warps, 64 bytes each, at the end of the previous step
-    // (every e4m3 value is exact in fp16).  TMEM: one score
+    // A = P in TMEM and B = V widened from e4m3 to fp16 in shared memory by a
+    // converter warp, a tile ahead of its use (every e4m3 value is exact in
+    // fp16).  TMEM: one score
     // buffer S shared by the two tiles (each tile's softmax frees it as soon as
     // it has loaded its scores, and the two issuers take turns), P_A, P_B
     // (64 columns each) and O_A, O_B.
@@ -87,14 +87,16 @@ struct Cfg {
     static constexpr bool P_SMEM = !F16P && (D == 64);
     // Warps: 0 producer; with P_SMEM or F16P, 1 and 2 are MMA issuers, one
     // per tile, each answering only its own tile's barriers (without them
-    // warp 1 issues for both tiles); then 2 x 4 softmax warps.
+    // warp 1 issues for both tiles); then 2 x 4 softmax warps; F16P adds a
+    // V converter warp last.
     static constexpr int ISSUERS = (P_SMEM || F16P) ? 2 : 1;
     // 16-bit inputs: the O tile (bf16 / fp16) is exactly a Q tile, so the
     // epilogue stages O in the tile's own Q buffer (free once its last P V is
     // done) and writes it with one TMA store.
     static constexpr bool TMA_O = (KIND != kE4M3);
     static constexpr int SOFTMAX_WARP0 = 1 + ISSUERS;
-    static constexpr int THREADS = 32 * (SOFTMAX_WARP0 + 8);
+    static constexpr int CONVERTER_WARP = SOFTMAX_WARP0 + 8;
+    static constexpr int THREADS = 32 * (SOFTMAX_WARP0 + 8 + (F16P ? 1 : 0));
     static constexpr int PT = P_SMEM ? BM * BN * E : 0;    // bytes of one P tile in smem
     static constexpr int P_CHUNK = BM * 128;               // bytes of a 128-byte-wide P chunk
     // fp16 copy of one V tile (F16P): 128 keys x D, 128-byte swizzled chunks
@@ -259,21 +261,21 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         mbar_init(b_q_full, 1);
         for (int t = 0; t < 2; ++t) {
             mbar_init(b_s_full + 8 * t, 1);
-            mbar_init(b_p_full + 8 * t, 128);
+            mbar_init(b_p_full + 8 * t, 4);    // one arrival per softmax warp
             mbar_init(b_pv_done + 8 * t, 1);
-            mbar_init(b_s_free + 8 * t, 128);
+            mbar_init(b_s_free + 8 * t, 4);    // one arrival per softmax warp
         }
         mbar_init(b_drain, 1);
         mbar_init(b_drain_b, 1);
         for (int t = 0; t < 2; ++t) {
-            mbar_init(b_v16_full + 8 * t, 256);  // every softmax thread converts a slice
+            mbar_init(b_v16_full + 8 * t, 1);    // the converter warp
             mbar_init(b_v16_empty + 8 * t, 2);   // one release per tile's issuer
         }
         for (int s = 0; s < C::SLOTS; ++s) {
             mbar_init(b_kv_full + 8 * s, 1);
             // one release per issuer that reads the ring; F16P: V items (odd
-            // slots) are read by the eight softmax warps, one release each
-            mbar_init(b_kv_empty + 8 * s, (C::F16P && (s & 1)) ? 8 : C::ISSUERS);
+            // slots) are read only by the converter
+            mbar_init(b_kv_empty + 8 * s, (C::F16P && (s & 1)) ? 1 : C::ISSUERS);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -402,7 +404,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                 // (a tile past its own key range drops out), and each waits
                 // until the softmax of the one before it has loaded its scores
                 // (s_free).  P_t V_j reads fp16 P_t from TMEM and the fp16 copy
-                // of V_j the softmax warps wrote into buffer j % 2; the buffer is
+                // of V_j the converter wrote into buffer j % 2; the buffer is
                 // released when the MMA has read it.  Key tiles this tile
                 // never reads release their K slot and V buffer once filled.
                 const int t = __shfl_sync(0xffffffffu, warp, 0) - 1;
@@ -572,6 +574,62 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             }
         }
         __syncwarp();
+    } else if (C::F16P && warp == C::CONVERTER_WARP) {
+        // ------------------------------------------- V converter (F16P only)
+        // Widens each e4m3 V tile (ring slot) into an fp16 tile in buffer
+        // j % 2, laid out as a 16-bit V tile loaded by TMA would be (128-byte
+        // rows of 64 values, 128-byte swizzle); every e4m3 value is exact in
+        // fp16.  Loads go out eight at a time so their latency overlaps.  The
+        // ring slot is released once read; the buffer is handed to both
+        // issuers through v16_full (every lane's writes fenced for the async
+        // proxy, then one arrival for the warp).  It waits for the buffer to
+        // be released by both tiles' P V MMAs of two tiles earlier.
+        constexpr int UNITS = C::CB / 16;        // 16-byte units per e4m3 row
+        constexpr int PER = BN * UNITS / 32;     // units per lane
+        constexpr int BATCH = 8;
+        for (int j = 0; j < n_max; ++j) {
+            const int itV = 2 * j + 1;
+            const int slot = itV % C::SLOTS;
+            bool ok = __all_sync(0xffffffffu, wait_bar(b_kv_full + 8 * slot,
+                                                       (uint32_t)(itV / C::SLOTS) & 1u, abort_flag, lim));
+            if (ok)
+                ok = __all_sync(0xffffffffu, wait_bar(b_v16_empty + 8 * (j & 1),
+                                                      ((uint32_t)(j >> 1) & 1u) ^ 1u, abort_flag, lim));
+            if (!ok) break;
+            const uint32_t src = smem_u32(sKV + (size_t)slot * C::TILE);
+            const uint32_t dst = smem_u32(sV16 + (size_t)(j & 1) * C::V16T);
+#pragma unroll
+            for (int k0 = 0; k0 < PER; k0 += BATCH) {
+                uint32_t x[BATCH][4];
+#pragma unroll
+                for (int k = 0; k < BATCH; ++k) {
+                    const int u = lane + 32 * (k0 + k), rr = u / UNITS, w = u % UNITS;
+                    // e4m3 row rr: 128-byte swizzle (w ^ rr%8) or 64-byte (w ^ (rr/2)%4)
+                    const int wp = (C::CB == 128) ? (w ^ (rr & 7)) : (w ^ ((rr >> 1) & 3));
+                    ld_shared_v4(src + (uint32_t)(rr * C::CB + wp * 16), x[k]);
+                }
+#pragma unroll
+                for (int k = 0; k < BATCH; ++k) {
+                    const int u = lane + 32 * (k0 + k), rr = u / UNITS, w = u % UNITS;
+                    uint32_t hv[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        hv[2 * e] = e4m3x2_to_f16x2((uint16_t)(x[k][e] & 0xffffu));
+                        hv[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(x[k][e] >> 16));
+                    }
+                    // values d = 16 w .. 16 w + 15: fp16 chunk w / 4, units 2 (w % 4), +1
+                    const uint32_t row = dst + (uint32_t)((w >> 2) * C::V16_CHUNK + rr * C::V16_CB);
+                    const int u0 = 2 * (w & 3);
+                    st_shared_v4(row + (uint32_t)((u0 ^ (rr & 7)) << 4), hv[0], hv[1], hv[2], hv[3]);
+                    st_shared_v4(row + (uint32_t)(((u0 + 1) ^ (rr & 7)) << 4), hv[4], hv[5], hv[6],
+                                 hv[7]);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            mbar_arrive_1(b_v16_full + 8 * (j & 1));
+            mbar_arrive_1(b_kv_empty + 8 * slot);
+        }
     } else {
         // --------------------------------------- softmax + epilogue (2 x 128 thr)
         const int t = (warp - C::SOFTMAX_WARP0) >> 2;  // tile of this warp group
@@ -600,62 +658,6 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         const uint32_t p_row = smem_u32(sP + t * C::PT) + (uint32_t)(r >> 3) * 1024u +
                                (uint32_t)(r & 7) * 128u;
 
-        // F16P: every softmax thread (both tiles' warps, whichever key tiles
-        // its own tile reads) widens a 64-byte share of each e4m3 V tile into
-        // the fp16 buffer jv % 2: 16-byte units g, g + 256, ... of the tile.
-        // V_0 before the first step, V_{j+1} at the end of step j (where the
-        // softmax would otherwise wait for its next scores), and the V tiles
-        // past this tile's own key range after its last step.  The ring slot
-        // is released by one lane of each of the eight warps, the buffer is
-        // full when all 256 threads have arrived.
-        const int gv = (warp - C::SOFTMAX_WARP0) * 32 + lane;
-        auto convert_v = [&](int jv) -> bool {
-            const int itV = 2 * jv + 1;
-            const int slot = itV % C::SLOTS;
-            bool okc = __all_sync(0xffffffffu, wait_bar(b_kv_full + 8 * slot,
-                                                        (uint32_t)(itV / C::SLOTS) & 1u, abort_flag, lim));
-            if (okc)
-                okc = __all_sync(0xffffffffu, wait_bar(b_v16_empty + 8 * (jv & 1),
-                                                       ((uint32_t)(jv >> 1) & 1u) ^ 1u, abort_flag, lim));
-            if (!okc) return false;
-            const uint32_t src = smem_u32(sKV + (size_t)slot * C::TILE);
-            const uint32_t dst = smem_u32(sV16 + (size_t)(jv & 1) * C::V16T);
-            constexpr int UNITS = C::CB / 16;        // 16-byte units per e4m3 row
-            constexpr int PER = BN * UNITS / 256;    // units per thread
-            uint32_t x[PER][4];
-#pragma unroll
-            for (int k = 0; k < PER; ++k) {
-                const int u = gv + 256 * k, rr = u / UNITS, w = u % UNITS;
-                // e4m3 row rr: 128-byte swizzle (w ^ rr%8) or 64-byte (w ^ (rr/2)%4)
-                const int wp = (C::CB == 128) ? (w ^ (rr & 7)) : (w ^ ((rr >> 1) & 3));
-                ld_shared_v4(src + (uint32_t)(rr * C::CB + wp * 16), x[k]);
-            }
-#pragma unroll
-            for (int k = 0; k < PER; ++k) {
-                const int u = gv + 256 * k, rr = u / UNITS, w = u % UNITS;
-                uint32_t hv[8];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    hv[2 * e] = e4m3x2_to_f16x2((uint16_t)(x[k][e] & 0xffffu));
-                    hv[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(x[k][e] >> 16));
-                }
-                // values d = 16 w .. 16 w + 15: fp16 chunk w / 4, units 2 (w % 4), +1
-                const uint32_t row = dst + (uint32_t)((w >> 2) * C::V16_CHUNK + rr * C::V16_CB);
-                const int u0 = 2 * (w & 3);
-                st_shared_v4(row + (uint32_t)((u0 ^ (rr & 7)) << 4), hv[0], hv[1], hv[2], hv[3]);
-                st_shared_v4(row + (uint32_t)(((u0 + 1) ^ (rr & 7)) << 4), hv[4], hv[5], hv[6],
-                             hv[7]);
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(b_v16_full + 8 * (jv & 1));
-            __syncwarp();
-            mbar_arrive_1(b_kv_empty + 8 * slot);
-            return true;
-        };
-        if constexpr (C::F16P) {
-            if (n_max > 0) ok = convert_v(0);
-        }
-
         for (int j = 0; j < nt && ok; ++j) {
             if (!__all_sync(0xffffffffu, wait_bar(s_full, (uint32_t)j & 1u, abort_flag, lim))) {
                 ok = false;
@@ -675,7 +677,8 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             if constexpr (C::P_SMEM || C::F16P) {
                 // the scores are in registers: the next score MMA may overwrite them
                 tc_fence_before();
-                mbar_arrive(b_s_free + 8 * t);
+                __syncwarp();
+                mbar_arrive_1(b_s_free + 8 * t);
             }
             float s[BN];
 #pragma unroll
@@ -763,8 +766,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             if (any && j > 0) {
                 // O_t is touched only to rescale it; it is stable once
                 // P_{j-1} V_{j-1} has completed
-                if (!__all_sync(0xffffffffu,
-                                wait_bar(pv_done, (uint32_t)(j - 1) & 1u, abort_flag, lim))) {
+                if (!__all_sync(0xffffffffu, wait_bar(pv_done, (uint32_t)(j - 1) & 1u, abort_flag, lim))) {
                     ok = false;
                     break;
                 }
@@ -792,18 +794,10 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(p_full);
-            if constexpr (C::F16P) {
-                if (j + 1 < n_max && !convert_v(j + 1)) {
-                    ok = false;
-                    break;
-                }
-            }
+            __syncwarp();
+            mbar_arrive_1(p_full);
         }
-        if constexpr (C::F16P) {
-            // V tiles past this tile's key range (the other tile reads them)
-            for (int jv = nt + 1; jv < n_max && ok; ++jv) ok = convert_v(jv);
-        }
+
 
         if (ok && nt > 0)
             ok = __all_sync(0xffffffffu, wait_bar(pv_done, (uint32_t)(nt - 1) & 1u, abort_flag, lim));
