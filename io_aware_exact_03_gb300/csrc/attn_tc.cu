@@ -658,8 +658,14 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         const uint32_t p_row = smem_u32(sP + t * C::PT) + (uint32_t)(r >> 3) * 1024u +
                                (uint32_t)(r & 7) * 128u;
 
+        // P_SMEM / F16P: the scores of the next step and the release of the P
+        // buffer are tested early (mbar_test) and the results used later, so
+        // the barrier round trips overlap the softmax; a failed test falls back
+        // to the bounded wait.
+        uint32_t s_pre = 0, pv_pre = 0;
         for (int j = 0; j < nt && ok; ++j) {
-            if (!__all_sync(0xffffffffu, wait_bar(s_full, (uint32_t)j & 1u, abort_flag, lim))) {
+            if (!__all_sync(0xffffffffu, s_pre != 0u) &&
+                !__all_sync(0xffffffffu, wait_bar(s_full, (uint32_t)j & 1u, abort_flag, lim))) {
                 ok = false;
                 break;
             }
@@ -679,6 +685,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 mbar_arrive_1(b_s_free + 8 * t);
+                if (j > 0) pv_pre = mbar_test(pv_done, (uint32_t)(j - 1) & 1u);
             }
             float s[BN];
 #pragma unroll
@@ -737,12 +744,13 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                     pk[x / 2] = (KIND == kBF16) ? pack_bf16(p0, p1) : pack_f16(p0, p1);
                 }
                 if constexpr (C::P_SMEM || C::F16P) {
-                    if (u == 0 && j > 0 &&
+                    if (u == 0 && j > 0 && !__all_sync(0xffffffffu, pv_pre != 0u) &&
                         !__all_sync(0xffffffffu, wait_bar(pv_done, (uint32_t)(j - 1) & 1u,
                                                           abort_flag, lim))) {
                         ok = false;
                         break;
                     }
+                    if (C::F16P && u == 0 && j > 0) tc_fence_after();  // P V_{j-1} has read P_t
                 }
                 if constexpr (C::P_SMEM) {
                     // row r of a 128-byte-swizzled K-major tile: 16-byte unit w
@@ -758,6 +766,9 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                 }
             }
             if (!ok) break;
+            if constexpr (C::P_SMEM || C::F16P) {
+                s_pre = (j + 1 < nt) ? mbar_test(s_full, (uint32_t)(j + 1) & 1u) : 0u;
+            }
             if constexpr (C::P_SMEM) fence_proxy_async_smem();
             const float sum =
                 ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));
@@ -765,8 +776,10 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
 
             if (any && j > 0) {
                 // O_t is touched only to rescale it; it is stable once
-                // P_{j-1} V_{j-1} has completed
-                if (!__all_sync(0xffffffffu, wait_bar(pv_done, (uint32_t)(j - 1) & 1u, abort_flag, lim))) {
+                // P_{j-1} V_{j-1} has completed (P_SMEM / F16P: already
+                // confirmed before the first P store)
+                if (!(C::P_SMEM || C::F16P) &&
+                    !__all_sync(0xffffffffu, wait_bar(pv_done, (uint32_t)(j - 1) & 1u, abort_flag, lim))) {
                     ok = false;
                     break;
                 }
