@@ -587,6 +587,23 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         constexpr int UNITS = C::CB / 16;        // 16-byte units per e4m3 row
         constexpr int PER = BN * UNITS / 32;     // units per lane
         constexpr int BATCH = 8;
+        // Unit idx of the tile -> (row rr, 16-byte unit w of the e4m3 row),
+        // chosen so that the eight lanes of each quarter-warp hit eight
+        // different 16-byte bank groups both when they load (e4m3 swizzle)
+        // and when they store (fp16 swizzle, the two 64-value chunks 16 KB
+        // apart).  d = 128: a quarter takes two adjacent rows, one row's
+        // units in fp16 chunk 0 and the other's in chunk 1.  d = 64: a
+        // quarter takes two adjacent rows, four units each.
+        auto unit_of = [&](int idx, int& rr, int& w) {
+            if constexpr (UNITS == 8) {
+                const int w_lo = idx & 3, half = (idx >> 2) & 1, sel = (idx >> 3) & 1;
+                rr = 2 * (idx >> 4) + half;
+                w = 4 * (half ^ sel) + w_lo;
+            } else {
+                rr = idx / UNITS;
+                w = idx % UNITS;
+            }
+        };
         for (int j = 0; j < n_max; ++j) {
             const int itV = 2 * j + 1;
             const int slot = itV % C::SLOTS;
@@ -598,19 +615,21 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             if (!ok) break;
             const uint32_t src = smem_u32(sKV + (size_t)slot * C::TILE);
             const uint32_t dst = smem_u32(sV16 + (size_t)(j & 1) * C::V16T);
-#pragma unroll
+#pragma unroll 1
             for (int k0 = 0; k0 < PER; k0 += BATCH) {
                 uint32_t x[BATCH][4];
 #pragma unroll
                 for (int k = 0; k < BATCH; ++k) {
-                    const int u = lane + 32 * (k0 + k), rr = u / UNITS, w = u % UNITS;
+                    int rr, w;
+                    unit_of(lane + 32 * (k0 + k), rr, w);
                     // e4m3 row rr: 128-byte swizzle (w ^ rr%8) or 64-byte (w ^ (rr/2)%4)
                     const int wp = (C::CB == 128) ? (w ^ (rr & 7)) : (w ^ ((rr >> 1) & 3));
                     ld_shared_v4(src + (uint32_t)(rr * C::CB + wp * 16), x[k]);
                 }
 #pragma unroll
                 for (int k = 0; k < BATCH; ++k) {
-                    const int u = lane + 32 * (k0 + k), rr = u / UNITS, w = u % UNITS;
+                    int rr, w;
+                    unit_of(lane + 32 * (k0 + k), rr, w);
                     uint32_t hv[8];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
