@@ -259,7 +259,10 @@ ATTN_API size_t attn_fwd_host_workspace_bytes(int B, int H, int N_q, int N_k, in
  * load reserves the array's memory and may synchronise.  Callers that cannot
  * afford either make their first call on each device outside the region where
  * allocation is not allowed (for example at start-up); later calls reserve
- * nothing.  All calls share the one array, so calls whose
+ * nothing.  The looked-up address is kept per device ordinal for the life of
+ * the process: after cudaDeviceReset on a device, do not call this function
+ * on that device again in the same process (the kept address would be
+ * stale).  All calls share the one array, so calls whose
  * work overlaps on the GPU (other streams, other host threads) race: order
  * them on one stream or synchronise between them.  No state carries over from
  * one call to the next that the result depends on. */
