@@ -383,31 +383,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                 reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
                 reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
                 uint32_t pk[32], dk[32];
+                // every column of this step allowed for every key of the warp:
+                // no per-element mask, packed f32x2 arithmetic
+                if (__all_sync(0xffffffffu, key_ok && c_min < 0)) {
 #pragma unroll
-                for (int x = 0; x < 64; x += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4*>(vl + 64 * v + x);
-                    const float4 d4 = *reinterpret_cast<const float4*>(vD + 64 * v + x);
-                    float pv[4], dsv[4];
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                    const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                    for (int x = 0; x < 64; x += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4*>(vl + 64 * v + x);
+                        const float4 d4 = *reinterpret_cast<const float4*>(vD + 64 * v + x);
+                        float pv[4], dsv[4], a[4], tt[4];
+                        ffma2(a[0], a[1], __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]), cl, cl,
+                              -l4.x, -l4.y);
+                        ffma2(a[2], a[3], __uint_as_float(sr[x + 2]), __uint_as_float(sr[x + 3]), cl,
+                              cl, -l4.z, -l4.w);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int col = 64 * v + x + e;
-                        const bool allowed = key_ok && col > c_min;
-                        const float pe = allowed ? ex2(fmaf(__uint_as_float(sr[x + e]), cl, -lv[e])) : 0.f;
-                        pv[e] = pe;
-                        dsv[e] = pe * (__uint_as_float(dr[x + e]) - dv[e]);
+                        for (int e = 0; e < 4; ++e) pv[e] = ex2(a[e]);
+                        fadd2(tt[0], tt[1], __uint_as_float(dr[x]), __uint_as_float(dr[x + 1]),
+                              -d4.x, -d4.y);
+                        fadd2(tt[2], tt[3], __uint_as_float(dr[x + 2]), __uint_as_float(dr[x + 3]),
+                              -d4.z, -d4.w);
+                        ffma2(dsv[0], dsv[1], pv[0], pv[1], tt[0], tt[1], 0.f, 0.f);
+                        ffma2(dsv[2], dsv[3], pv[2], pv[3], tt[2], tt[3], 0.f, 0.f);
+                        if constexpr (KIND == kBF16) {
+                            pk[x / 2] = pack_bf16(pv[0], pv[1]);
+                            pk[x / 2 + 1] = pack_bf16(pv[2], pv[3]);
+                            dk[x / 2] = pack_bf16(dsv[0], dsv[1]);
+                            dk[x / 2 + 1] = pack_bf16(dsv[2], dsv[3]);
+                        } else {
+                            pk[x / 2] = pack_f16(pv[0], pv[1]);
+                            pk[x / 2 + 1] = pack_f16(pv[2], pv[3]);
+                            dk[x / 2] = pack_f16(dsv[0], dsv[1]);
+                            dk[x / 2 + 1] = pack_f16(dsv[2], dsv[3]);
+                        }
                     }
-                    if constexpr (KIND == kBF16) {
-                        pk[x / 2] = pack_bf16(pv[0], pv[1]);
-                        pk[x / 2 + 1] = pack_bf16(pv[2], pv[3]);
-                        dk[x / 2] = pack_bf16(dsv[0], dsv[1]);
-                        dk[x / 2 + 1] = pack_bf16(dsv[2], dsv[3]);
-                    } else {
-                        pk[x / 2] = pack_f16(pv[0], pv[1]);
-                        pk[x / 2 + 1] = pack_f16(pv[2], pv[3]);
-                        dk[x / 2] = pack_f16(dsv[0], dsv[1]);
-                        dk[x / 2 + 1] = pack_f16(dsv[2], dsv[3]);
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 64; x += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4*>(vl + 64 * v + x);
+                        const float4 d4 = *reinterpret_cast<const float4*>(vD + 64 * v + x);
+                        float pv[4], dsv[4];
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int col = 64 * v + x + e;
+                            const bool allowed = key_ok && col > c_min;
+                            const float pe = allowed ? ex2(fmaf(__uint_as_float(sr[x + e]), cl, -lv[e])) : 0.f;
+                            pv[e] = pe;
+                            dsv[e] = pe * (__uint_as_float(dr[x + e]) - dv[e]);
+                        }
+                        if constexpr (KIND == kBF16) {
+                            pk[x / 2] = pack_bf16(pv[0], pv[1]);
+                            pk[x / 2 + 1] = pack_bf16(pv[2], pv[3]);
+                            dk[x / 2] = pack_bf16(dsv[0], dsv[1]);
+                            dk[x / 2 + 1] = pack_bf16(dsv[2], dsv[3]);
+                        } else {
+                            pk[x / 2] = pack_f16(pv[0], pv[1]);
+                            pk[x / 2 + 1] = pack_f16(pv[2], pv[3]);
+                            dk[x / 2] = pack_f16(dsv[0], dsv[1]);
+                            dk[x / 2 + 1] = pack_f16(dsv[2], dsv[3]);
+                        }
                     }
                 }
                 // 64 queries of P^T / dS^T = 32 columns, over columns this
@@ -654,18 +688,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
                 reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
                 uint32_t dk[32];
+                // every key of this step allowed for every row of the warp: no
+                // per-element mask, packed f32x2 arithmetic
+                if (__all_sync(0xffffffffu, row_ok && cl_max >= BN - 1)) {
 #pragma unroll
-                for (int x = 0; x < 64; x += 2) {
-                    float ds[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int col = 64 * v + x + e;
-                        const float pe = (row_ok && col <= cl_max)
-                                             ? ex2(fmaf(__uint_as_float(sr[x + e]), cl, -l2))
-                                             : 0.f;
-                        ds[e] = pe * (__uint_as_float(dr[x + e]) - Dr);
+                    for (int x = 0; x < 64; x += 2) {
+                        float a0, a1, t0, t1, d0, d1;
+                        ffma2(a0, a1, __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]), cl, cl,
+                              -l2, -l2);
+                        const float p0 = ex2(a0), p1 = ex2(a1);
+                        fadd2(t0, t1, __uint_as_float(dr[x]), __uint_as_float(dr[x + 1]), -Dr, -Dr);
+                        ffma2(d0, d1, p0, p1, t0, t1, 0.f, 0.f);
+                        dk[x / 2] = (KIND == kBF16) ? pack_bf16(d0, d1) : pack_f16(d0, d1);
                     }
-                    dk[x / 2] = (KIND == kBF16) ? pack_bf16(ds[0], ds[1]) : pack_f16(ds[0], ds[1]);
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 64; x += 2) {
+                        float ds[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int col = 64 * v + x + e;
+                            const float pe = (row_ok && col <= cl_max)
+                                                 ? ex2(fmaf(__uint_as_float(sr[x + e]), cl, -l2))
+                                                 : 0.f;
+                            ds[e] = pe * (__uint_as_float(dr[x + e]) - Dr);
+                        }
+                        dk[x / 2] = (KIND == kBF16) ? pack_bf16(ds[0], ds[1]) : pack_f16(ds[0], ds[1]);
+                    }
                 }
                 tmem_st32(t_row + kColDP + 32 * v, dk);
                 tmem_st_wait();
