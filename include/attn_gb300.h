@@ -307,6 +307,13 @@ ATTN_API attn_status_t attn_check_status(void* stream);
 /* Static, human-readable name of a status code. */
 ATTN_API const char* attn_status_string(attn_status_t s);
 
+/* Name of the CUDA error (cudaGetErrorName, e.g. "cudaErrorIllegalAddress")
+ * behind the last ATTN_ERR_CUDA returned on the calling host thread, or
+ * "none" if this thread has had none.  Static string; never fails.  After a
+ * device-side fault the CUDA context is unusable and every later call of the
+ * process returns ATTN_ERR_CUDA. */
+ATTN_API const char* attn_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif

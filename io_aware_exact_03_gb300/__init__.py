@@ -38,7 +38,10 @@ _LIB = None
 class AttnError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {attn_status_string(status)} (status {status})")
+        msg = f"{where}: {attn_status_string(status)} (status {status})"
+        if status == ATTN_ERR_CUDA and _LIB is not None:
+            msg += f" [{_LIB.attn_last_cuda_error().decode()}]"
+        super().__init__(msg)
 
 
 def build(force: bool = False) -> str:
@@ -97,6 +100,8 @@ def lib() -> ctypes.CDLL:
         L.attn_check_status.restype = i
         L.attn_status_string.argtypes = [i]
         L.attn_status_string.restype = ctypes.c_char_p
+        L.attn_last_cuda_error.argtypes = []
+        L.attn_last_cuda_error.restype = ctypes.c_char_p
         _LIB = L
     return _LIB
 

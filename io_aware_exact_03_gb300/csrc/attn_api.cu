@@ -31,9 +31,12 @@ attn_status_t validate(const attn::Problem& p) {
     return ATTN_OK;
 }
 
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
 attn_status_t from_cuda(cudaError_t e) {
     if (e == cudaSuccess) return ATTN_OK;
     if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
+    attn::note_cuda_error(e);
     return ATTN_ERR_CUDA;
 }
 
@@ -72,6 +75,10 @@ attn_status_t run_tc(const attn::Problem& p, cudaStream_t s) {
 }
 
 }  // namespace
+
+namespace attn {
+void note_cuda_error(cudaError_t e) { t_last_cuda_error = e; }
+}  // namespace attn
 
 extern "C" {
 
@@ -264,14 +271,22 @@ attn_status_t attn_selftest_abort(const void* q, const void* k, const void* v, v
 attn_status_t attn_check_status(void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return ATTN_ERR_CUDA;
     unsigned a = 0, b = 0, c = 0, g = 0;
-    if (attn::tc_take_status(&a, s) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (attn::tc256_take_status(&c, s) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (attn::simt_take_status(&b, s) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (attn::bwd_take_status(&g, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (e == cudaSuccess) e = attn::tc_take_status(&a, s);
+    if (e == cudaSuccess) e = attn::tc256_take_status(&c, s);
+    if (e == cudaSuccess) e = attn::simt_take_status(&b, s);
+    if (e == cudaSuccess) e = attn::bwd_take_status(&g, s);
+    if (e != cudaSuccess) {
+        attn::note_cuda_error(e);
+        return ATTN_ERR_CUDA;
+    }
     if ((a | b | c | g) & attn::kStatusTimeout) return ATTN_ERR_TIMEOUT;
     return ATTN_OK;
+}
+
+const char* attn_last_cuda_error(void) {
+    const cudaError_t e = t_last_cuda_error;
+    return e == cudaSuccess ? "none" : cudaGetErrorName(e);
 }
 
 const char* attn_status_string(attn_status_t s) {

@@ -124,10 +124,16 @@ attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o
         return ATTN_ERR_INVALID_ARG;
 
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    const cudaError_t eg = cudaGetDevice(&dev);
+    if (eg != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        attn::note_cuda_error(eg != cudaSuccess ? eg : cudaErrorInvalidDevice);
+        return ATTN_ERR_CUDA;
+    }
     Pipes& P = g_pipes[dev];
     std::lock_guard<std::mutex> lock(P.mu);
-    if (init_pipes(P) != cudaSuccess) {
+    const cudaError_t ei = init_pipes(P);
+    if (ei != cudaSuccess) {
+        attn::note_cuda_error(ei);
         (void)cudaGetLastError();
         return ATTN_ERR_CUDA;
     }
@@ -204,6 +210,7 @@ attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o
     if (ej == cudaSuccess) ej = cudaEventRecord(P.start, P.in);
     if (ej == cudaSuccess) ej = cudaStreamWaitEvent(us, P.start, 0);
     if (e != cudaSuccess || ej != cudaSuccess) {
+        attn::note_cuda_error(e != cudaSuccess ? e : ej);
         (void)cudaGetLastError();
         return ATTN_ERR_CUDA;
     }

@@ -81,6 +81,10 @@ cudaError_t launch_quantize_e4m3(const void* x, int dtype, const float* signs, v
 // Bounded-wait health check (attn_tc.cu).
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream);
 
+// Remembers, per host thread, the CUDA error behind the last ATTN_ERR_CUDA
+// (read back by attn_last_cuda_error).
+void note_cuda_error(cudaError_t e);
+
 // Split-KV on the tensor-core kernel plus the combine kernel (attn_tc.cu).
 constexpr int kMaxSplits = 32;
 size_t splitkv_workspace_bytes(long long B, long long H, long long N_q, int d, int n_splits);

@@ -33,11 +33,17 @@ void* g_scratch_ptr[kMaxDevices] = {};
 // Device address of the scratch array on the current device (nullptr on error).
 void* scratch_for_current_device() {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    const cudaError_t eg = cudaGetDevice(&dev);
+    if (eg != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        attn::note_cuda_error(eg != cudaSuccess ? eg : cudaErrorInvalidDevice);
+        return nullptr;
+    }
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
     if (!g_scratch_ptr[dev]) {
         void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_splitkv_scratch) != cudaSuccess || !ptr) {
+        const cudaError_t es = cudaGetSymbolAddress(&ptr, g_splitkv_scratch);
+        if (es != cudaSuccess || !ptr) {
+            attn::note_cuda_error(es != cudaSuccess ? es : cudaErrorInvalidSymbol);
             (void)cudaGetLastError();
             return nullptr;
         }

@@ -47,13 +47,23 @@ __device__ unsigned g_tc256_status = 0;
 constexpr int D = 256;
 constexpr int BM = 128;        // query rows per tile (MMA M)
 constexpr int BN = 128;        // keys per tile
-constexpr int kThreads = 192;  // producer, MMA issuer, 4 softmax warps
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSmemLimit = 232448;
 
 template <int KIND>
 struct Cfg256 {
     static constexpr int E = (KIND == kE4M3) ? 1 : 2;   // bytes per element
+    // e4m3 inputs: P goes to the P V product as fp16 (as in the d <= 128
+    // kernel: an e4m3 P keeps 3 mantissa bits, too few for a weight that is a
+    // sizeable share of its row), and V is widened from e4m3 to fp16 in
+    // shared memory by a converter warp (exact), whole key tiles, double
+    // buffered.
+    static constexpr bool F16P = (KIND == kE4M3);
+    // producer, MMA issuer, 4 softmax warps (+ 2 V converters for F16P; with
+    // eight warps every warp may hold up to 255 registers)
+    static constexpr int CONV_WARP0 = 6;
+    static constexpr int CONV_WARPS = F16P ? 2 : 0;
+    static constexpr int THREADS = 32 * (6 + CONV_WARPS);
     static constexpr int CB = 128;                       // bytes per swizzle chunk row
     static constexpr int CE = CB / E;                    // elements per chunk
     static constexpr int NC = D * E / CB;                // chunks per row: 4 (16-bit), 2 (e4m3)
@@ -62,25 +72,31 @@ struct Cfg256 {
     static constexpr int KCH = NC / 2;                   // d-chunks per K item
     static constexpr int KCHUNK = BN * CB;               // one K d-chunk: 128 keys x 128 B
     static constexpr int VCHUNK = (BN / 2) * CB;         // one V d-chunk: 64 keys x 128 B
-    // q_full, s_full x2, p_full x2, pv_done, drain, o_done
-    static constexpr int NB_FIXED = 1 + 2 + 2 + 1 + 1 + 1;
-    static constexpr int SLOTS_FIT = (kSmemLimit - 1024 - QTILE - 512) / ITEM;
+    // fp16 copy of one V half (64 keys x 256 values): four 64-value chunks of
+    // 64 keys x 128 B, the layout of a 16-bit V item; one key tile = 2 halves
+    static constexpr int V16_HALF = (BN / 2) * D * 2;
+    static constexpr int V16_VCHUNK = (BN / 2) * 128;
+    static constexpr int V16T = F16P ? 2 * V16_HALF : 0;
+    // q_full, s_full x2, p_full x2, pv_done, drain, o_done, v16_full x2, v16_empty x2
+    static constexpr int NB_FIXED = 1 + 2 + 2 + 1 + 1 + 1 + 4;
+    static constexpr int SLOTS_FIT = (kSmemLimit - 1024 - QTILE - 2 * V16T - 512) / ITEM;
     static constexpr int SLOTS = SLOTS_FIT > 12 ? 12 : SLOTS_FIT;
     static constexpr int NB = NB_FIXED + 2 * SLOTS;
-    static constexpr size_t SMEM = 1024 + (size_t)QTILE + (size_t)SLOTS * ITEM + NB * 8 + 16;
-    static constexpr int MMA_K = 32 / E;                 // K per MMA instruction
+    static constexpr size_t SMEM =
+        1024 + (size_t)QTILE + 2 * (size_t)V16T + (size_t)SLOTS * ITEM + NB * 8 + 16;
+    static constexpr int MMA_K = 32 / E;                 // K per Q K^T MMA instruction
+    static constexpr int PV_K = F16P ? 16 : MMA_K;       // keys per P V MMA instruction
+    static constexpr int PE = F16P ? 2 : E;              // bytes per P element
     static constexpr uint32_t FMT = (KIND == kBF16) ? 1u : 0u;
     static constexpr uint32_t IDESC_QK = instr_desc(FMT, FMT, 0, 0, BM, BN);
-    static constexpr uint32_t IDESC_PV = instr_desc(FMT, FMT, 0, 1, BM, D);
-    static constexpr uint32_t P_COLS = BN * E / 4;       // TMEM columns holding P
-    // Rescale rules as in the d = 64 / 128 kernel: the running output is
-    // rescaled when the row maximum grew by more than 2^8, and for e4m3 also
-    // when the tile's largest weight exceeds 1/8 of the row mass so far (an
-    // e4m3 weight above 1 carries up to 2^-4 relative rounding that the fp32
-    // row sum does not see).
+    static constexpr uint32_t IDESC_PV =
+        instr_desc(F16P ? 0u : FMT, F16P ? 0u : FMT, 0, 1, BM, D);
+    static constexpr uint32_t P_COLS = BN * PE / 4;      // TMEM columns holding P
+    // Rescale rule as in the d = 64 / 128 kernel: the running output is
+    // rescaled when the row maximum grew by more than 2^8 (P stays <= 256).
     static constexpr float RESCALE_THRESHOLD = 8.0f;
-    static constexpr float RESCALE_MASS = 0.125f;
     static_assert(SLOTS >= 4, "ring depth");
+    static_assert(!F16P || SLOTS % 4 == 0, "F16P: K and V items keep to their own slots");
     static_assert(SMEM <= (size_t)kSmemLimit, "shared memory budget");
 };
 
@@ -126,11 +142,24 @@ __device__ __forceinline__ int kv_tiles_for(int q0, const Tc256Params& p) {
     return last_key < 0 ? 0 : last_key / BN + 1;
 }
 
-// Ring items in first-use order: group 0 = K_0, group 1 = K_1 (if any), then
-// for j = 0..n-1: V_j, K_{j+2} (if any).  Each group is two items (halves).
-// Returns false past the end; *is_v and *tile say what group g is.
+// Ring items in load order, each group two items (halves); returns false past
+// the end, *is_v and *tile say what group g is.
+//  16-bit kinds: K_0, K_1 (if any), then for j = 0..n-1: V_j, K_{j+2} (if any):
+//   the MMA thread consumes every item, so slots may alternate freely between
+//   K and V.
+//  F16P (ALT): K_0, V_0, K_1, V_1, ...: with the ring a multiple of four items
+//   a slot only ever holds K (read by the MMA thread) or only V (read by the
+//   converter), so each slot's barriers have one waiter that sees every phase
+//   (a parity wait is only sound for a waiter at most one phase behind).
+template <bool ALT>
 __device__ __forceinline__ bool group_of(int g, int n, bool* is_v, int* tile) {
     if (n <= 0) return false;
+    if (ALT) {
+        if (g >= 2 * n) return false;
+        *is_v = (g & 1) != 0;
+        *tile = g >> 1;
+        return true;
+    }
     const int nk0 = n > 1 ? 2 : 1;  // leading K groups
     if (g < nk0) {
         *is_v = false;
@@ -153,7 +182,7 @@ __device__ __forceinline__ bool group_of(int g, int n, bool* is_v, int* tile) {
 }
 
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg256<KIND>::THREADS, 1)
     attn_tc256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const Tc256Params p) {
     using C = Cfg256<KIND>;
@@ -161,7 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sQ = smem;
-    uint8_t* sKV = smem + C::QTILE;  // SLOTS items
+    uint8_t* sV16 = smem + C::QTILE;          // two fp16 V tiles (F16P only)
+    uint8_t* sKV = sV16 + 2 * C::V16T;        // SLOTS items
     uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + (size_t)C::SLOTS * C::ITEM);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NB);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -178,6 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t b_pv_done = smem_u32(bars + 5);
     const uint32_t b_drain = smem_u32(bars + 6);
     const uint32_t b_o_done = smem_u32(bars + 7);
+    const uint32_t b_v16_full = smem_u32(bars + 8);   // + 8 * buffer (F16P)
+    const uint32_t b_v16_empty = smem_u32(bars + 10); // + 8 * buffer (F16P)
     const uint32_t b_kv_full = smem_u32(bars + C::NB_FIXED);               // + 8 * slot
     const uint32_t b_kv_empty = smem_u32(bars + C::NB_FIXED + C::SLOTS);   // + 8 * slot
 
@@ -224,6 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(b_pv_done, 1);
         mbar_init(b_drain, 1);
         mbar_init(b_o_done, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(b_v16_full + 8 * t, 2);    // the two converter warps
+            mbar_init(b_v16_empty + 8 * t, 1);   // the P V MMAs of the tile
+        }
         for (int s = 0; s < C::SLOTS; ++s) {
             mbar_init(b_kv_full + 8 * s, 1);
             mbar_init(b_kv_empty + 8 * s, 1);
@@ -258,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             bool is_v;
             int t_kv;
-            for (int grp = 0; ok && group_of(grp, n, &is_v, &t_kv); ++grp) {
+            for (int grp = 0; ok && group_of<C::F16P>(grp, n, &is_v, &t_kv); ++grp) {
                 const int key0 = (j0 + t_kv) * BN;
                 for (int half = 0; half < 2; ++half, ++it) {
                     if (it >= p.items_limit) {
@@ -323,20 +359,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // O += P_{buf} V from the two V items at ring positions it, it + 1
             auto issue_pv = [&](int buf, int it, bool first) {
+                if constexpr (C::F16P) {
+                    // B = the fp16 copy of V_j in buffer `it` (here the buffer index)
 #pragma unroll
-                for (int ks = 0; ks < BN / C::MMA_K; ++ks) {
-                    const int key = ks * C::MMA_K;
-                    const int item = it + key / (BN / 2);
-                    // V is MN-major: 8-key groups 8*CB apart, d-chunks VCHUNK apart
-                    const uint64_t vd = smem_desc(
-                        smem_u32(sKV + (size_t)slot_of(item) * C::ITEM + (key % (BN / 2)) * C::CB),
-                        C::VCHUNK, 8 * C::CB, 2u);
-                    const uint32_t a_tmem = tmem + 128u * buf + ks * (C::MMA_K * C::E / 4);
-                    const uint32_t acc = (!first || ks > 0) ? 1u : 0u;
-                    if constexpr (KIND == kE4M3)
-                        mma_f8_ts_1(tmem + kColO, a_tmem, vd, C::IDESC_PV, acc);
-                    else
+                    for (int ks = 0; ks < BN / C::PV_K; ++ks) {
+                        const int key = ks * C::PV_K;
+                        const uint64_t vd = smem_desc(
+                            smem_u32(sV16 + (size_t)it * C::V16T + (key / (BN / 2)) * C::V16_HALF +
+                                     (key % (BN / 2)) * 128),
+                            C::V16_VCHUNK, 8 * 128, 2u);
+                        const uint32_t a_tmem = tmem + 128u * buf + ks * (C::PV_K * 2 / 4);
+                        const uint32_t acc = (!first || ks > 0) ? 1u : 0u;
                         mma_f16_ts_1(tmem + kColO, a_tmem, vd, C::IDESC_PV, acc);
+                    }
+                } else {
+#pragma unroll
+                    for (int ks = 0; ks < BN / C::MMA_K; ++ks) {
+                        const int key = ks * C::MMA_K;
+                        const int item = it + key / (BN / 2);
+                        // V is MN-major: 8-key groups 8*CB apart, d-chunks VCHUNK apart
+                        const uint64_t vd = smem_desc(
+                            smem_u32(sKV + (size_t)slot_of(item) * C::ITEM + (key % (BN / 2)) * C::CB),
+                            C::VCHUNK, 8 * C::CB, 2u);
+                        const uint32_t a_tmem = tmem + 128u * buf + ks * (C::MMA_K * C::E / 4);
+                        const uint32_t acc = (!first || ks > 0) ? 1u : 0u;
+                        if constexpr (KIND == kE4M3)
+                            mma_f8_ts_1(tmem + kColO, a_tmem, vd, C::IDESC_PV, acc);
+                        else
+                            mma_f16_ts_1(tmem + kColO, a_tmem, vd, C::IDESC_PV, acc);
+                    }
                 }
             };
             auto wait_items = [&](int it) {
@@ -348,38 +399,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit_1(b_kv_empty + 8 * slot_of(it + 1));
             };
 
+            // ring position of the next group (16-bit kinds); F16P: K_t sits at
+            // positions 4t, 4t + 1
             int it = 0;
             bool ok = wb(b_q_full, 0);
             // scores of K_0 and K_1 into S_0 and S_1
             for (int t = 0; t < 2 && t < n && ok; ++t) {
-                ok = wait_items(it);
+                const int pos = C::F16P ? 4 * t : it;
+                ok = wait_items(pos);
                 if (!ok) break;
                 tc_fence_after();
-                issue_qk(t, it);
+                issue_qk(t, pos);
                 mma_commit_1(b_s_full + 8 * t);
-                release_items(it);
+                release_items(pos);
                 it += 2;
             }
             // per key tile j: O += P_j V_j, then the scores of K_{j+2} into the
             // buffer P_j was read from (the same thread's MMAs run in order)
             for (int j = 0; j < n && ok; ++j) {
                 const int buf = j & 1;
-                ok = wait_items(it);
+                // F16P: the V items go to the converter; P V reads its fp16 copy
+                ok = C::F16P ? wb(b_v16_full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u) : wait_items(it);
                 if (ok) ok = wb(b_p_full + 8 * buf, (uint32_t)(j >> 1) & 1u);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(buf, it, j == 0);
+                issue_pv(buf, C::F16P ? (j & 1) : it, j == 0);
                 mma_commit_1(b_pv_done);
                 if (j + 1 == n) mma_commit_1(b_o_done);
-                release_items(it);
+                if constexpr (C::F16P)
+                    mma_commit_1(b_v16_empty + 8 * (j & 1));
+                else
+                    release_items(it);
                 it += 2;
                 if (j + 2 < n) {
-                    ok = wait_items(it);
+                    const int pos = C::F16P ? 4 * (j + 2) : it;
+                    ok = wait_items(pos);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_qk(buf, it);
+                    issue_qk(buf, pos);
                     mma_commit_1(b_s_full + 8 * buf);
-                    release_items(it);
+                    release_items(pos);
                     it += 2;
                 }
             }
@@ -389,6 +448,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+    } else if (C::F16P && warp >= C::CONV_WARP0) {
+        // ------------------------------------------ V converters (F16P only)
+        // Two warps widen each V tile (ring positions 4j + 2, 4j + 3: two
+        // half items) into fp16 buffer j % 2, laid out like a 16-bit V item.
+        // Warp c takes half item c (64 keys x 256 values): it loads its 16 KB
+        // into registers, frees the ring slot at once (so the next V tile's
+        // load overlaps this conversion), then waits for the fp16 buffer and
+        // writes it.
+        // Lane-to-unit mapping: the eight lanes of a quarter-warp take two
+        // adjacent rows whose units go to different fp16 chunks, so both the
+        // e4m3 loads and the fp16 stores hit eight different bank groups.
+        const int hh = warp - C::CONV_WARP0;
+        constexpr int PER = (BN / 2) * (D / 16) / 32;  // 16-byte units per lane: 32
+        for (int jv = 0; jv < n; ++jv) {
+            const int it = 4 * jv + 2 + hh;
+            bool ok = __all_sync(0xffffffffu, wait_bar(b_kv_full + 8 * slot_of(it), par_of(it), abort_flag, lim));
+            if (!ok) break;
+            const uint32_t src = smem_u32(sKV + (size_t)slot_of(it) * C::ITEM);
+            uint32_t x[PER][4];
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                // unit lane + 32 k: e4m3 d-chunk k / 16 (values 128 (k / 16) .. +127)
+                const int cc = k >> 4, i2 = (lane + 32 * k) & 511;
+                const int w_lo = i2 & 3, half = (i2 >> 2) & 1, sel = (i2 >> 3) & 1;
+                const int rr = 2 * (i2 >> 4) + half, w = 4 * (half ^ sel) + w_lo;
+                ld_shared_v4(src + (uint32_t)(cc * C::VCHUNK + rr * 128 + ((w ^ (rr & 7)) << 4)), x[k]);
+            }
+            // the loads are complete once their values are used; the release
+            // below orders them before the producer's next TMA into the slot
+            uint32_t keep = 0;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) keep |= x[k][0] | x[k][1] | x[k][2] | x[k][3];
+            asm volatile("" ::"r"(keep));
+            __syncwarp();
+            mbar_arrive_1(b_kv_empty + 8 * slot_of(it));
+            ok = __all_sync(0xffffffffu, wait_bar(b_v16_empty + 8 * (jv & 1),
+                                                  ((uint32_t)(jv >> 1) & 1u) ^ 1u, abort_flag, lim));
+            if (!ok) break;
+            const uint32_t dst = smem_u32(sV16 + (size_t)(jv & 1) * C::V16T + hh * C::V16_HALF);
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int cc = k >> 4, i2 = (lane + 32 * k) & 511;
+                const int w_lo = i2 & 3, half = (i2 >> 2) & 1, sel = (i2 >> 3) & 1;
+                const int rr = 2 * (i2 >> 4) + half, w = 4 * (half ^ sel) + w_lo;
+                uint32_t hv[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    hv[2 * e] = e4m3x2_to_f16x2((uint16_t)(x[k][e] & 0xffffu));
+                    hv[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(x[k][e] >> 16));
+                }
+                // values d = 128 cc + 16 w .. +15: fp16 chunk 2 cc + w / 4, units 2 (w % 4), +1
+                const uint32_t row = dst + (uint32_t)((2 * cc + (w >> 2)) * C::V16_VCHUNK + rr * 128);
+                const int u0 = 2 * (w & 3);
+                st_shared_v4(row + (uint32_t)((u0 ^ (rr & 7)) << 4), hv[0], hv[1], hv[2], hv[3]);
+                st_shared_v4(row + (uint32_t)(((u0 + 1) ^ (rr & 7)) << 4), hv[4], hv[5], hv[6], hv[7]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            mbar_arrive_1(b_v16_full + 8 * (jv & 1));
+        }
     } else {
         // --------------------------------------- softmax + epilogue (128 thr)
         const int quad = warp & 3;  // TMEM lane quadrant this warp may access
@@ -448,9 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float mx = max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]),
                                   fmaxf(mc[6], mc[7]));
             const float m_new = mx * c;
-            bool need = m_new > m_used + C::RESCALE_THRESHOLD;
-            if (KIND == kE4M3)
-                need = need || (m_new > m_used && ex2(m_new - m_used) > l * C::RESCALE_MASS);
+            const bool need = m_new > m_used + C::RESCALE_THRESHOLD;
             const bool any = __any_sync(0xffffffffu, need);
             float alpha = 1.f;
             if (any) {
@@ -462,34 +579,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             float sc[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) sc[k] = 0.f;
-            constexpr int PER_CHUNK = 32 * 4 / C::E;  // score columns per 32 TMEM columns
+            constexpr int PER_CHUNK = 32 * 4 / C::PE;  // score columns per 32 TMEM columns
 #pragma unroll
             for (int u = 0; u < (int)C::P_COLS / 32; ++u) {
                 uint32_t pk[32];
-                if constexpr (KIND == kE4M3) {
 #pragma unroll
-                    for (int x = 0; x < PER_CHUNK; x += 4) {
-                        const int y = u * PER_CHUNK + x;
-                        float a0, a1, a2, a3;
-                        ffma2(a0, a1, s[y], s[y + 1], c, c, -m_ref, -m_ref);
-                        ffma2(a2, a3, s[y + 2], s[y + 3], c, c, -m_ref, -m_ref);
-                        const float p0 = ex2(a0), p1 = ex2(a1), p2 = ex2(a2), p3 = ex2(a3);
-                        const int k = ((x / 4) & 3) * 2;
-                        fadd2(sc[k], sc[k + 1], sc[k], sc[k + 1], p0, p1);
-                        fadd2(sc[k], sc[k + 1], sc[k], sc[k + 1], p2, p3);
-                        pk[x / 4] = pack_e4m3(p0, p1, p2, p3);
-                    }
-                } else {
-#pragma unroll
-                    for (int x = 0; x < PER_CHUNK; x += 2) {
-                        const int y = u * PER_CHUNK + x;
-                        float a0, a1;
-                        ffma2(a0, a1, s[y], s[y + 1], c, c, -m_ref, -m_ref);
-                        const float p0 = ex2(a0), p1 = ex2(a1);
-                        const int k = ((x / 2) & 3) * 2;
-                        fadd2(sc[k], sc[k + 1], sc[k], sc[k + 1], p0, p1);
-                        pk[x / 2] = (KIND == kBF16) ? pack_bf16(p0, p1) : pack_f16(p0, p1);
-                    }
+                for (int x = 0; x < PER_CHUNK; x += 2) {
+                    const int y = u * PER_CHUNK + x;
+                    float a0, a1;
+                    ffma2(a0, a1, s[y], s[y + 1], c, c, -m_ref, -m_ref);
+                    const float p0 = ex2(a0), p1 = ex2(a1);
+                    const int k = ((x / 2) & 3) * 2;
+                    fadd2(sc[k], sc[k + 1], sc[k], sc[k + 1], p0, p1);
+                    pk[x / 2] = (KIND == kBF16) ? pack_bf16(p0, p1) : pack_f16(p0, p1);
                 }
                 tmem_st32(t_row + 128u * buf + 32 * u, pk);
             }
@@ -642,7 +744,7 @@ cudaError_t launch_k(const Problem& pr, cudaStream_t stream, int n_splits, float
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)n_cta, (unsigned)n_splits);
-    attn_tc256_kernel<KIND><<<grid, kThreads, C::SMEM, stream>>>(mq, mk, mv, p);
+    attn_tc256_kernel<KIND><<<grid, C::THREADS, C::SMEM, stream>>>(mq, mk, mv, p);
     return cudaGetLastError();
 }
 

@@ -380,14 +380,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x) {
     return r;
 }
 
-// Four fp32 -> packed e4m3x4 (round to nearest even, saturating); x0 goes to
-// the lowest byte.
-__device__ __forceinline__ uint32_t pack_e4m3(float x0, float x1, float x2, float x3) {
-    uint16_t lo, hi;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(x1), "f"(x0));
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(x3), "f"(x2));
-    return (uint32_t)lo | ((uint32_t)hi << 16);
-}
 
 }  // namespace ptx
 }  // namespace attn

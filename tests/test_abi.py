@@ -57,6 +57,14 @@ def test_status_strings(L):
     assert L.attn_status_string(99) == b"unknown status"
 
 
+def test_last_cuda_error_names_a_cuda_error(L):
+    # "none" until a call returns ATTN_ERR_CUDA on this thread, then the
+    # cudaGetErrorName of its cause (calls made without a GPU can set it)
+    L.attn_last_cuda_error.restype = ctypes.c_char_p
+    name = L.attn_last_cuda_error()
+    assert name == b"none" or name.startswith(b"cuda"), name
+
+
 P = 0x10000  # a 16-byte aligned fake address; never dereferenced by these calls
 
 
