@@ -234,16 +234,17 @@ def test_gqa_matches_oracle(shape):
     compare(case, O, lse, O_ref, lse_ref)
 
 
-def test_c5_every_row_within_the_fp8_tolerance():
-    """C5 (B2 H16 N8192 d128, e4m3 with 0.1 % x10 outliers) against the fp64
-    oracle at the stated FP8 bound (O max abs error <= 6e-2 beyond the bf16
-    output's own rounding, lse <= 1e-3) on 4096 seeded rows plus the 256 rows
-    where the tensor-core kernel and the CUDA-core kernel (fp32 scores, fp32
-    P) differ most, out of all 262 144.  Over every row the two kernels agree
-    within 1e-2 beyond one bf16 ulp (each output is rounded on its own), and
-    the CUDA-core kernel is within 1e-3 (plus its rounding) of the oracle on
-    the checked rows."""
-    case = synthetic.CASES["C5"]
+@pytest.mark.parametrize("name", ["C5", "D256F"])
+def test_fp8_every_row_within_the_fp8_tolerance(name):
+    """C5 (B2 H16 N8192 d128) and D256F (B2 H8 N8192 d256), e4m3 with 0.1 %
+    x10 outliers, against the fp64 oracle at the stated FP8 bound (O max abs
+    error <= 6e-2 beyond the bf16 output's own rounding, lse <= 1e-3) on 4096
+    seeded rows plus the 256 rows where the tensor-core kernel and the
+    CUDA-core kernel (fp32 scores, fp32 P) differ most, out of all rows.  Over
+    every row the two kernels agree within 1e-2 beyond one bf16 ulp (each
+    output is rounded on its own), and the CUDA-core kernel is within 1e-3
+    (plus its rounding) of the oracle on the checked rows."""
+    case = synthetic.CASES.get(name) or synthetic.EXTRA_CASES[name]
     inputs = synthetic.make_inputs(case)
     dev = to_device(inputs)
     o1, l1 = attn.attn_fwd_fp8(dev["q"], dev["k"], dev["v"], dev["q_descale"], dev["k_descale"],
