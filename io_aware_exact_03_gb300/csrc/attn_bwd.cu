@@ -27,7 +27,8 @@
 //   * bwd_dq: one CTA per 128-row query tile.  Per key tile: S = Q K^T and
 //     dP = dO V^T, one thread per query row forms dS, then dQ += dS K.
 // Every output element is written by one CTA: no atomics, deterministic.
-// Warps: 0 TMA producer, 1 MMA issuer (TMEM owner), 2-5 elementwise.  Every
+// Warps: 0 TMA producer, 1 MMA issuer (TMEM owner), 2-5 elementwise (bwd_dkdv:
+// 2-5 and 6-9, one group per half of each query tile's queries).  Every
 // mbarrier wait is bounded; on expiry the CTA drains, frees TMEM and exits
 // with the status word set.
 #include <cuda.h>
@@ -49,7 +50,8 @@ __device__ unsigned g_bwd_status = 0;
 
 constexpr int BM = 128;        // query rows per tile
 constexpr int BN = 128;        // keys per tile
-constexpr int kThreads = 192;  // producer, MMA issuer, 4 elementwise warps
+constexpr int kThreads = 192;    // bwd_dq: producer, MMA issuer, 4 elementwise warps
+constexpr int kThreadsKV = 320;  // bwd_dkdv: producer, MMA issuer, 2 x 4 elementwise warps
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSmemLimit = 232448;
 
@@ -186,15 +188,17 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const void* o, const void
 
 // ---------------------------------------------------------------- dK, dV
 template <int D, int KIND>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsKV, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                     const BwdParams p) {
     using C = BCfg<D, KIND>;
     constexpr int SLOTS = C::SLOTS_KV;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned by offsetting the shared array itself, so that every
+    // pointer derived from it stays in the shared address space (plain loads
+    // through it compile to shared-memory loads, not generic ones)
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* sK = smem;
     uint8_t* sV = smem + C::TILE;
     uint8_t* sRing = smem + 2 * C::TILE;
@@ -332,10 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int ks = half * (BM / C::MMA_K / 2) + kh;
                         const uint32_t o16 = (uint32_t)(ks * C::MMA_K * C::CB) >> 4;
                         const uint32_t acc = (s > 0 || ks > 0) ? 1u : 0u;
-                        mma_f16_ts_1(tmem + kColAcc, tmem + kColS + ks * (C::MMA_K / 2), gmn + o16,
-                                   C::IDESC_ACC, acc);
-                        mma_f16_ts_1(tmem + kColAcc + D, tmem + kColDP + ks * (C::MMA_K / 2), qmn + o16,
-                                   C::IDESC_ACC, acc);
+                        // P^T / dS^T of query half h: the first 32 of its own 64 columns
+                        const uint32_t pcol = 64u * half + kh * (C::MMA_K / 2);
+                        mma_f16_ts_1(tmem + kColAcc, tmem + kColS + pcol, gmn + o16, C::IDESC_ACC, acc);
+                        mma_f16_ts_1(tmem + kColAcc + D, tmem + kColDP + pcol, qmn + o16, C::IDESC_ACC,
+                                     acc);
                     }
                 }
                 if (!ok) break;
@@ -350,8 +355,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ---------------------------------------- elementwise: one key row per thread
+        // ------------------------ elementwise: one key row per thread, two groups
+        // Warps 2-5 take the step's queries [0, 64), warps 6-9 queries [64,
+        // 128), side by side (two warps per sub-partition hide each other's
+        // TMEM and exp latencies); each writes its P^T / dS^T over the first 32
+        // of its own 64 columns, which only it has read.
         const int quad = warp & 3;
+        const int hq = (warp - 2) >> 2;  // query half of this warp group
         const int r = quad * 32 + lane;
         const int kk = key0 + r;                 // this thread's key
         const bool key_ok = kk < p.N_k;
@@ -370,8 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // query column c is allowed for this key iff kk <= q0 + c + shift,
             // i.e. c > kk - shift - q0 - 1
             const int c_min = p.causal ? kk - shift - q0 - 1 : -1;
-#pragma unroll
-            for (int v = 0; v < 2; ++v) {
+            {
+                const int v = hq;
                 uint32_t sr[64], dr[64];
                 tmem_ld32(t_row + kColS + 64 * v, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
                 tmem_ld32(t_row + kColS + 64 * v + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
@@ -385,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t pk[32], dk[32];
                 // every column of this step allowed for every key of the warp:
                 // no per-element mask, packed f32x2 arithmetic
-                if (__all_sync(0xffffffffu, key_ok && c_min < 0)) {
+                if (__all_sync(0xffffffffu, key_ok && c_min < 64 * v)) {
 #pragma unroll
                     for (int x = 0; x < 64; x += 4) {
                         const float4 l4 = *reinterpret_cast<const float4*>(vl + 64 * v + x);
@@ -446,19 +456,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // 64 queries of P^T / dS^T = 32 columns, over columns this
                 // thread has already read; then this half may be consumed
-                tmem_st32(t_row + kColS + 32 * v, pk);
-                tmem_st32(t_row + kColDP + 32 * v, dk);
+                tmem_st32(t_row + kColS + 64 * v, pk);
+                tmem_st32(t_row + kColDP + 64 * v, dk);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(v ? b_p_half1 : b_p_half0);
             }
         }
-        // ---- epilogue: dV and scale * dK for this key row
+        // ---- epilogue: dV (warps 2-5) and scale * dK (warps 6-9) for this key row
         if (ok && n_steps > 0)
             ok = __all_sync(0xffffffffu, wait_bar(b_acc_done, 0u, abort_flag, lim));
         if (ok) {
             tc_fence_after();
-            for (int which = 0; which < 2; ++which) {
+            {
+                const int which = hq;
                 uint16_t* dst = reinterpret_cast<uint16_t*>(which == 0 ? p.out_a : p.out_b) +
                                 (((size_t)b * p.N_k + (key_ok ? kk : 0)) * p.H_kv + hk) * D;
                 const float mul = which == 0 ? 1.f : p.scale;
@@ -507,8 +518,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = BCfg<D, KIND>;
     constexpr int SLOTS = C::SLOTS_Q;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned by offsetting the shared array itself, so that every
+    // pointer derived from it stays in the shared address space (plain loads
+    // through it compile to shared-memory loads, not generic ones)
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* sQ = smem;
     uint8_t* sG = smem + C::TILE;
     uint8_t* sRing = smem + 2 * C::TILE;
@@ -824,7 +837,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
         e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)C::SMEM_KV);
         if (e != cudaSuccess) return e;
-        bwd_dkdv_kernel<D, KIND><<<(unsigned)n_cta, kThreads, C::SMEM_KV, stream>>>(mq, mk, mv, mg, p);
+        bwd_dkdv_kernel<D, KIND><<<(unsigned)n_cta, kThreadsKV, C::SMEM_KV, stream>>>(mq, mk, mv, mg, p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
