@@ -268,14 +268,14 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         mbar_init(b_drain, 1);
         mbar_init(b_drain_b, 1);
         for (int t = 0; t < 2; ++t) {
-            mbar_init(b_v16_full + 8 * t, 1);    // the converter warp
+            mbar_init(b_v16_full + 8 * t, 4);    // converter, producer and both issuers
             mbar_init(b_v16_empty + 8 * t, 2);   // one release per tile's issuer
         }
         for (int s = 0; s < C::SLOTS; ++s) {
             mbar_init(b_kv_full + 8 * s, 1);
             // one release per issuer that reads the ring; F16P: V items (odd
             // slots) are read only by the converter
-            mbar_init(b_kv_empty + 8 * s, (C::F16P && (s & 1)) ? 1 : C::ISSUERS);
+            mbar_init(b_kv_empty + 8 * s, (C::F16P && (s & 1)) ? 4 : C::ISSUERS);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -295,39 +295,235 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
+    // F16P: V_j's e4m3 tile (ring item 2j + 1) widened into fp16 buffer j % 2,
+    // laid out as a 16-bit V tile loaded by TMA would be (128-byte rows of 64
+    // values, 128-byte swizzle; every e4m3 value is exact in fp16).  The work
+    // is shared out by 16-byte units between the converter warp, the producer
+    // warp and each MMA issuer (right after issuing its P V of the step
+    // before), so that the fp16 stores are spread over the four SM
+    // sub-partitions instead of loading one: from one warp they went through
+    // its sub-partition's shared-memory / special-function issue path beside
+    // two softmax warps and cost ~17 % of C5's time.
+    constexpr int V_UNITS = C::CB / 16;       // 16-byte units per e4m3 row
+    constexpr int V_PER = BN * V_UNITS / 32;  // units per lane, whole tile
+    // shares, in units per lane: converter warp [0, V_CONV), producer warp
+    // [V_PROD0, +V_PROD), issuer t [V_ISS0 + t V_ISS, +V_ISS).  Measured on
+    // C5 (ms per call): all on the converter 0.635; converter 1/2 + issuers
+    // 1/4 each 0.605; a quarter each 0.616; issuers 1/2 each 0.734; converter
+    // 1/2, producer 1/4, issuers 1/8 each 0.581 (kept: the issuers' MMA issue
+    // tolerates little extra work).
+    constexpr int V_CONV = V_PER / 2, V_PROD = V_PER / 4, V_ISS = V_PER / 8;
+    constexpr int V_PROD0 = V_CONV, V_ISS0 = V_CONV + V_PROD;
+    static_assert(V_CONV + V_PROD + 2 * V_ISS == V_PER, "the shares cover every unit");
+    // Unit idx of the tile -> (row rr, 16-byte unit w of the e4m3 row),
+    // chosen so that the eight lanes of each quarter-warp hit eight different
+    // 16-byte bank groups both when they load (e4m3 swizzle) and when they
+    // store (fp16 swizzle, the two 64-value chunks 16 KB apart).  d = 128: a
+    // quarter takes two adjacent rows, one row's units in fp16 chunk 0 and the
+    // other's in chunk 1.  d = 64: a quarter takes two adjacent rows, four
+    // units each.
+    auto unit_of = [&](int idx, int& rr, int& w) {
+        if constexpr (V_UNITS == 8) {
+            const int w_lo = idx & 3, half = (idx >> 2) & 1, sel = (idx >> 3) & 1;
+            rr = 2 * (idx >> 4) + half;
+            w = 4 * (half ^ sel) + w_lo;
+        } else {
+            rr = idx / V_UNITS;
+            w = idx % V_UNITS;
+        }
+    };
+    // one share (this lane's units [k_begin, k_end)) of V_j: wait for the tile
+    // and for the buffer (released by both tiles' P V MMAs two tiles
+    // earlier), widen with loads batched so their latency overlaps, then hand
+    // the share over (every lane's writes fenced for the async proxy, one
+    // arrival per warp on v16_full and on the ring slot's release)
+    auto widen_share = [&](int j, int k_begin, int k_end) -> bool {
+        const int itV = 2 * j + 1;
+        const int slot = itV % C::SLOTS;
+        bool ok = __all_sync(0xffffffffu, wait_bar(b_kv_full + 8 * slot, (uint32_t)(itV / C::SLOTS) & 1u,
+                                                   abort_flag, lim));
+        if (ok)
+            ok = __all_sync(0xffffffffu, wait_bar(b_v16_empty + 8 * (j & 1), ((uint32_t)(j >> 1) & 1u) ^ 1u,
+                                                  abort_flag, lim));
+        if (!ok) return false;
+        const uint32_t src = smem_u32(sKV + (size_t)slot * C::TILE);
+        const uint32_t dst = smem_u32(sV16 + (size_t)(j & 1) * C::V16T);
+        // loads in batches of 8 units (4 or 2 where the share is not a multiple of 8)
+        if ((k_end - k_begin) % 8 == 0) {
+#pragma unroll 1
+            for (int k0 = k_begin; k0 < k_end; k0 += 8) {
+                uint32_t x[8][4];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    int rr, w;
+                    unit_of(lane + 32 * (k0 + k), rr, w);
+                    // e4m3 row rr: 128-byte swizzle (w ^ rr%8) or 64-byte (w ^ (rr/2)%4)
+                    const int wp = (C::CB == 128) ? (w ^ (rr & 7)) : (w ^ ((rr >> 1) & 3));
+                    ld_shared_v4(src + (uint32_t)(rr * C::CB + wp * 16), x[k]);
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    int rr, w;
+                    unit_of(lane + 32 * (k0 + k), rr, w);
+                    uint32_t hv[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        hv[2 * e] = e4m3x2_to_f16x2((uint16_t)(x[k][e] & 0xffffu));
+                        hv[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(x[k][e] >> 16));
+                    }
+                    // values d = 16 w .. 16 w + 15: fp16 chunk w / 4, units 2 (w % 4), +1
+                    const uint32_t row = dst + (uint32_t)((w >> 2) * C::V16_CHUNK + rr * C::V16_CB);
+                    const int u0 = 2 * (w & 3);
+                    st_shared_v4(row + (uint32_t)((u0 ^ (rr & 7)) << 4), hv[0], hv[1], hv[2], hv[3]);
+                    st_shared_v4(row + (uint32_t)(((u0 + 1) ^ (rr & 7)) << 4), hv[4], hv[5], hv[6], hv[7]);
+                }
+            }
+        } else if ((k_end - k_begin) % 4 == 0) {
+#pragma unroll 1
+            for (int k0 = k_begin; k0 < k_end; k0 += 4) {
+                uint32_t x[4][4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    int rr, w;
+                    unit_of(lane + 32 * (k0 + k), rr, w);
+                    // e4m3 row rr: 128-byte swizzle (w ^ rr%8) or 64-byte (w ^ (rr/2)%4)
+                    const int wp = (C::CB == 128) ? (w ^ (rr & 7)) : (w ^ ((rr >> 1) & 3));
+                    ld_shared_v4(src + (uint32_t)(rr * C::CB + wp * 16), x[k]);
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    int rr, w;
+                    unit_of(lane + 32 * (k0 + k), rr, w);
+                    uint32_t hv[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        hv[2 * e] = e4m3x2_to_f16x2((uint16_t)(x[k][e] & 0xffffu));
+                        hv[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(x[k][e] >> 16));
+                    }
+                    // values d = 16 w .. 16 w + 15: fp16 chunk w / 4, units 2 (w % 4), +1
+                    const uint32_t row = dst + (uint32_t)((w >> 2) * C::V16_CHUNK + rr * C::V16_CB);
+                    const int u0 = 2 * (w & 3);
+                    st_shared_v4(row + (uint32_t)((u0 ^ (rr & 7)) << 4), hv[0], hv[1], hv[2], hv[3]);
+                    st_shared_v4(row + (uint32_t)(((u0 + 1) ^ (rr & 7)) << 4), hv[4], hv[5], hv[6], hv[7]);
+                }
+            }
+        } else {
+#pragma unroll 1
+            for (int k0 = k_begin; k0 < k_end; k0 += 2) {
+                uint32_t x[2][4];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    int rr, w;
+                    unit_of(lane + 32 * (k0 + k), rr, w);
+                    // e4m3 row rr: 128-byte swizzle (w ^ rr%8) or 64-byte (w ^ (rr/2)%4)
+                    const int wp = (C::CB == 128) ? (w ^ (rr & 7)) : (w ^ ((rr >> 1) & 3));
+                    ld_shared_v4(src + (uint32_t)(rr * C::CB + wp * 16), x[k]);
+                }
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    int rr, w;
+                    unit_of(lane + 32 * (k0 + k), rr, w);
+                    uint32_t hv[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        hv[2 * e] = e4m3x2_to_f16x2((uint16_t)(x[k][e] & 0xffffu));
+                        hv[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(x[k][e] >> 16));
+                    }
+                    // values d = 16 w .. 16 w + 15: fp16 chunk w / 4, units 2 (w % 4), +1
+                    const uint32_t row = dst + (uint32_t)((w >> 2) * C::V16_CHUNK + rr * C::V16_CB);
+                    const int u0 = 2 * (w & 3);
+                    st_shared_v4(row + (uint32_t)((u0 ^ (rr & 7)) << 4), hv[0], hv[1], hv[2], hv[3]);
+                    st_shared_v4(row + (uint32_t)(((u0 + 1) ^ (rr & 7)) << 4), hv[4], hv[5], hv[6], hv[7]);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        mbar_arrive_1(b_v16_full + 8 * (j & 1));
+        mbar_arrive_1(b_kv_empty + 8 * slot);
+        return true;
+    };
+
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0 && n_max > 0) {
-            const int nq = (n_kv[0] > 0) + (n_kv[1] > 0);
-            mbar_arrive_expect_tx(b_q_full, (uint32_t)(nq * C::TILE));
-            for (int t = 0; t < 2; ++t) {
-                if (n_kv[t] == 0) continue;
-                for (int c = 0; c < C::NC; ++c)
-                    tma_load_4d(smem_u32(sQ + t * C::TILE + c * C::CHUNK), &tmQ, b_q_full,
-                                c * (C::CB / C::E), h, q0[t], b);
-            }
-            // item 2j = K_j, item 2j+1 = V_j (the order the MMAs first use them)
-            int it = 0;
-            bool ok = true;
-            for (; it < 2 * n_max && it < p.items_limit; ++it) {
-                const int slot = it % C::SLOTS;
-                const uint32_t ph = (uint32_t)(it / C::SLOTS) & 1u;
-                if (!wait_bar(b_kv_empty + 8 * slot, ph ^ 1u, abort_flag, lim)) {
-                    ok = false;
-                    break;
+        if constexpr (C::F16P) {
+            // The whole warp runs the loop (lane 0 issues the copies) and also
+            // widens its share of every V tile: its share of V_c right after
+            // V_{c+2}'s load has gone out (buffer c % 2 is then about to be
+            // freed by the P V MMAs of tile c - 2; P V_c is two tiles on).
+            if (n_max > 0) {
+                if (lane == 0) {
+                    const int nq = (n_kv[0] > 0) + (n_kv[1] > 0);
+                    mbar_arrive_expect_tx(b_q_full, (uint32_t)(nq * C::TILE));
+                    for (int t = 0; t < 2; ++t) {
+                        if (n_kv[t] == 0) continue;
+                        for (int c = 0; c < C::NC; ++c)
+                            tma_load_4d(smem_u32(sQ + t * C::TILE + c * C::CHUNK), &tmQ, b_q_full,
+                                        c * (C::CB / C::E), h, q0[t], b);
+                    }
                 }
-                mbar_arrive_expect_tx(b_kv_full + 8 * slot, C::TILE);
-                const CUtensorMap* tm = (it & 1) ? &tmV : &tmK;
-                uint8_t* dst = sKV + (size_t)slot * C::TILE;
-                for (int c = 0; c < C::NC; ++c)
-                    tma_load_4d(smem_u32(dst + c * C::CHUNK), tm, b_kv_full + 8 * slot,
-                                c * (C::CB / C::E), h_kv, (j0 + (it >> 1)) * BN, b);
+                __syncwarp();
+                // item 2j = K_j, item 2j+1 = V_j (the order the MMAs first use them)
+                int it = 0, next_share = 0;
+                bool ok = true;
+                for (; it < 2 * n_max && it < p.items_limit && ok; ++it) {
+                    const int slot = it % C::SLOTS;
+                    const uint32_t ph = (uint32_t)(it / C::SLOTS) & 1u;
+                    ok = __all_sync(0xffffffffu, wait_bar(b_kv_empty + 8 * slot, ph ^ 1u, abort_flag, lim));
+                    if (!ok) break;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(b_kv_full + 8 * slot, C::TILE);
+                        const CUtensorMap* tm = (it & 1) ? &tmV : &tmK;
+                        uint8_t* dst = sKV + (size_t)slot * C::TILE;
+                        for (int c = 0; c < C::NC; ++c)
+                            tma_load_4d(smem_u32(dst + c * C::CHUNK), tm, b_kv_full + 8 * slot,
+                                        c * (C::CB / C::E), h_kv, (j0 + (it >> 1)) * BN, b);
+                    }
+                    __syncwarp();
+                    if ((it & 1) && (it >> 1) >= 2) ok = widen_share(next_share++, V_PROD0, V_PROD0 + V_PROD);
+                }
+                // the last tiles' shares
+                for (; ok && next_share < n_max; ++next_share) ok = widen_share(next_share, V_PROD0, V_PROD0 + V_PROD);
+                if (!ok && lane == 0) {
+                    // let every load already issued land before the CTA can exit
+                    wait_drain(b_q_full, 0, p.drain_ns);
+                    for (int k = (it > C::SLOTS ? it - C::SLOTS : 0); k < it; ++k)
+                        wait_drain(b_kv_full + 8 * (k % C::SLOTS), (uint32_t)(k / C::SLOTS) & 1u, p.drain_ns);
+                }
             }
-            if (!ok) {
-                // let every load already issued land before the CTA can exit
-                wait_drain(b_q_full, 0, p.drain_ns);
-                for (int k = (it > C::SLOTS ? it - C::SLOTS : 0); k < it; ++k)
-                    wait_drain(b_kv_full + 8 * (k % C::SLOTS), (uint32_t)(k / C::SLOTS) & 1u, p.drain_ns);
+        } else {
+            if (lane == 0 && n_max > 0) {
+                const int nq = (n_kv[0] > 0) + (n_kv[1] > 0);
+                mbar_arrive_expect_tx(b_q_full, (uint32_t)(nq * C::TILE));
+                for (int t = 0; t < 2; ++t) {
+                    if (n_kv[t] == 0) continue;
+                    for (int c = 0; c < C::NC; ++c)
+                        tma_load_4d(smem_u32(sQ + t * C::TILE + c * C::CHUNK), &tmQ, b_q_full,
+                                    c * (C::CB / C::E), h, q0[t], b);
+                }
+                // item 2j = K_j, item 2j+1 = V_j (the order the MMAs first use them)
+                int it = 0;
+                bool ok = true;
+                for (; it < 2 * n_max && it < p.items_limit; ++it) {
+                    const int slot = it % C::SLOTS;
+                    const uint32_t ph = (uint32_t)(it / C::SLOTS) & 1u;
+                    if (!wait_bar(b_kv_empty + 8 * slot, ph ^ 1u, abort_flag, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(b_kv_full + 8 * slot, C::TILE);
+                    const CUtensorMap* tm = (it & 1) ? &tmV : &tmK;
+                    uint8_t* dst = sKV + (size_t)slot * C::TILE;
+                    for (int c = 0; c < C::NC; ++c)
+                        tma_load_4d(smem_u32(dst + c * C::CHUNK), tm, b_kv_full + 8 * slot,
+                                    c * (C::CB / C::E), h_kv, (j0 + (it >> 1)) * BN, b);
+                }
+                if (!ok) {
+                    // let every load already issued land before the CTA can exit
+                    wait_drain(b_q_full, 0, p.drain_ns);
+                    for (int k = (it > C::SLOTS ? it - C::SLOTS : 0); k < it; ++k)
+                        wait_drain(b_kv_full + 8 * (k % C::SLOTS), (uint32_t)(k / C::SLOTS) & 1u, p.drain_ns);
+                }
             }
         }
         __syncwarp();
@@ -404,9 +600,10 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                 // (a tile past its own key range drops out), and each waits
                 // until the softmax of the one before it has loaded its scores
                 // (s_free).  P_t V_j reads fp16 P_t from TMEM and the fp16 copy
-                // of V_j the converter wrote into buffer j % 2; the buffer is
-                // released when the MMA has read it.  Key tiles this tile
-                // never reads release their K slot and V buffer once filled.
+                // of V_j in buffer j % 2 (widened by the converter warp and both
+                // issuers); the buffer is released when the MMA has read it.
+                // Key tiles this tile never reads release their K slot and V
+                // buffer once filled (and still get this issuer's share of V).
                 const int t = __shfl_sync(0xffffffffu, warp, 0) - 1;
                 const int nt = n_kv[t], nt_o = n_kv[1 - t];
                 const uint32_t drain_t = t == 0 ? b_drain : b_drain_b;
@@ -426,6 +623,8 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                     }
                     return pt < 0 || wb(b_s_free + 8 * pt, (uint32_t)pj & 1u);
                 };
+                // this issuer's quarter of every V tile's units
+                const int vk0 = V_ISS0 + t * V_ISS, vk1 = vk0 + V_ISS;
                 ok = wb(b_q_full, 0);
                 if (ok && nt > 0) {
                     ok = wb(b_kv_full + 8 * slot_of(0), par_of(0));
@@ -437,6 +636,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                         mma_commit_1(b_kv_empty + 8 * slot_of(0));
                     }
                 }
+                if (ok && n_max > 0) ok = widen_share(0, vk0, vk1);
                 for (int j = 0; j < nt && ok; ++j) {
                     const int itK = 2 * j + 2;
                     if (j + 1 < nt) {
@@ -455,12 +655,15 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                     issue_pv(t, j & 1, j == 0);
                     mma_commit_1(b_pv_done + 8 * t);
                     mma_commit_1(b_v16_empty + 8 * (j & 1));
+                    // the MMAs run on their own: widen this issuer's share of the next V
+                    if (j + 1 < n_max) ok = widen_share(j + 1, vk0, vk1);
                 }
                 for (int j = nt; j < n_max && ok; ++j) {
                     ok = wb(b_kv_full + 8 * slot_of(2 * j), par_of(2 * j));
                     if (ok) mbar_arrive_1(b_kv_empty + 8 * slot_of(2 * j));
                     if (ok) ok = wb(b_v16_full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u);
                     if (ok) mbar_arrive_1(b_v16_empty + 8 * (j & 1));
+                    if (ok && j + 1 < n_max) ok = widen_share(j + 1, vk0, vk1);
                 }
                 if (!ok) {
                     // make sure none of this issuer's MMAs still runs when TMEM is freed
@@ -576,79 +779,9 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         __syncwarp();
     } else if (C::F16P && warp == C::CONVERTER_WARP) {
         // ------------------------------------------- V converter (F16P only)
-        // Widens each e4m3 V tile (ring slot) into an fp16 tile in buffer
-        // j % 2, laid out as a 16-bit V tile loaded by TMA would be (128-byte
-        // rows of 64 values, 128-byte swizzle); every e4m3 value is exact in
-        // fp16.  Loads go out eight at a time so their latency overlaps.  The
-        // ring slot is released once read; the buffer is handed to both
-        // issuers through v16_full (every lane's writes fenced for the async
-        // proxy, then one arrival for the warp).  It waits for the buffer to
-        // be released by both tiles' P V MMAs of two tiles earlier.
-        constexpr int UNITS = C::CB / 16;        // 16-byte units per e4m3 row
-        constexpr int PER = BN * UNITS / 32;     // units per lane
-        constexpr int BATCH = 8;
-        // Unit idx of the tile -> (row rr, 16-byte unit w of the e4m3 row),
-        // chosen so that the eight lanes of each quarter-warp hit eight
-        // different 16-byte bank groups both when they load (e4m3 swizzle)
-        // and when they store (fp16 swizzle, the two 64-value chunks 16 KB
-        // apart).  d = 128: a quarter takes two adjacent rows, one row's
-        // units in fp16 chunk 0 and the other's in chunk 1.  d = 64: a
-        // quarter takes two adjacent rows, four units each.
-        auto unit_of = [&](int idx, int& rr, int& w) {
-            if constexpr (UNITS == 8) {
-                const int w_lo = idx & 3, half = (idx >> 2) & 1, sel = (idx >> 3) & 1;
-                rr = 2 * (idx >> 4) + half;
-                w = 4 * (half ^ sel) + w_lo;
-            } else {
-                rr = idx / UNITS;
-                w = idx % UNITS;
-            }
-        };
-        for (int j = 0; j < n_max; ++j) {
-            const int itV = 2 * j + 1;
-            const int slot = itV % C::SLOTS;
-            bool ok = __all_sync(0xffffffffu, wait_bar(b_kv_full + 8 * slot,
-                                                       (uint32_t)(itV / C::SLOTS) & 1u, abort_flag, lim));
-            if (ok)
-                ok = __all_sync(0xffffffffu, wait_bar(b_v16_empty + 8 * (j & 1),
-                                                      ((uint32_t)(j >> 1) & 1u) ^ 1u, abort_flag, lim));
-            if (!ok) break;
-            const uint32_t src = smem_u32(sKV + (size_t)slot * C::TILE);
-            const uint32_t dst = smem_u32(sV16 + (size_t)(j & 1) * C::V16T);
-#pragma unroll 1
-            for (int k0 = 0; k0 < PER; k0 += BATCH) {
-                uint32_t x[BATCH][4];
-#pragma unroll
-                for (int k = 0; k < BATCH; ++k) {
-                    int rr, w;
-                    unit_of(lane + 32 * (k0 + k), rr, w);
-                    // e4m3 row rr: 128-byte swizzle (w ^ rr%8) or 64-byte (w ^ (rr/2)%4)
-                    const int wp = (C::CB == 128) ? (w ^ (rr & 7)) : (w ^ ((rr >> 1) & 3));
-                    ld_shared_v4(src + (uint32_t)(rr * C::CB + wp * 16), x[k]);
-                }
-#pragma unroll
-                for (int k = 0; k < BATCH; ++k) {
-                    int rr, w;
-                    unit_of(lane + 32 * (k0 + k), rr, w);
-                    uint32_t hv[8];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        hv[2 * e] = e4m3x2_to_f16x2((uint16_t)(x[k][e] & 0xffffu));
-                        hv[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(x[k][e] >> 16));
-                    }
-                    // values d = 16 w .. 16 w + 15: fp16 chunk w / 4, units 2 (w % 4), +1
-                    const uint32_t row = dst + (uint32_t)((w >> 2) * C::V16_CHUNK + rr * C::V16_CB);
-                    const int u0 = 2 * (w & 3);
-                    st_shared_v4(row + (uint32_t)((u0 ^ (rr & 7)) << 4), hv[0], hv[1], hv[2], hv[3]);
-                    st_shared_v4(row + (uint32_t)(((u0 + 1) ^ (rr & 7)) << 4), hv[4], hv[5], hv[6],
-                                 hv[7]);
-                }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            mbar_arrive_1(b_v16_full + 8 * (j & 1));
-            mbar_arrive_1(b_kv_empty + 8 * slot);
-        }
+        // Its share of every V tile's units (producer and issuers take the rest).
+        for (int j = 0; j < n_max; ++j)
+            if (!widen_share(j, 0, V_CONV)) break;
     } else {
         // --------------------------------------- softmax + epilogue (2 x 128 thr)
         const int t = (warp - C::SOFTMAX_WARP0) >> 2;  // tile of this warp group
