@@ -449,8 +449,12 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         if constexpr (C::F16P) {
             // The whole warp runs the loop (lane 0 issues the copies) and also
             // widens its share of every V tile: its share of V_c right after
-            // V_{c+2}'s load has gone out (buffer c % 2 is then about to be
-            // freed by the P V MMAs of tile c - 2; P V_c is two tiles on).
+            // V_{c+LAG}'s load has gone out.  LAG must stay below the ring's
+            // depth in tiles (V_{c+SLOTS/2} reuses V_c's slot, which only the
+            // complete widening of V_c frees); 3 measured best on C5 (0.576
+            // ms per call against 0.581 for 1 or 2).
+            constexpr int LAG = 3;
+            static_assert(!C::F16P || LAG < C::SLOTS / 2, "the producer's share must come before its slot is needed");
             if (n_max > 0) {
                 if (lane == 0) {
                     const int nq = (n_kv[0] > 0) + (n_kv[1] > 0);
@@ -480,7 +484,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                                         c * (C::CB / C::E), h_kv, (j0 + (it >> 1)) * BN, b);
                     }
                     __syncwarp();
-                    if ((it & 1) && (it >> 1) >= 2) ok = widen_share(next_share++, V_PROD0, V_PROD0 + V_PROD);
+                    if ((it & 1) && (it >> 1) >= LAG) ok = widen_share(next_share++, V_PROD0, V_PROD0 + V_PROD);
                 }
                 // the last tiles' shares
                 for (; ok && next_share < n_max; ++next_share) ok = widen_share(next_share, V_PROD0, V_PROD0 + V_PROD);
