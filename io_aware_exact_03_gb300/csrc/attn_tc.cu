@@ -970,31 +970,116 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
 
         if (ok && nt > 0)
             ok = __all_sync(0xffffffffu, wait_bar(pv_done, (uint32_t)(nt - 1) & 1u, abort_flag, lim));
-        if (ok) {
-            tc_fence_after();
+        // e4m3, d = 128: O (bf16) is staged in Q_t's buffer, which holds one
+        // 64-column chunk of it (16 KB), and written by two TMA stores, so the
+        // rows leave as whole 128-byte lines (stored from registers, each warp
+        // store instruction touched 32 rows 4 KB apart).  Q_t is no longer
+        // read: this issuer's pv_done covers its last score MMA.
+        constexpr bool STAGE_O8 = (KIND == kE4M3 && D == 128);
+        if (STAGE_O8 && p.n_splits == 1) {
             const bool valid = row_g < p.N_q;
-            const bool has = l > 0.f;
-            const float inv = has ? dv / l : 0.f;
-            const bool split = p.n_splits > 1;
-            const size_t prow_idx =
-                ((size_t)blockIdx.y * ((size_t)p.B * p.H) + bh) * p.N_q + (valid ? row_g : 0);
-            uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
-                             (((size_t)b * p.N_q + (valid ? row_g : 0)) * p.H + h) * D;
-            float* prow = split ? p.part_o + prow_idx * D : nullptr;
+            const float inv = l > 0.f ? dv / l : 0.f;
+            if (ok) tc_fence_after();
+            const uint32_t row_base =
+                smem_u32(sQ + t * C::TILE) + (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u;
+            for (int c = 0; c < D / 64; ++c) {
+                if (ok) {
 #pragma unroll
-            for (int u = 0; u < D / 32; ++u) {
-                uint32_t oo[32];
-                if (nt > 0) {
-                    tmem_ld32(t_row + col_o<D>(t) + 32 * u, oo);
-                    tmem_ld_wait();
-                    reg_fence32(oo);
-                } else {
+                    for (int uu = 0; uu < 2; ++uu) {
+                        uint32_t oo[32];
+                        if (nt > 0) {
+                            tmem_ld32(t_row + col_o<D>(t) + 32 * (2 * c + uu), oo);
+                            tmem_ld_wait();
+                            reg_fence32(oo);
+                        } else {
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) oo[x] = 0u;
+                            for (int x = 0; x < 32; ++x) oo[x] = 0u;
+                        }
+                        uint32_t packed[16];
+#pragma unroll
+                        for (int x = 0; x < 16; ++x)
+                            packed[x] = pack_bf16(__uint_as_float(oo[2 * x]) * inv,
+                                                  __uint_as_float(oo[2 * x + 1]) * inv);
+                        // row r of the 128-byte-swizzled chunk: unit w at w ^ (r % 8)
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            const int w = uu * 4 + x;
+                            st_shared_v4(row_base + ((uint32_t)(w ^ (r & 7)) << 4), packed[4 * x],
+                                         packed[4 * x + 1], packed[4 * x + 2], packed[4 * x + 3]);
+                        }
+                    }
                 }
-                if (C::TMA_O && !split) {
-                    // row r of the 128-byte-swizzled tile in Q_t's buffer: 16-byte
-                    // unit w of d-chunk c sits at unit w ^ (r % 8)
+                // every thread of the tile reaches both barriers, whether or not
+                // its waits succeeded; one thread stores the chunk (rows past
+                // N_q are not written) and waits until it has been read
+                fence_proxy_async_smem();
+                named_barrier(1 + t, 128);
+                if (r == 0 && ok && !*abort_flag && q0[t] < p.N_q) {
+                    tma_store_4d(&tmO, smem_u32(sQ + t * C::TILE), c * 64, h, q0[t], b);
+                    bulk_commit_group();
+                    bulk_wait_group_read0();
+                }
+                named_barrier(1 + t, 128);
+            }
+            if (ok && valid && p.lse)
+                p.lse[(size_t)bh * p.N_q + row_g] =
+                    l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        } else {
+            if (ok) {
+                tc_fence_after();
+                const bool valid = row_g < p.N_q;
+                const bool has = l > 0.f;
+                const float inv = has ? dv / l : 0.f;
+                const bool split = p.n_splits > 1;
+                const size_t prow_idx =
+                    ((size_t)blockIdx.y * ((size_t)p.B * p.H) + bh) * p.N_q + (valid ? row_g : 0);
+                uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
+                                 (((size_t)b * p.N_q + (valid ? row_g : 0)) * p.H + h) * D;
+                float* prow = split ? p.part_o + prow_idx * D : nullptr;
+#pragma unroll
+                for (int u = 0; u < D / 32; ++u) {
+                    uint32_t oo[32];
+                    if (nt > 0) {
+                        tmem_ld32(t_row + col_o<D>(t) + 32 * u, oo);
+                        tmem_ld_wait();
+                        reg_fence32(oo);
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) oo[x] = 0u;
+                    }
+                    if (C::TMA_O && !split) {
+                        // row r of the 128-byte-swizzled tile in Q_t's buffer: 16-byte
+                        // unit w of d-chunk c sits at unit w ^ (r % 8)
+                        uint32_t packed[16];
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) {
+                            const float a0 = __uint_as_float(oo[2 * x]) * inv;
+                            const float a1 = __uint_as_float(oo[2 * x + 1]) * inv;
+                            packed[x] = (KIND == kFP16) ? pack_f16(a0, a1) : pack_bf16(a0, a1);
+                        }
+                        const uint32_t row_base = smem_u32(sQ + t * C::TILE + (u / 2) * C::CHUNK) +
+                                                  (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u;
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            const int w = (u % 2) * 4 + x;
+                            st_shared_v4(row_base + ((uint32_t)(w ^ (r & 7)) << 4), packed[4 * x],
+                                         packed[4 * x + 1], packed[4 * x + 2], packed[4 * x + 3]);
+                        }
+                        continue;
+                    }
+                    if (split) {
+                        // partial of this split, normalised by its own row sum
+                        if (valid) {
+                            float4* dst = reinterpret_cast<float4*>(prow + 32 * u);
+#pragma unroll
+                            for (int x = 0; x < 8; ++x)
+                                dst[x] = make_float4(__uint_as_float(oo[4 * x]) * inv,
+                                                     __uint_as_float(oo[4 * x + 1]) * inv,
+                                                     __uint_as_float(oo[4 * x + 2]) * inv,
+                                                     __uint_as_float(oo[4 * x + 3]) * inv);
+                        }
+                        continue;
+                    }
                     uint32_t packed[16];
 #pragma unroll
                     for (int x = 0; x < 16; ++x) {
@@ -1002,64 +1087,35 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                         const float a1 = __uint_as_float(oo[2 * x + 1]) * inv;
                         packed[x] = (KIND == kFP16) ? pack_f16(a0, a1) : pack_bf16(a0, a1);
                     }
-                    const uint32_t row_base = smem_u32(sQ + t * C::TILE + (u / 2) * C::CHUNK) +
-                                              (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u;
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const int w = (u % 2) * 4 + x;
-                        st_shared_v4(row_base + ((uint32_t)(w ^ (r & 7)) << 4), packed[4 * x],
-                                     packed[4 * x + 1], packed[4 * x + 2], packed[4 * x + 3]);
-                    }
-                    continue;
-                }
-                if (split) {
-                    // partial of this split, normalised by its own row sum
                     if (valid) {
-                        float4* dst = reinterpret_cast<float4*>(prow + 32 * u);
+                        uint4* dst = reinterpret_cast<uint4*>(orow + 32 * u);
 #pragma unroll
-                        for (int x = 0; x < 8; ++x)
-                            dst[x] = make_float4(__uint_as_float(oo[4 * x]) * inv,
-                                                 __uint_as_float(oo[4 * x + 1]) * inv,
-                                                 __uint_as_float(oo[4 * x + 2]) * inv,
-                                                 __uint_as_float(oo[4 * x + 3]) * inv);
+                        for (int x = 0; x < 4; ++x)
+                            dst[x] = make_uint4(packed[4 * x], packed[4 * x + 1], packed[4 * x + 2],
+                                                packed[4 * x + 3]);
                     }
-                    continue;
                 }
-                uint32_t packed[16];
-#pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const float a0 = __uint_as_float(oo[2 * x]) * inv;
-                    const float a1 = __uint_as_float(oo[2 * x + 1]) * inv;
-                    packed[x] = (KIND == kFP16) ? pack_f16(a0, a1) : pack_bf16(a0, a1);
-                }
-                if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * u);
-#pragma unroll
-                    for (int x = 0; x < 4; ++x)
-                        dst[x] = make_uint4(packed[4 * x], packed[4 * x + 1], packed[4 * x + 2],
-                                            packed[4 * x + 3]);
-                }
+                const float lse_row = has ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+                if (valid && split)
+                    p.part_lse[prow_idx] = lse_row;
+                else if (valid && p.lse)
+                    p.lse[(size_t)bh * p.N_q + row_g] = lse_row;
             }
-            const float lse_row = has ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-            if (valid && split)
-                p.part_lse[prow_idx] = lse_row;
-            else if (valid && p.lse)
-                p.lse[(size_t)bh * p.N_q + row_g] = lse_row;
-        }
-        if (C::TMA_O && p.n_splits == 1) {
-            // Every thread of the tile reaches this barrier, whether or not its
-            // waits succeeded (a barrier that an aborted warp skipped would
-            // never open).  Then one thread stores the tile from Q_t's buffer
-            // (rows past N_q are not written) and waits until the store has
-            // read shared memory.
-            fence_proxy_async_smem();
-            named_barrier(1 + t, 128);
-            if (r == 0 && ok && !*abort_flag && q0[t] < p.N_q) {
-                for (int c = 0; c < C::NC; ++c)
-                    tma_store_4d(&tmO, smem_u32(sQ + t * C::TILE + c * C::CHUNK), c * (C::CB / C::E),
-                                 h, q0[t], b);
-                bulk_commit_group();
-                bulk_wait_group_read0();
+            if (C::TMA_O && p.n_splits == 1) {
+                // Every thread of the tile reaches this barrier, whether or not its
+                // waits succeeded (a barrier that an aborted warp skipped would
+                // never open).  Then one thread stores the tile from Q_t's buffer
+                // (rows past N_q are not written) and waits until the store has
+                // read shared memory.
+                fence_proxy_async_smem();
+                named_barrier(1 + t, 128);
+                if (r == 0 && ok && !*abort_flag && q0[t] < p.N_q) {
+                    for (int c = 0; c < C::NC; ++c)
+                        tma_store_4d(&tmO, smem_u32(sQ + t * C::TILE + c * C::CHUNK), c * (C::CB / C::E),
+                                     h, q0[t], b);
+                    bulk_commit_group();
+                    bulk_wait_group_read0();
+                }
             }
         }
     }
@@ -1140,8 +1196,13 @@ cudaError_t launch_t(const Problem& pr, cudaStream_t stream, int n_splits = 1,
     CUtensorMap mq, mk, mv, mo;
     const int ce = C::CB / C::E;
     // O has the layout of Q; for 16-bit inputs also its element size
+    // e4m3 at d = 128: O is bf16, 64-column chunks staged in the Q buffer
+    const bool o8 = KIND == kE4M3 && D == 128 && n_splits == 1;
     if (C::TMA_O && n_splits == 1) {
         if (!tma::encode_map(&mo, pr.o, KIND, pr.B, pr.N_q, pr.H, D, ce, BM))
+            return cudaErrorInvalidValue;
+    } else if (o8) {
+        if (!tma::encode_map(&mo, pr.o, kBF16, pr.B, pr.N_q, pr.H, D, 64, BM))
             return cudaErrorInvalidValue;
     }
     if (!tma::encode_map(&mq, pr.q, KIND, pr.B, pr.N_q, pr.H, D, ce, BM) ||
@@ -1188,7 +1249,7 @@ cudaError_t launch_t(const Problem& pr, cudaStream_t stream, int n_splits = 1,
     if (e != cudaSuccess) return e;
     if (n_splits < 1 || n_splits > 65535) return cudaErrorInvalidValue;
     dim3 grid((unsigned)n_cta, (unsigned)n_splits);
-    if (!(C::TMA_O && n_splits == 1)) mo = mq;  // not read
+    if (!(C::TMA_O && n_splits == 1) && !o8) mo = mq;  // not read
     attn_tc_kernel<D, KIND><<<grid, C::THREADS, C::SMEM, stream>>>(mq, mk, mv, mo, p);
     return cudaGetLastError();
 }
