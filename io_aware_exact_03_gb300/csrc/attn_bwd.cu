@@ -73,18 +73,21 @@ struct BCfg {
     static constexpr int SLOTS_KV_FIT = (kSmemLimit - 1024 - 2 * TILE - 512) / ITEM_KV;
     static constexpr int SLOTS_KV = SLOTS_KV_FIT > 6 ? 6 : SLOTS_KV_FIT;
     static constexpr size_t SMEM_KV = 1024 + 2 * (size_t)TILE + (size_t)SLOTS_KV * ITEM_KV + 512;
-    // bwd_dq ring item: K tile, V tile
-    static constexpr int ITEM_Q = 2 * TILE;
-    static constexpr int SLOTS_Q_FIT = (kSmemLimit - 1024 - 2 * TILE - 512) / ITEM_Q;
-    static constexpr int SLOTS_Q = SLOTS_Q_FIT > 6 ? 6 : SLOTS_Q_FIT;
-    static constexpr size_t SMEM_Q = 1024 + 2 * (size_t)TILE + (size_t)SLOTS_Q * ITEM_Q + 512;
-    static_assert(SLOTS_KV >= 2 && SLOTS_Q >= 2, "ring depth");
+    // bwd_dq: separate K and V rings (V_j is free once dP_j is issued, K_j only
+    // after dQ_j): two V slots, the rest of shared memory (up to four) for K
+    static constexpr int V_SLOTS_Q = 2;
+    static constexpr int TILES_Q_FIT = (kSmemLimit - 1024 - 2 * TILE - 512) / TILE;
+    static constexpr int K_SLOTS_Q = (TILES_Q_FIT - V_SLOTS_Q) > 4 ? 4 : (TILES_Q_FIT - V_SLOTS_Q);
+    static constexpr size_t SMEM_Q =
+        1024 + 2 * (size_t)TILE + (size_t)(K_SLOTS_Q + V_SLOTS_Q) * TILE + 512;
+    static_assert(SLOTS_KV >= 2 && K_SLOTS_Q >= 3, "ring depth");
     static_assert(SMEM_KV <= (size_t)kSmemLimit && SMEM_Q <= (size_t)kSmemLimit, "smem");
 };
 
 // TMEM columns (both kernels): S or S^T [0,128), dP or dP^T [128,256),
-// accumulators from 256 (dV then dK, or dQ).
-constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256;
+// accumulators from 256 (dV then dK, or dQ); bwd_dq keeps a second S buffer
+// in [384, 512) (its accumulator takes at most 128 columns).
+constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256, kColS1 = 384;
 
 struct BwdParams {
     int B, H, N_q, N_k, N_pad;
@@ -516,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                   const BwdParams p) {
     using C = BCfg<D, KIND>;
-    constexpr int SLOTS = C::SLOTS_Q;
+    constexpr int KS = C::K_SLOTS_Q, VS = C::V_SLOTS_Q;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned by offsetting the shared array itself, so that every
     // pointer derived from it stays in the shared address space (plain loads
@@ -524,9 +527,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* sQ = smem;
     uint8_t* sG = smem + C::TILE;
-    uint8_t* sRing = smem + 2 * C::TILE;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + (size_t)SLOTS * C::ITEM_Q);
-    constexpr int NB = 6 + 2 * SLOTS;
+    uint8_t* sK = smem + 2 * C::TILE;   // KS K tiles
+    uint8_t* sV = sK + (size_t)KS * C::TILE;  // VS V tiles
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sV + (size_t)VS * C::TILE);
+    constexpr int NB = 7 + 2 * (KS + VS);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + NB);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     const uint32_t b_q_full = smem_u32(bars);
@@ -536,8 +540,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t b_p_half0 = smem_u32(bars + 2), b_p_half1 = smem_u32(bars + 5);
     const uint32_t b_acc_done = smem_u32(bars + 3);
     const uint32_t b_drain = smem_u32(bars + 4);
-    const uint32_t b_item_full = smem_u32(bars + 6);
-    const uint32_t b_item_empty = smem_u32(bars + 6 + SLOTS);
+    // dP_j has been read into registers: dP_{j+1} may overwrite it
+    const uint32_t b_dp_free = smem_u32(bars + 6);
+    const uint32_t b_k_full = smem_u32(bars + 7);                 // + 8 * K slot
+    const uint32_t b_k_empty = smem_u32(bars + 7 + KS);           // + 8 * K slot
+    const uint32_t b_v_full = smem_u32(bars + 7 + 2 * KS);        // + 8 * V slot
+    const uint32_t b_v_empty = smem_u32(bars + 7 + 2 * KS + VS);  // + 8 * V slot
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int b, h, rank;
@@ -563,9 +571,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(b_p_half1, 128);
         mbar_init(b_acc_done, 1);
         mbar_init(b_drain, 1);
-        for (int s = 0; s < SLOTS; ++s) {
-            mbar_init(b_item_full + 8 * s, 1);
-            mbar_init(b_item_empty + 8 * s, 1);
+        mbar_init(b_dp_free, 128);
+        for (int s = 0; s < KS; ++s) {
+            mbar_init(b_k_full + 8 * s, 1);
+            mbar_init(b_k_empty + 8 * s, 1);
+        }
+        for (int s = 0; s < VS; ++s) {
+            mbar_init(b_v_full + 8 * s, 1);
+            mbar_init(b_v_empty + 8 * s, 1);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -587,26 +600,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_4d(smem_u32(sQ + c * C::CHUNK), &tmQ, b_q_full, c * C::CE, h, q0, b);
                 tma_load_4d(smem_u32(sG + c * C::CHUNK), &tmG, b_q_full, c * C::CE, h, q0, b);
             }
+            // K_j then V_j, each into its own ring
             bool ok = true;
-            int j = 0;
-            for (; j < n; ++j) {
-                const int slot = j % SLOTS;
-                if (!wait_bar(b_item_empty + 8 * slot, ((uint32_t)(j / SLOTS) & 1u) ^ 1u, abort_flag, lim)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t* dst = sRing + (size_t)slot * C::ITEM_Q;
-                mbar_arrive_expect_tx(b_item_full + 8 * slot, (uint32_t)C::ITEM_Q);
-                for (int c = 0; c < C::NC; ++c) {
-                    tma_load_4d(smem_u32(dst + c * C::CHUNK), &tmK, b_item_full + 8 * slot, c * C::CE, hk, j * BN, b);
-                    tma_load_4d(smem_u32(dst + C::TILE + c * C::CHUNK), &tmV, b_item_full + 8 * slot,
+            int nk = 0, nv = 0;  // tiles issued into each ring
+            for (int j = 0; j < n && ok; ++j) {
+                const int ks = j % KS, vs = j % VS;
+                ok = wait_bar(b_k_empty + 8 * ks, ((uint32_t)(j / KS) & 1u) ^ 1u, abort_flag, lim);
+                if (!ok) break;
+                mbar_arrive_expect_tx(b_k_full + 8 * ks, (uint32_t)C::TILE);
+                for (int c = 0; c < C::NC; ++c)
+                    tma_load_4d(smem_u32(sK + (size_t)ks * C::TILE + c * C::CHUNK), &tmK, b_k_full + 8 * ks,
                                 c * C::CE, hk, j * BN, b);
-                }
+                ++nk;
+                ok = wait_bar(b_v_empty + 8 * vs, ((uint32_t)(j / VS) & 1u) ^ 1u, abort_flag, lim);
+                if (!ok) break;
+                mbar_arrive_expect_tx(b_v_full + 8 * vs, (uint32_t)C::TILE);
+                for (int c = 0; c < C::NC; ++c)
+                    tma_load_4d(smem_u32(sV + (size_t)vs * C::TILE + c * C::CHUNK), &tmV, b_v_full + 8 * vs,
+                                c * C::CE, hk, j * BN, b);
+                ++nv;
             }
             if (!ok) {
                 wait_drain(b_q_full, 0, kWaitLimitNs);
-                for (int k = (j > SLOTS ? j - SLOTS : 0); k < j; ++k)
-                    wait_drain(b_item_full + 8 * (k % SLOTS), (uint32_t)(k / SLOTS) & 1u, kWaitLimitNs);
+                for (int k = (nk > KS ? nk - KS : 0); k < nk; ++k)
+                    wait_drain(b_k_full + 8 * (k % KS), (uint32_t)(k / KS) & 1u, kWaitLimitNs);
+                for (int k = (nv > VS ? nv - VS : 0); k < nv; ++k)
+                    wait_drain(b_v_full + 8 * (k % VS), (uint32_t)(k / VS) & 1u, kWaitLimitNs);
             }
         }
         __syncwarp();
@@ -619,30 +638,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n > 0) {
             const uint64_t qd = smem_desc(smem_u32(sQ), 16, 8 * C::CB, 2u);
             const uint64_t gd = smem_desc(smem_u32(sG), 16, 8 * C::CB, 2u);
-            bool ok = wb(b_q_full, 0);
-            for (int j = 0; j < n && ok; ++j) {
-                const int slot = j % SLOTS;
-                ok = wb(b_item_full + 8 * slot, (uint32_t)(j / SLOTS) & 1u);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t ka = smem_u32(sRing + (size_t)slot * C::ITEM_Q);
-                const uint32_t va = ka + C::TILE;
-                const uint64_t kd = smem_desc(ka, 16, 8 * C::CB, 2u);
-                const uint64_t vd = smem_desc(va, 16, 8 * C::CB, 2u);
-                // S = Q K^T and dP = dO V^T
+            // S_j goes to S buffer j % 2 and dS_j over it, so the scores of key
+            // tile j + 1 run while the elementwise warps work on tile j: S_{j+1}
+            // at once (its buffer was last read by dQ_{j-1}, issued before), dP_{j+1}
+            // once dP_j has been read (dp_free); then dQ_j from dS_j.
+            auto sbuf = [](int j) { return (j & 1) ? kColS1 : kColS; };
+            auto k_addr = [&](int j) { return smem_u32(sK + (size_t)(j % KS) * C::TILE); };
+            auto v_desc = [&](int j) {
+                return smem_desc(smem_u32(sV + (size_t)(j % VS) * C::TILE), 16, 8 * C::CB, 2u);
+            };
+            auto wait_k = [&](int j) { return wb(b_k_full + 8 * (j % KS), (uint32_t)(j / KS) & 1u); };
+            auto wait_v = [&](int j) { return wb(b_v_full + 8 * (j % VS), (uint32_t)(j / VS) & 1u); };
+            auto issue_s = [&](int j, uint64_t kd) {  // S_j = Q K_j^T
 #pragma unroll
                 for (int c = 0; c < C::NC; ++c) {
 #pragma unroll
                     for (int ks = 0; ks < C::CB / 32; ++ks) {
                         const uint32_t o16 = (uint32_t)(c * C::CHUNK + ks * 32) >> 4;
-                        const uint32_t acc = (c | ks) != 0;
-                        mma_f16_ss_1(tmem + kColS, qd + o16, kd + o16, C::IDESC_S, acc);
-                        mma_f16_ss_1(tmem + kColDP, gd + o16, vd + o16, C::IDESC_S, acc);
+                        mma_f16_ss_1(tmem + sbuf(j), qd + o16, kd + o16, C::IDESC_S, (c | ks) != 0);
                     }
                 }
+            };
+            auto issue_dp = [&](uint64_t vd) {  // dP_j = dO V_j^T
+#pragma unroll
+                for (int c = 0; c < C::NC; ++c) {
+#pragma unroll
+                    for (int ks = 0; ks < C::CB / 32; ++ks) {
+                        const uint32_t o16 = (uint32_t)(c * C::CHUNK + ks * 32) >> 4;
+                        mma_f16_ss_1(tmem + kColDP, gd + o16, vd + o16, C::IDESC_S, (c | ks) != 0);
+                    }
+                }
+            };
+            bool ok = wb(b_q_full, 0);
+            if (ok) ok = wait_k(0);
+            if (ok) ok = wait_v(0);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, smem_desc(k_addr(0), 16, 8 * C::CB, 2u));
+                issue_dp(v_desc(0));
                 mma_commit_1(b_s_full);
-                // dQ += dS K: A = dS from TMEM (K = 128 keys, in two halves), B = K MN-major
-                const uint64_t kmn = smem_desc(ka, C::CHUNK, 8 * C::CB, 2u);
+                mma_commit_1(b_v_empty);  // V_0 is read by dP_0 only
+            }
+            for (int j = 0; j < n && ok; ++j) {
+                if (j + 1 < n) {
+                    ok = wait_k(j + 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(j + 1, smem_desc(k_addr(j + 1), 16, 8 * C::CB, 2u));
+                    ok = wait_v(j + 1);
+                    if (ok) ok = wb(b_dp_free, (uint32_t)j & 1u);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_dp(v_desc(j + 1));
+                    mma_commit_1(b_s_full);
+                    mma_commit_1(b_v_empty + 8 * ((j + 1) % VS));
+                }
+                // dQ += dS K: A = dS_j from S buffer j % 2 (K = 128 keys, in two
+                // halves), B = K_j MN-major
+                const uint64_t kmn = smem_desc(k_addr(j), C::CHUNK, 8 * C::CB, 2u);
                 for (int half = 0; half < 2 && ok; ++half) {
                     ok = wb(half ? b_p_half1 : b_p_half0, (uint32_t)j & 1u);
                     if (!ok) break;
@@ -652,12 +705,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int ks = half * (BN / C::MMA_K / 2) + kh;
                         const uint32_t o16 = (uint32_t)(ks * C::MMA_K * C::CB) >> 4;
                         const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
-                        mma_f16_ts_1(tmem + kColAcc, tmem + kColDP + ks * (C::MMA_K / 2), kmn + o16,
-                                   C::IDESC_ACC, acc);
+                        mma_f16_ts_1(tmem + kColAcc, tmem + sbuf(j) + ks * (C::MMA_K / 2), kmn + o16,
+                                     C::IDESC_ACC, acc);
                     }
                 }
                 if (!ok) break;
-                mma_commit_1(b_item_empty + 8 * slot);
+                mma_commit_1(b_k_empty + 8 * (j % KS));  // K_j is read by S_j and dQ_j
             }
             if (ok) {
                 mma_commit_1(b_acc_done);
@@ -687,12 +740,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
+            const uint32_t sb = (j & 1) ? kColS1 : kColS;  // S buffer of this key tile
             const int cl_max = row_lim - j * BN;  // columns > cl_max are masked
 #pragma unroll
             for (int v = 0; v < 2; ++v) {
                 uint32_t sr[64], dr[64];
-                tmem_ld32(t_row + kColS + 64 * v, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-                tmem_ld32(t_row + kColS + 64 * v + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                tmem_ld32(t_row + sb + 64 * v, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                tmem_ld32(t_row + sb + 64 * v + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
                 tmem_ld32(t_row + kColDP + 64 * v, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
                 tmem_ld32(t_row + kColDP + 64 * v + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
                 tmem_ld_wait();
@@ -700,6 +754,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
                 reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
                 reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+                if (v == 1) {
+                    // all of dP_j is in registers: the next tile's dP may overwrite it
+                    tc_fence_before();
+                    mbar_arrive(b_dp_free);
+                }
                 uint32_t dk[32];
                 // every key of this step allowed for every row of the warp: no
                 // per-element mask, packed f32x2 arithmetic
@@ -729,7 +788,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dk[x / 2] = (KIND == kBF16) ? pack_bf16(ds[0], ds[1]) : pack_f16(ds[0], ds[1]);
                     }
                 }
-                tmem_st32(t_row + kColDP + 32 * v, dk);
+                // dS of these 64 keys = 32 columns, over S columns read above
+                tmem_st32(t_row + sb + 32 * v, dk);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(v ? b_p_half1 : b_p_half0);
