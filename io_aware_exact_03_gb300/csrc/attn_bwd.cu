@@ -16,7 +16,7 @@
 //   dQ   = scale dS K,   dK = scale dS^T Q
 //
 // Three kernels, each using only MMA forms of the forward kernel:
-//   * bwd_prep: D_i and lse_i in base 2 into a padded workspace (one warp per
+//   * bwd_prep: D_i and lse_i in base 2 into a padded workspace (D / 8 lanes per
 //     row; rows with no key get lse2 = +inf so their P is exactly 0);
 //   * bwd_dkdv: one CTA per 128-key tile.  Per query tile: S^T = K Q^T and
 //     dP^T = V dO^T into TMEM (both K-major from shared memory, the forward's
@@ -139,57 +139,73 @@ __device__ __forceinline__ void decode(long long L, const BwdParams& p, int n_he
 }
 
 // ---------------------------------------------------------------- prep
-// One warp per row; each lane loads its d / 32 consecutive elements of o and
-// dO with one vector load each (memory-bound: reads o and dO once).
+// Memory-bound (reads o and dO once).  Each lane loads 16 bytes (8 values) of
+// o and of dO per row, D / 8 lanes covering a row; a warp takes 8 rows, so
+// every lane has 8 loads of 16 bytes in flight before its first use.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const void* o, const void* dO, const float* lse,
                                                        float* lse2, float* Dvec, int B, int H, int N_q,
                                                        int N_pad, int fp16) {
-    constexpr int PER = D / 32;  // elements per lane: 2 (d 64) or 4 (d 128)
-    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    constexpr int LPR = D / 8;      // lanes per row: 16 (d 128) or 8 (d 64)
+    constexpr int RPI = 32 / LPR;   // rows per warp load: 2 or 4
+    constexpr int RPW = 8;          // rows per warp
+    constexpr int NI = RPW / RPI;   // load rounds: 4 or 2
     const int lane = threadIdx.x & 31;
-    if (row >= (long long)B * H * N_pad) return;
-    const long long bh = row / N_pad;
-    const int i = (int)(row % N_pad);
-    float dsum = 0.f, l2 = INFINITY;
-    if (i < N_q) {
-        const int b = (int)(bh / H), h = (int)(bh % H);
-        const size_t base = (((size_t)b * N_q + i) * H + h) * D + (size_t)lane * PER;
-        uint32_t ow[PER / 2], gw[PER / 2];
-        if constexpr (PER == 4) {
-            const uint2 a2 = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(o) + base);
-            const uint2 g2 = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(dO) + base);
-            ow[0] = a2.x; ow[1] = a2.y; gw[0] = g2.x; gw[1] = g2.y;
-        } else {
-            ow[0] = *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(o) + base);
-            gw[0] = *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(dO) + base);
-        }
+    const int sub = lane / LPR, cl = lane % LPR;
+    const long long total = (long long)B * H * N_pad;
+    const long long row0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * RPW;
+    uint4 ov[NI], gv[NI];
+    bool live[NI];
 #pragma unroll
-        for (int w = 0; w < PER / 2; ++w) {
-            float a0, a1, g0, g1;
-            if (fp16) {
-                const float2 af = __half22float2(*reinterpret_cast<const __half2*>(&ow[w]));
-                const float2 gf = __half22float2(*reinterpret_cast<const __half2*>(&gw[w]));
-                a0 = af.x; a1 = af.y; g0 = gf.x; g1 = gf.y;
-            } else {
-                const float2 af = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[w]));
-                const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[w]));
-                a0 = af.x; a1 = af.y; g0 = gf.x; g1 = gf.y;
-            }
-            dsum = fmaf(a0, g0, fmaf(a1, g1, dsum));
+    for (int k = 0; k < NI; ++k) {
+        const long long row = row0 + k * RPI + sub;
+        const long long bh = row / N_pad;
+        const int i = (int)(row % N_pad);
+        live[k] = row < total && i < N_q;
+        ov[k] = make_uint4(0u, 0u, 0u, 0u);
+        gv[k] = ov[k];
+        if (live[k]) {
+            const int b = (int)(bh / H), h = (int)(bh % H);
+            const size_t base = (((size_t)b * N_q + i) * H + h) * D + (size_t)cl * 8;
+            ov[k] = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(o) + base);
+            gv[k] = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(dO) + base);
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
-        const float ls = lse[bh * N_q + i];
-        l2 = ls == -INFINITY ? INFINITY : ls * 1.4426950408889634f;
     }
-    if (lane == 0) {
-        Dvec[row] = dsum;
-        lse2[row] = l2;
+#pragma unroll
+    for (int k = 0; k < NI; ++k) {
+        const uint32_t ow[4] = {ov[k].x, ov[k].y, ov[k].z, ov[k].w};
+        const uint32_t gw[4] = {gv[k].x, gv[k].y, gv[k].z, gv[k].w};
+        float dsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            float2 af, gf;
+            if (fp16) {
+                af = __half22float2(*reinterpret_cast<const __half2*>(&ow[w]));
+                gf = __half22float2(*reinterpret_cast<const __half2*>(&gw[w]));
+            } else {
+                af = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[w]));
+                gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[w]));
+            }
+            dsum = fmaf(af.x, gf.x, fmaf(af.y, gf.y, dsum));
+        }
+        // sum over the LPR lanes of this row (an aligned group of lanes)
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+        const long long row = row0 + k * RPI + sub;
+        if (cl == 0 && row < total) {
+            const long long bh = row / N_pad;
+            const int i = (int)(row % N_pad);
+            float l2 = INFINITY;  // padding rows and rows with no key: P is exactly 0
+            if (i < N_q) {
+                const float ls = lse[bh * N_q + i];
+                l2 = ls == -INFINITY ? INFINITY : ls * 1.4426950408889634f;
+            }
+            Dvec[row] = live[k] ? dsum : 0.f;
+            lse2[row] = l2;
+        }
     }
 }
 
-// ---------------------------------------------------------------- dK, dV
 template <int D, int KIND>
 __global__ void __launch_bounds__(kThreadsKV, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -859,7 +875,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
     float* lse2 = static_cast<float*>(a.workspace);
     float* Dvec = lse2 + (size_t)a.B * a.H * N_pad;
     const long long rows = (long long)a.B * a.H * N_pad;
-    bwd_prep_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(a.o, a.dO, a.lse, lse2, Dvec, a.B,
+    bwd_prep_kernel<D><<<(unsigned)((rows + 63) / 64), 256, 0, stream>>>(a.o, a.dO, a.lse, lse2, Dvec, a.B,
                                                                       a.H, a.N_q, N_pad, KIND == kFP16);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
