@@ -308,11 +308,13 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
     constexpr int V_PER = BN * V_UNITS / 32;  // units per lane, whole tile
     // shares, in units per lane: converter warp [0, V_CONV), producer warp
     // [V_PROD0, +V_PROD), issuer t [V_ISS0 + t V_ISS, +V_ISS).  Measured on
-    // C5 (ms per call): all on the converter 0.635; converter 1/2 + issuers
-    // 1/4 each 0.605; a quarter each 0.616; issuers 1/2 each 0.734; converter
-    // 1/2, producer 1/4, issuers 1/8 each 0.581 (kept: the issuers' MMA issue
-    // tolerates little extra work).
-    constexpr int V_CONV = V_PER / 2, V_PROD = V_PER / 4, V_ISS = V_PER / 8;
+    // C5 (ms per call, units of 1/32 of a tile per warp): all on the converter
+    // 0.635; converter 16, issuers 8 each 0.605; 8 each 0.616; issuers 16
+    // each 0.734; converter 16, producer 8, issuers 4 each 0.572-0.581;
+    // converter 20, producer 8, issuers 2 each 0.567-0.571 (kept: the issuers'
+    // MMA issue tolerates little extra work); converter 24, producer 4,
+    // issuers 2 each 0.595; one-unit issuer shares 0.59-0.60.
+    constexpr int V_CONV = 5 * V_PER / 8, V_ISS = V_PER / 16, V_PROD = V_PER - V_CONV - 2 * V_ISS;
     constexpr int V_PROD0 = V_CONV, V_ISS0 = V_CONV + V_PROD;
     static_assert(V_CONV + V_PROD + 2 * V_ISS == V_PER, "the shares cover every unit");
     // Unit idx of the tile -> (row rr, 16-byte unit w of the e4m3 row),
@@ -348,7 +350,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         if (!ok) return false;
         const uint32_t src = smem_u32(sKV + (size_t)slot * C::TILE);
         const uint32_t dst = smem_u32(sV16 + (size_t)(j & 1) * C::V16T);
-        // loads in batches of 8 units (4 or 2 where the share is not a multiple of 8)
+        // loads in batches of 8 units (4, 2 or 1 where the share is not a multiple of 8)
         if ((k_end - k_begin) % 8 == 0) {
 #pragma unroll 1
             for (int k0 = k_begin; k0 < k_end; k0 += 8) {
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                     st_shared_v4(row + (uint32_t)(((u0 + 1) ^ (rr & 7)) << 4), hv[4], hv[5], hv[6], hv[7]);
                 }
             }
-        } else {
+        } else if ((k_end - k_begin) % 2 == 0) {
 #pragma unroll 1
             for (int k0 = k_begin; k0 < k_end; k0 += 2) {
                 uint32_t x[2][4];
@@ -421,6 +423,35 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                 }
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
+                    int rr, w;
+                    unit_of(lane + 32 * (k0 + k), rr, w);
+                    uint32_t hv[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        hv[2 * e] = e4m3x2_to_f16x2((uint16_t)(x[k][e] & 0xffffu));
+                        hv[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(x[k][e] >> 16));
+                    }
+                    // values d = 16 w .. 16 w + 15: fp16 chunk w / 4, units 2 (w % 4), +1
+                    const uint32_t row = dst + (uint32_t)((w >> 2) * C::V16_CHUNK + rr * C::V16_CB);
+                    const int u0 = 2 * (w & 3);
+                    st_shared_v4(row + (uint32_t)((u0 ^ (rr & 7)) << 4), hv[0], hv[1], hv[2], hv[3]);
+                    st_shared_v4(row + (uint32_t)(((u0 + 1) ^ (rr & 7)) << 4), hv[4], hv[5], hv[6], hv[7]);
+                }
+            }
+        } else {
+#pragma unroll 1
+            for (int k0 = k_begin; k0 < k_end; k0 += 1) {
+                uint32_t x[1][4];
+#pragma unroll
+                for (int k = 0; k < 1; ++k) {
+                    int rr, w;
+                    unit_of(lane + 32 * (k0 + k), rr, w);
+                    // e4m3 row rr: 128-byte swizzle (w ^ rr%8) or 64-byte (w ^ (rr/2)%4)
+                    const int wp = (C::CB == 128) ? (w ^ (rr & 7)) : (w ^ ((rr >> 1) & 3));
+                    ld_shared_v4(src + (uint32_t)(rr * C::CB + wp * 16), x[k]);
+                }
+#pragma unroll
+                for (int k = 0; k < 1; ++k) {
                     int rr, w;
                     unit_of(lane + 32 * (k0 + k), rr, w);
                     uint32_t hv[8];
