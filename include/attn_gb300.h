@@ -96,6 +96,29 @@ ATTN_API attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v,
                            int B, int H, int N_q, int N_k, int d, float scale, int causal,
                            void* stream);
 
+/* attn_fwd_fp8 with a caller workspace, for d = 64 and 128: the P V product
+ * runs on fp16 operands (fp16 P; see "FlashAttention-3 (BN)", section "Low
+ * precision (FP8) and reducing quantisation error", on FP8's accuracy cost),
+ * so every e4m3 V value must be widened to fp16 (exactly).  attn_fwd_fp8 does
+ * that on chip in every CTA that reads a V tile; here one elementwise kernel
+ * first writes the fp16 copy of v into the workspace and the attention kernel
+ * then loads fp16 V tiles directly.  The result is bit for bit that of
+ * attn_fwd_fp8 with the same arguments.
+ * workspace: device memory of at least attn_fwd_fp8_workspace_bytes(B, H, N_k,
+ * d) bytes (fp16 [B, N_k, H, d]), 16-byte aligned, overwritten; it must not
+ * overlap any argument.  d = 256 runs attn_fwd_fp8's kernel and does not use
+ * the workspace.  Errors as attn_fwd_fp8, plus ATTN_ERR_INVALID_ARG for a
+ * missing, misaligned or too small workspace. */
+ATTN_API attn_status_t attn_fwd_fp8_ws(const void* q, const void* k, const void* v, void* o,
+                                       float* lse, const float* q_descale,
+                                       const float* k_descale, const float* v_descale, int B,
+                                       int H, int N_q, int N_k, int d, float scale, int causal,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes attn_fwd_fp8_ws needs: 2 * B * N_k * H * d for d = 64 or
+ * 128, 0 for d = 256 or invalid arguments. */
+ATTN_API size_t attn_fwd_fp8_workspace_bytes(int B, int H, int N_k, int d);
+
 /* The same operation on the CUDA cores only (fp32 FMAs, no tensor cores): a
  * second, independent GPU implementation used to cross-check the tensor-core
  * path.  Descales may be NULL (unit) and are used only for ATTN_FP8_E4M3. */
@@ -291,12 +314,17 @@ ATTN_API attn_status_t attn_selftest_wait(unsigned timeout_us, void* stream);
  * attn_check_status returns ATTN_ERR_TIMEOUT and clears the status, and the
  * context stays usable.  o and lse are left with undefined contents.  Needs
  * N_q > 0 and N_k > 0 (else ATTN_ERR_INVALID_ARG); other errors as attn_fwd.
+ * workspace: NULL, or for ATTN_FP8_E4M3 at d = 64 / 128 a workspace as
+ * attn_fwd_fp8_ws takes (then that function's kernels run: the V widening in
+ * full, the attention kernel cut short); a workspace for any other dtype or d,
+ * or one that is misaligned or too small, gives ATTN_ERR_INVALID_ARG.
  * Not part of the method: a diagnostic of the failure-detection path. */
 ATTN_API attn_status_t attn_selftest_abort(const void* q, const void* k, const void* v, void* o,
                                            float* lse, const float* q_descale,
                                            const float* k_descale, const float* v_descale,
                                            int B, int H, int N_q, int N_k, int d, float scale,
-                                           int causal, attn_dtype_t dtype, unsigned timeout_us,
+                                           int causal, attn_dtype_t dtype, void* workspace,
+                                           size_t workspace_bytes, unsigned timeout_us,
                                            void* stream);
 
 /* Synchronises `stream`, then returns and clears the device status word:

@@ -20,7 +20,8 @@ import os
 
 from . import ext_build as _build
 
-__all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_simt", "attn_fwd_splitkv", "attn_fwd_gqa",
+__all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_fp8_ws", "attn_fwd_fp8_workspace_bytes",
+           "attn_fwd_simt", "attn_fwd_splitkv", "attn_fwd_gqa",
            "attn_quantize_e4m3",
            "attn_splitkv_workspace_bytes", "attn_check_status", "attn_status_string",
            "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_host", "attn_fwd_host_workspace_bytes",
@@ -64,6 +65,11 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd.restype = i
         L.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, i, i, i, i, i, f, i, vp]
         L.attn_fwd_fp8.restype = i
+        L.attn_fwd_fp8_ws.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, i, i, i, i, i, f, i, vp,
+                                      ctypes.c_size_t, vp]
+        L.attn_fwd_fp8_ws.restype = i
+        L.attn_fwd_fp8_workspace_bytes.argtypes = [i, i, i, i]
+        L.attn_fwd_fp8_workspace_bytes.restype = ctypes.c_size_t
         L.attn_fwd_simt.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, i, i, i, i, i, f, i, i, vp]
         L.attn_fwd_simt.restype = i
         sz = ctypes.c_size_t
@@ -94,7 +100,7 @@ def lib() -> ctypes.CDLL:
         L.attn_selftest_wait.argtypes = [ctypes.c_uint, vp]
         L.attn_selftest_wait.restype = i
         L.attn_selftest_abort.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, i, i, i, i, i, f, i, i,
-                                          ctypes.c_uint, vp]
+                                          vp, ctypes.c_size_t, ctypes.c_uint, vp]
         L.attn_selftest_abort.restype = i
         L.attn_check_status.argtypes = [vp]
         L.attn_check_status.restype = i
@@ -193,22 +199,50 @@ def attn_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, stream=None):
     return o, lse
 
 
+def _check_fp8(q, q_descale, k_descale, v_descale, B, H, where):
+    torch = _torch()
+    if q.dtype != torch.float8_e4m3fn:
+        raise TypeError(f"{where} takes float8_e4m3fn inputs")
+    for name, t in (("q_descale", q_descale), ("k_descale", k_descale), ("v_descale", v_descale)):
+        if not (t.is_cuda and t.dtype == torch.float32 and t.numel() == B * H and t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA float32 tensor of B*H values")
+
+
 def attn_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, o=None, lse=None, scale=None,
                  causal=False, stream=None):
     """Tensor-core forward pass on e4m3 codes with per-(batch, head) fp32 descales [B, H]."""
     B, N_q, H, d, N_k = _check_inputs(q, k, v)
-    torch = _torch()
-    if q.dtype != torch.float8_e4m3fn:
-        raise TypeError("attn_fwd_fp8 takes float8_e4m3fn inputs")
-    for name, t in (("q_descale", q_descale), ("k_descale", k_descale), ("v_descale", v_descale)):
-        if not (t.is_cuda and t.dtype == torch.float32 and t.numel() == B * H and t.is_contiguous()):
-            raise ValueError(f"{name} must be a contiguous CUDA float32 tensor of B*H values")
+    _check_fp8(q, q_descale, k_descale, v_descale, B, H, "attn_fwd_fp8")
     o, lse = _outputs(q, o, lse, B, N_q, H, d)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     st = lib().attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(q_descale),
                             _ptr(k_descale), _ptr(v_descale), B, H, N_q, N_k, d, scale,
                             int(bool(causal)), _stream(stream, q.device))
     _raise(st, "attn_fwd_fp8")
+    return o, lse
+
+
+def attn_fwd_fp8_workspace_bytes(B, H, N_k, d) -> int:
+    return int(lib().attn_fwd_fp8_workspace_bytes(B, H, N_k, d))
+
+
+def attn_fwd_fp8_ws(q, k, v, q_descale, k_descale, v_descale, o=None, lse=None, scale=None,
+                    causal=False, workspace=None, stream=None):
+    """attn_fwd_fp8 with V widened to fp16 once into a workspace (allocated when not
+    given) before the attention kernel; the same result bit for bit."""
+    B, N_q, H, d, N_k = _check_inputs(q, k, v)
+    _check_fp8(q, q_descale, k_descale, v_descale, B, H, "attn_fwd_fp8_ws")
+    o, lse = _outputs(q, o, lse, B, N_q, H, d)
+    need = attn_fwd_fp8_workspace_bytes(B, H, N_k, d)
+    if workspace is None and need > 0:
+        workspace = _torch().empty(need, dtype=_torch().uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib().attn_fwd_fp8_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(q_descale),
+                               _ptr(k_descale), _ptr(v_descale), B, H, N_q, N_k, d, scale,
+                               int(bool(causal)), _ptr(workspace), ws_bytes,
+                               _stream(stream, q.device))
+    _raise(st, "attn_fwd_fp8_ws")
     return o, lse
 
 
@@ -383,17 +417,19 @@ def attn_selftest_wait(timeout_us=1000, stream=None, device=None):
 
 
 def attn_selftest_abort(q, k, v, q_descale=None, k_descale=None, v_descale=None, scale=None,
-                        causal=False, timeout_us=500, stream=None):
+                        causal=False, timeout_us=500, workspace=None, stream=None):
     """Run the attention kernel with its K/V loader stopped after the first
     tile and every wait limited to timeout_us: the abort path's health check.
+    With a workspace (e4m3, d = 64 / 128) attn_fwd_fp8_ws's kernels run.
     The next attn_check_status raises AttnError(ATTN_ERR_TIMEOUT)."""
     B, N_q, H, d, N_k = _check_inputs(q, k, v)
     o, lse = _outputs(q, None, None, B, N_q, H, d)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib().attn_selftest_abort(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(q_descale),
                                    _ptr(k_descale), _ptr(v_descale), B, H, N_q, N_k, d, scale,
-                                   int(bool(causal)), _dtype_code(q), int(timeout_us),
-                                   _stream(stream, q.device))
+                                   int(bool(causal)), _dtype_code(q), _ptr(workspace), ws_bytes,
+                                   int(timeout_us), _stream(stream, q.device))
     _raise(st, "attn_selftest_abort")
 
 

@@ -103,6 +103,31 @@ attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
     return run_tc(p, static_cast<cudaStream_t>(stream));
 }
 
+size_t attn_fwd_fp8_workspace_bytes(int B, int H, int N_k, int d) {
+    if (B < 0 || H < 0 || N_k < 0) return 0;
+    return attn::fp8_ws_workspace_bytes(B, H, N_k, d);
+}
+
+attn_status_t attn_fwd_fp8_ws(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const float* q_descale, const float* k_descale,
+                              const float* v_descale, int B, int H, int N_q, int N_k, int d,
+                              float scale, int causal, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+    attn::Problem p = make_problem(q, k, v, o, lse, q_descale, k_descale, v_descale, B, H, N_q,
+                                   N_k, d, scale, causal, attn::kE4M3);
+    attn_status_t st = validate(p);
+    if (st != ATTN_OK || is_empty(p)) return st;
+    if (!q_descale || !k_descale || !v_descale) return ATTN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (d == 256) return run_tc(p, s);  // widens V on chip; the workspace is not used
+    const size_t need = attn::fp8_ws_workspace_bytes(B, H, N_k, d);
+    if (need > 0 && (!workspace || !aligned(workspace, 16) || workspace_bytes < need))
+        return ATTN_ERR_INVALID_ARG;
+    cudaError_t e = attn::launch_tc_fp8_ws(p, workspace, workspace_bytes, s);
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    return from_cuda(e);
+}
+
 attn_status_t attn_fwd_simt(const void* q, const void* k, const void* v, void* o, float* lse,
                             const float* q_descale, const float* k_descale,
                             const float* v_descale, int B, int H, int N_q, int N_k, int d,
@@ -252,8 +277,8 @@ attn_status_t attn_selftest_wait(unsigned timeout_us, void* stream) {
 attn_status_t attn_selftest_abort(const void* q, const void* k, const void* v, void* o,
                                   float* lse, const float* q_descale, const float* k_descale,
                                   const float* v_descale, int B, int H, int N_q, int N_k, int d,
-                                  float scale, int causal, attn_dtype_t dtype, unsigned timeout_us,
-                                  void* stream) {
+                                  float scale, int causal, attn_dtype_t dtype, void* workspace,
+                                  size_t workspace_bytes, unsigned timeout_us, void* stream) {
     if (timeout_us == 0 || timeout_us > 10u * 1000u * 1000u) return ATTN_ERR_INVALID_ARG;
     attn::Problem p = make_problem(q, k, v, o, lse, q_descale, k_descale, v_descale, B, H, N_q,
                                    N_k, d, scale, causal, (int)dtype);
@@ -261,9 +286,17 @@ attn_status_t attn_selftest_abort(const void* q, const void* k, const void* v, v
     if (st != ATTN_OK) return st;
     // the check needs work to cut short: at least one query row and one key
     if (is_empty(p) || N_k == 0) return ATTN_ERR_INVALID_ARG;
+    // with a workspace, e4m3 at d = 64 / 128 runs attn_fwd_fp8_ws's kernels
+    const bool ws = workspace != nullptr && dtype == ATTN_FP8_E4M3 && (d == 64 || d == 128);
+    if (workspace && !ws) return ATTN_ERR_INVALID_ARG;
+    if (ws && (!aligned(workspace, 16) ||
+               workspace_bytes < attn::fp8_ws_workspace_bytes(B, H, N_k, d)))
+        return ATTN_ERR_INVALID_ARG;
     p.selftest_wait_ns = 1000ull * timeout_us;
     p.selftest_items = 1;  // the loader stops after the first K/V ring item
-    cudaError_t e = attn::launch_tc(p, static_cast<cudaStream_t>(stream));
+    cudaError_t e = ws ? attn::launch_tc_fp8_ws(p, workspace, workspace_bytes,
+                                                static_cast<cudaStream_t>(stream))
+                       : attn::launch_tc(p, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) (void)cudaGetLastError();
     return from_cuda(e);
 }

@@ -87,6 +87,11 @@ void note_cuda_error(cudaError_t e);
 
 // Split-KV on the tensor-core kernel plus the combine kernel (attn_tc.cu).
 constexpr int kMaxSplits = 32;
+// e4m3 forward whose V is first widened to fp16 in the caller's workspace
+// (B * N_k * H_kv * d fp16 values; d = 64 or 128, else 0 bytes / unsupported).
+size_t fp8_ws_workspace_bytes(long long B, long long H_kv, long long N_k, int d);
+cudaError_t launch_tc_fp8_ws(const Problem& p, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream);
 size_t splitkv_workspace_bytes(long long B, long long H, long long N_q, int d, int n_splits);
 cudaError_t launch_tc_splitkv(const Problem& p, int n_splits, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream);

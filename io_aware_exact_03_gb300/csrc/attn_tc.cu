@@ -51,6 +51,11 @@ using namespace ptx;
 
 __device__ unsigned g_tc_status = 0;
 
+// Kernel variant of e4m3 inputs whose V arrives already widened to fp16 (the
+// host runs widen_e4m3_kernel into the caller's workspace first): Q and K are
+// e4m3 as in kE4M3, V tiles come into the ring by TMA as fp16.
+constexpr int kE4M3_V16 = 16;
+
 constexpr int BM = 128;        // query rows per tile (MMA M)
 constexpr int BN = 128;        // keys per tile (MMA N of Q K^T, K of P V)
 constexpr uint32_t kTmemCols = 512;
@@ -58,7 +63,8 @@ constexpr int kSmemLimit = 232448;  // max dynamic shared memory per CTA
 
 template <int D, int KIND>
 struct Cfg {
-    static constexpr int E = (KIND == kE4M3) ? 1 : 2;     // bytes per element
+    static constexpr bool E4 = (KIND == kE4M3 || KIND == kE4M3_V16);  // e4m3 Q and K
+    static constexpr int E = E4 ? 1 : 2;                   // bytes per element of Q, K
     static constexpr int RB = D * E;                       // bytes per row
     static constexpr int CB = RB >= 128 ? 128 : RB;        // bytes per swizzle chunk
     static constexpr int NC = RB / CB;                     // chunks per row
@@ -76,7 +82,10 @@ struct Cfg {
     // buffer S shared by the two tiles (each tile's softmax frees it as soon as
     // it has loaded its scores, and the two issuers take turns), P_A, P_B
     // (64 columns each) and O_A, O_B.
-    static constexpr bool F16P = (KIND == kE4M3);
+    static constexpr bool F16P = E4;
+    // V as fp16 from global memory (kE4M3_V16): no widening on chip, no
+    // converter warp; the ring's slots are sized for the larger fp16 V tile.
+    static constexpr bool V16G = (KIND == kE4M3_V16);
     // P_t in shared memory (K-major, 128-byte swizzle) instead of over S_t in
     // TMEM (16-bit types at d = 64): S_t is free as soon as the softmax has
     // loaded it, so the next Q K^T runs while the softmax works.  The cost is
@@ -93,10 +102,10 @@ struct Cfg {
     // 16-bit inputs: the O tile (bf16 / fp16) is exactly a Q tile, so the
     // epilogue stages O in the tile's own Q buffer (free once its last P V is
     // done) and writes it with one TMA store.
-    static constexpr bool TMA_O = (KIND != kE4M3);
+    static constexpr bool TMA_O = !E4;
     static constexpr int SOFTMAX_WARP0 = 1 + ISSUERS;
     static constexpr int CONVERTER_WARP = SOFTMAX_WARP0 + 8;
-    static constexpr int THREADS = 32 * (SOFTMAX_WARP0 + 8 + (F16P ? 1 : 0));
+    static constexpr int THREADS = 32 * (SOFTMAX_WARP0 + 8 + (F16P && !V16G ? 1 : 0));
     static constexpr int PT = P_SMEM ? BM * BN * E : 0;    // bytes of one P tile in smem
     static constexpr int P_CHUNK = BM * 128;               // bytes of a 128-byte-wide P chunk
     // fp16 copy of one V tile (F16P): 128 keys x D, 128-byte swizzled chunks
@@ -104,21 +113,28 @@ struct Cfg {
     static constexpr int V16_CB = 2 * D >= 128 ? 128 : 2 * D;
     static constexpr int V16_CHUNK = BN * V16_CB;
     static constexpr int V16T = F16P ? BN * 2 * D : 0;
+    static constexpr int V16_NC = 2 * D / V16_CB;          // 128-byte chunks per fp16 V row
+    // the two fp16 V buffers widened on chip (kE4M3 only)
+    static constexpr int V16BUF = (F16P && !V16G) ? V16T : 0;
+    // bytes per ring slot: a K or V tile of the input type, or (V16G) the
+    // larger of an e4m3 K tile and an fp16 V tile
+    static constexpr int SLOT = (V16G && V16T > TILE) ? V16T : TILE;
     // q_full, s_full x2, p_full x2, pv_done x2, drain, s_free x2, drain of
     // issuer B, v16_full x2, v16_empty x2
     static constexpr int NB_FIXED = 1 + 2 + 2 + 2 + 1 + 2 + 1 + 4;
     static constexpr int SLOTS_FIT =
-        (kSmemLimit - 1024 - 2 * TILE - 2 * PT - 2 * V16T - 512) / TILE;
+        (kSmemLimit - 1024 - 2 * TILE - 2 * PT - 2 * V16BUF - 512) / SLOT;
     // K/V ring depth; F16P needs it even (K items in even slots, V in odd)
     static constexpr int SLOTS = (SLOTS_FIT > 8 ? 8 : SLOTS_FIT) & (F16P ? ~1 : ~0);
     static constexpr uint32_t LAYOUT = (CB == 128) ? 2u : 4u;  // 128B / 64B swizzle
     static constexpr int MMA_K = 32 / E;                   // K per Q K^T MMA instruction
     static constexpr int NB = NB_FIXED + 2 * SLOTS;        // mbarriers
     static constexpr size_t SMEM_USED =
-        1024 + (size_t)TILE * (2 + SLOTS) + 2 * PT + 2 * (size_t)V16T + NB * 8 + 16;
+        1024 + (size_t)TILE * 2 + (size_t)SLOT * SLOTS + 2 * PT + 2 * (size_t)V16BUF + NB * 8 + 16;
     // at least ~120 KB so two CTAs never share an SM (each takes all of TMEM)
     static constexpr size_t SMEM = SMEM_USED > 122880 ? SMEM_USED : 122880;
     static constexpr uint32_t FMT = (KIND == kBF16) ? 1u : 0u;  // bf16 = 1, f16 / e4m3 = 0
+    static_assert(!V16G || D <= 128, "fp16 V from global memory: d = 64 or 128");
     static constexpr uint32_t IDESC_QK = instr_desc(FMT, FMT, 0, 0, BM, BN);
     // P V: 16-bit operands (F16P: fp16 P and fp16 V)
     static constexpr uint32_t IDESC_PV = instr_desc(F16P ? 0u : FMT, F16P ? 0u : FMT, 0, 1, BM, D);
@@ -195,9 +211,9 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sQ = smem;                      // two tiles: A then B
     uint8_t* sP = smem + 2 * C::TILE;        // two P tiles (P_SMEM only)
-    uint8_t* sV16 = sP + 2 * C::PT;          // two fp16 V tiles (F16P only)
-    uint8_t* sKV = sV16 + 2 * C::V16T;       // SLOTS tiles
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + (size_t)C::SLOTS * C::TILE);
+    uint8_t* sV16 = sP + 2 * C::PT;          // two fp16 V tiles (F16P without V16G)
+    uint8_t* sKV = sV16 + 2 * C::V16BUF;     // SLOTS slots of C::SLOT bytes
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + (size_t)C::SLOTS * C::SLOT);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NB);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -274,8 +290,9 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         for (int s = 0; s < C::SLOTS; ++s) {
             mbar_init(b_kv_full + 8 * s, 1);
             // one release per issuer that reads the ring; F16P: V items (odd
-            // slots) are read only by the converter
-            mbar_init(b_kv_empty + 8 * s, (C::F16P && (s & 1)) ? 4 : C::ISSUERS);
+            // slots) are released by the four warps that widen them (V16G:
+            // read by both issuers' P V MMAs, like the K items)
+            mbar_init(b_kv_empty + 8 * s, (C::F16P && !C::V16G && (s & 1)) ? 4 : C::ISSUERS);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -348,8 +365,8 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             ok = __all_sync(0xffffffffu, wait_bar(b_v16_empty + 8 * (j & 1), ((uint32_t)(j >> 1) & 1u) ^ 1u,
                                                   abort_flag, lim));
         if (!ok) return false;
-        const uint32_t src = smem_u32(sKV + (size_t)slot * C::TILE);
-        const uint32_t dst = smem_u32(sV16 + (size_t)(j & 1) * C::V16T);
+        const uint32_t src = smem_u32(sKV + (size_t)slot * C::SLOT);
+        const uint32_t dst = smem_u32(sV16 + (size_t)(j & 1) * C::V16BUF);
         // loads in batches of 8 units (4, 2 or 1 where the share is not a multiple of 8)
         if ((k_end - k_begin) % 8 == 0) {
 #pragma unroll 1
@@ -477,7 +494,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        if constexpr (C::F16P) {
+        if constexpr (C::F16P && !C::V16G) {
             // The whole warp runs the loop (lane 0 issues the copies) and also
             // widens its share of every V tile: its share of V_c right after
             // V_{c+LAG}'s load has gone out.  LAG must stay below the ring's
@@ -509,7 +526,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                     if (lane == 0) {
                         mbar_arrive_expect_tx(b_kv_full + 8 * slot, C::TILE);
                         const CUtensorMap* tm = (it & 1) ? &tmV : &tmK;
-                        uint8_t* dst = sKV + (size_t)slot * C::TILE;
+                        uint8_t* dst = sKV + (size_t)slot * C::SLOT;
                         for (int c = 0; c < C::NC; ++c)
                             tma_load_4d(smem_u32(dst + c * C::CHUNK), tm, b_kv_full + 8 * slot,
                                         c * (C::CB / C::E), h_kv, (j0 + (it >> 1)) * BN, b);
@@ -546,12 +563,20 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(b_kv_full + 8 * slot, C::TILE);
-                    const CUtensorMap* tm = (it & 1) ? &tmV : &tmK;
-                    uint8_t* dst = sKV + (size_t)slot * C::TILE;
-                    for (int c = 0; c < C::NC; ++c)
-                        tma_load_4d(smem_u32(dst + c * C::CHUNK), tm, b_kv_full + 8 * slot,
-                                    c * (C::CB / C::E), h_kv, (j0 + (it >> 1)) * BN, b);
+                    uint8_t* dst = sKV + (size_t)slot * C::SLOT;
+                    if (C::V16G && (it & 1)) {
+                        // fp16 V tile: V16_NC chunks of 64 values
+                        mbar_arrive_expect_tx(b_kv_full + 8 * slot, C::V16T);
+                        for (int c = 0; c < C::V16_NC; ++c)
+                            tma_load_4d(smem_u32(dst + c * C::V16_CHUNK), &tmV, b_kv_full + 8 * slot,
+                                        c * (C::V16_CB / 2), h_kv, (j0 + (it >> 1)) * BN, b);
+                    } else {
+                        mbar_arrive_expect_tx(b_kv_full + 8 * slot, C::TILE);
+                        const CUtensorMap* tm = (it & 1) ? &tmV : &tmK;
+                        for (int c = 0; c < C::NC; ++c)
+                            tma_load_4d(smem_u32(dst + c * C::CHUNK), tm, b_kv_full + 8 * slot,
+                                        c * (C::CB / C::E), h_kv, (j0 + (it >> 1)) * BN, b);
+                    }
                 }
                 if (!ok) {
                     // let every load already issued land before the CTA can exit
@@ -574,7 +599,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                 // descriptors of the tile bases; each MMA adds its byte offset / 16
                 const uint64_t qd = smem_desc(smem_u32(sQ + t * C::TILE), 16, 8 * C::CB, C::LAYOUT);
                 const uint64_t kd =
-                    smem_desc(smem_u32(sKV + (size_t)slot * C::TILE), 16, 8 * C::CB, C::LAYOUT);
+                    smem_desc(smem_u32(sKV + (size_t)slot * C::SLOT), 16, 8 * C::CB, C::LAYOUT);
 #pragma unroll
                 for (int c = 0; c < C::NC; ++c) {
 #pragma unroll
@@ -583,7 +608,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                         const uint64_t da = qd + off16;
                         const uint64_t db = kd + off16;
                         const uint32_t acc = (c | ks) != 0;
-                        if constexpr (KIND == kE4M3)
+                        if constexpr (C::E4)
                             mma_f8_ss_1(tmem + col_s<C::F16P>(t), da, db, C::IDESC_QK, acc);
                         else
                             mma_f16_ss_1(tmem + col_s<C::F16P>(t), da, db, C::IDESC_QK, acc);
@@ -593,10 +618,12 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             auto issue_pv = [&](int t, int slot, bool first) {
                 if constexpr (C::F16P) {
                     // A = fp16 P_t in TMEM (8 columns per 16 keys); B = the fp16
-                    // V tile in buffer `slot`, MN-major: 8-key groups 8*128
-                    // bytes apart, 64-value d-chunks V16_CHUNK apart
-                    const uint64_t vd = smem_desc(smem_u32(sV16 + (size_t)slot * C::V16T),
-                                                  C::V16_CHUNK, 8 * C::V16_CB, 2u);
+                    // V tile in buffer `slot` (V16G: in ring slot `slot`),
+                    // MN-major: 8-key groups 8*128 bytes apart, 64-value
+                    // d-chunks V16_CHUNK apart
+                    const uint8_t* vt = C::V16G ? sKV + (size_t)slot * C::SLOT
+                                                : sV16 + (size_t)slot * C::V16BUF;
+                    const uint64_t vd = smem_desc(smem_u32(vt), C::V16_CHUNK, 8 * C::V16_CB, 2u);
 #pragma unroll
                     for (int ks = 0; ks < BN / C::PV_K; ++ks) {
                         const uint64_t db = vd + ((uint32_t)(ks * C::PV_K * C::V16_CB) >> 4);
@@ -608,7 +635,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                 }
                 // V is MN-major: 8-key groups 8*CB apart, d-chunks CHUNK apart
                 const uint64_t vd =
-                    smem_desc(smem_u32(sKV + (size_t)slot * C::TILE), C::CHUNK, 8 * C::CB, C::LAYOUT);
+                    smem_desc(smem_u32(sKV + (size_t)slot * C::SLOT), C::CHUNK, 8 * C::CB, C::LAYOUT);
 #pragma unroll
                 for (int ks = 0; ks < BN / C::MMA_K; ++ks) {
                     const uint64_t db = vd + ((uint32_t)(ks * C::MMA_K * C::CB) >> 4);
@@ -637,6 +664,8 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                 // (s_free).  P_t V_j reads fp16 P_t from TMEM and the fp16 copy
                 // of V_j in buffer j % 2 (widened by the converter warp and both
                 // issuers); the buffer is released when the MMA has read it.
+                // V16G: the fp16 V_j is ring item 2j + 1 itself, released to the
+                // producer by both issuers' P V commits, like K_j.
                 // Key tiles this tile never reads release their K slot and V
                 // buffer once filled (and still get this issuer's share of V).
                 const int t = __shfl_sync(0xffffffffu, warp, 0) - 1;
@@ -671,7 +700,8 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                         mma_commit_1(b_kv_empty + 8 * slot_of(0));
                     }
                 }
-                if (ok && n_max > 0) ok = widen_share(0, vk0, vk1);
+                if constexpr (!C::V16G)
+                    if (ok && n_max > 0) ok = widen_share(0, vk0, vk1);
                 for (int j = 0; j < nt && ok; ++j) {
                     const int itK = 2 * j + 2;
                     if (j + 1 < nt) {
@@ -683,22 +713,35 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                         mma_commit_1(b_s_full + 8 * t);
                         mma_commit_1(b_kv_empty + 8 * slot_of(itK));
                     }
-                    ok = wb(b_v16_full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u);
+                    const int itV = 2 * j + 1;
+                    if constexpr (C::V16G)
+                        ok = wb(b_kv_full + 8 * slot_of(itV), par_of(itV));
+                    else
+                        ok = wb(b_v16_full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u);
                     if (ok) ok = wb(b_p_full + 8 * t, (uint32_t)j & 1u);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_pv(t, j & 1, j == 0);
+                    issue_pv(t, C::V16G ? slot_of(itV) : (j & 1), j == 0);
                     mma_commit_1(b_pv_done + 8 * t);
-                    mma_commit_1(b_v16_empty + 8 * (j & 1));
-                    // the MMAs run on their own: widen this issuer's share of the next V
-                    if (j + 1 < n_max) ok = widen_share(j + 1, vk0, vk1);
+                    if constexpr (C::V16G) {
+                        mma_commit_1(b_kv_empty + 8 * slot_of(itV));
+                    } else {
+                        mma_commit_1(b_v16_empty + 8 * (j & 1));
+                        // the MMAs run on their own: widen this issuer's share of the next V
+                        if (j + 1 < n_max) ok = widen_share(j + 1, vk0, vk1);
+                    }
                 }
                 for (int j = nt; j < n_max && ok; ++j) {
                     ok = wb(b_kv_full + 8 * slot_of(2 * j), par_of(2 * j));
                     if (ok) mbar_arrive_1(b_kv_empty + 8 * slot_of(2 * j));
-                    if (ok) ok = wb(b_v16_full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u);
-                    if (ok) mbar_arrive_1(b_v16_empty + 8 * (j & 1));
-                    if (ok && j + 1 < n_max) ok = widen_share(j + 1, vk0, vk1);
+                    if constexpr (C::V16G) {
+                        if (ok) ok = wb(b_kv_full + 8 * slot_of(2 * j + 1), par_of(2 * j + 1));
+                        if (ok) mbar_arrive_1(b_kv_empty + 8 * slot_of(2 * j + 1));
+                    } else {
+                        if (ok) ok = wb(b_v16_full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u);
+                        if (ok) mbar_arrive_1(b_v16_empty + 8 * (j & 1));
+                        if (ok && j + 1 < n_max) ok = widen_share(j + 1, vk0, vk1);
+                    }
                 }
                 if (!ok) {
                     // make sure none of this issuer's MMAs still runs when TMEM is freed
@@ -812,7 +855,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (C::F16P && warp == C::CONVERTER_WARP) {
+    } else if (C::F16P && !C::V16G && warp == C::CONVERTER_WARP) {
         // ------------------------------------------- V converter (F16P only)
         // Its share of every V tile's units (producer and issuers take the rest).
         for (int j = 0; j < n_max; ++j)
@@ -833,7 +876,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         // tiles with any column beyond the tile's first row's limit need a mask
         const int tile_lim = p.causal ? min(p.N_k - 1, q0[t] + shift) : p.N_k - 1;
         float dq = 1.f, dk = 1.f, dv = 1.f;
-        if (KIND == kE4M3) {
+        if (C::E4) {
             if (p.q_descale) dq = p.q_descale[bh];
             if (p.k_descale) dk = p.k_descale[b * p.H_kv + h_kv];
             if (p.v_descale) dv = p.v_descale[b * p.H_kv + h_kv];
@@ -1006,7 +1049,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         // rows leave as whole 128-byte lines (stored from registers, each warp
         // store instruction touched 32 rows 4 KB apart).  Q_t is no longer
         // read: this issuer's pv_done covers its last score MMA.
-        constexpr bool STAGE_O8 = (KIND == kE4M3 && D == 128);
+        constexpr bool STAGE_O8 = (C::E4 && D == 128);
         if (STAGE_O8 && p.n_splits == 1) {
             const bool valid = row_g < p.N_q;
             const float inv = l > 0.f ? dv / l : 0.f;
@@ -1219,26 +1262,50 @@ __global__ void __launch_bounds__(256) splitkv_combine_kernel(const float* __res
     if (lane == 0 && lse) lse[(size_t)bh * N_q + i] = tot > 0.f ? mx + __logf(tot) : -INFINITY;
 }
 
+// V for kE4M3_V16: e4m3 codes -> fp16 values, 16 codes per thread and step
+// (exact: every e4m3 value is an fp16 value).  n16 = element count / 16.
+__global__ void __launch_bounds__(256) widen_e4m3_kernel(const uint4* __restrict__ v,
+                                                         uint4* __restrict__ v16, long long n16) {
+    for (long long i = (long long)blockIdx.x * 256 + threadIdx.x; i < n16;
+         i += (long long)gridDim.x * 256) {
+        const uint4 x = v[i];
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t hv[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            hv[2 * e] = e4m3x2_to_f16x2((uint16_t)(w[e] & 0xffffu));
+            hv[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(w[e] >> 16));
+        }
+        v16[2 * i] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        v16[2 * i + 1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+    }
+}
+
 // ------------------------------------------------------------------- host side
 template <int D, int KIND>
 cudaError_t launch_t(const Problem& pr, cudaStream_t stream, int n_splits = 1,
-                     float* part_o = nullptr, float* part_lse = nullptr) {
+                     float* part_o = nullptr, float* part_lse = nullptr,
+                     const void* v16 = nullptr) {
     using C = Cfg<D, KIND>;
     CUtensorMap mq, mk, mv, mo;
     const int ce = C::CB / C::E;
+    const int dt = C::E4 ? (int)kE4M3 : KIND;  // element type of Q and K
     // O has the layout of Q; for 16-bit inputs also its element size
     // e4m3 at d = 128: O is bf16, 64-column chunks staged in the Q buffer
-    const bool o8 = KIND == kE4M3 && D == 128 && n_splits == 1;
+    const bool o8 = C::E4 && D == 128 && n_splits == 1;
     if (C::TMA_O && n_splits == 1) {
-        if (!tma::encode_map(&mo, pr.o, KIND, pr.B, pr.N_q, pr.H, D, ce, BM))
+        if (!tma::encode_map(&mo, pr.o, dt, pr.B, pr.N_q, pr.H, D, ce, BM))
             return cudaErrorInvalidValue;
     } else if (o8) {
         if (!tma::encode_map(&mo, pr.o, kBF16, pr.B, pr.N_q, pr.H, D, 64, BM))
             return cudaErrorInvalidValue;
     }
-    if (!tma::encode_map(&mq, pr.q, KIND, pr.B, pr.N_q, pr.H, D, ce, BM) ||
-        !tma::encode_map(&mk, pr.N_k > 0 ? pr.k : pr.q, KIND, pr.B, pr.N_k, pr.H_kv, D, ce, BN) ||
-        !tma::encode_map(&mv, pr.N_k > 0 ? pr.v : pr.q, KIND, pr.B, pr.N_k, pr.H_kv, D, ce, BN))
+    if (C::V16G && pr.N_k > 0 && !v16) return cudaErrorInvalidValue;
+    const void* vsrc = pr.N_k == 0 ? pr.q : (C::V16G ? v16 : pr.v);
+    if (!tma::encode_map(&mq, pr.q, dt, pr.B, pr.N_q, pr.H, D, ce, BM) ||
+        !tma::encode_map(&mk, pr.N_k > 0 ? pr.k : pr.q, dt, pr.B, pr.N_k, pr.H_kv, D, ce, BN) ||
+        !(C::V16G ? tma::encode_map(&mv, vsrc, kFP16, pr.B, pr.N_k, pr.H_kv, D, C::V16_CB / 2, BN)
+                  : tma::encode_map(&mv, vsrc, dt, pr.B, pr.N_k, pr.H_kv, D, ce, BN)))
         return cudaErrorInvalidValue;
     TcParams p;
     p.B = pr.B;
@@ -1266,7 +1333,7 @@ cudaError_t launch_t(const Problem& pr, cudaStream_t stream, int n_splits = 1,
     // K/V head shared by H / H_kv query heads) fill ~48 MiB of L2.  The groups
     // are then evened out so the last one is not a lone small group that
     // would run by itself at the end.
-    const long long kv_head_bytes = 2LL * (pr.N_k > 0 ? pr.N_k : 1) * D * C::E;
+    const long long kv_head_bytes = (long long)(pr.N_k > 0 ? pr.N_k : 1) * D * (C::V16G ? 3 : 2 * C::E);
     long long G = (48LL << 20) * (pr.H / pr.H_kv) / kv_head_bytes;
     if (G < 1) G = 1;
     if (G > n_bh) G = n_bh;
@@ -1304,6 +1371,29 @@ cudaError_t launch_tc(const Problem& p, cudaStream_t stream) {
             break;
     }
     return cudaErrorNotSupported;
+}
+
+size_t fp8_ws_workspace_bytes(long long B, long long H_kv, long long N_k, int d) {
+    if (d != 64 && d != 128) return 0;
+    return (size_t)(B * N_k * H_kv) * (size_t)d * 2;
+}
+
+cudaError_t launch_tc_fp8_ws(const Problem& p, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream) {
+    if (p.dtype != kE4M3 || (p.d != 64 && p.d != 128)) return cudaErrorNotSupported;
+    if (workspace_bytes < fp8_ws_workspace_bytes(p.B, p.H_kv, p.N_k, p.d))
+        return cudaErrorInvalidValue;
+    const long long n16 = (long long)p.B * p.N_k * p.H_kv * p.d / 16;
+    if (n16 > 0) {
+        const long long want = (n16 + 255) / 256;
+        const unsigned blocks = (unsigned)(want < 152LL * 16 ? want : 152LL * 16);
+        widen_e4m3_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(p.v),
+                                                     static_cast<uint4*>(workspace), n16);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (p.d == 64) return launch_t<64, kE4M3_V16>(p, stream, 1, nullptr, nullptr, workspace);
+    return launch_t<128, kE4M3_V16>(p, stream, 1, nullptr, nullptr, workspace);
 }
 
 size_t splitkv_workspace_bytes(long long B, long long H, long long N_q, int d, int n_splits) {

@@ -42,6 +42,9 @@ def run_gpu(case: synthetic.Case, dev: dict, impl: str = "tc"):
                                        dev["v_descale"], **kw)
         else:
             o, lse = attn.attn_fwd(q, k, v, **kw)
+    elif impl == "fp8ws":
+        o, lse = attn.attn_fwd_fp8_ws(q, k, v, dev["q_descale"], dev["k_descale"],
+                                      dev["v_descale"], **kw)
     elif impl == "gqa":
         o, lse = attn.attn_fwd_gqa(q, k, v, q_descale=dev.get("q_descale"),
                                    k_descale=dev.get("k_descale"),

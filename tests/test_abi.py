@@ -120,6 +120,33 @@ def test_splitkv_workspace_size(L):
     assert L.attn_splitkv_workspace_bytes(2, 3, 100, 64, 33) == 0
 
 
+def test_fp8_ws_workspace_size(L):
+    # the fp16 copy of v: 2 * B * N_k * H * d bytes for d = 64 / 128, else 0
+    assert L.attn_fwd_fp8_workspace_bytes(2, 16, 8192, 128) == 2 * 2 * 8192 * 16 * 128
+    assert L.attn_fwd_fp8_workspace_bytes(3, 5, 129, 64) == 2 * 3 * 129 * 5 * 64
+    assert L.attn_fwd_fp8_workspace_bytes(2, 8, 8192, 256) == 0
+    assert L.attn_fwd_fp8_workspace_bytes(1, 1, 16, 96) == 0
+    assert L.attn_fwd_fp8_workspace_bytes(-1, 1, 16, 64) == 0
+    assert L.attn_fwd_fp8_workspace_bytes(1, 1, 0, 64) == 0
+
+
+def test_fp8_ws_rejects_bad_arguments(L):
+    # every check below returns before anything is launched
+    need = L.attn_fwd_fp8_workspace_bytes(1, 1, 16, 64)
+    base = (P, P, P, P, P)
+    args = (1, 1, 16, 16, 64, 0.125, 0)
+    ok_ds = (P, P, P)
+    assert L.attn_fwd_fp8_ws(*base, *ok_ds, *args, None, need, None) == attn.ATTN_ERR_INVALID_ARG
+    assert L.attn_fwd_fp8_ws(*base, *ok_ds, *args, P, need - 1, None) == attn.ATTN_ERR_INVALID_ARG
+    assert L.attn_fwd_fp8_ws(*base, *ok_ds, *args, P + 8, need, None) == attn.ATTN_ERR_INVALID_ARG
+    assert L.attn_fwd_fp8_ws(*base, None, P, P, *args, P, need, None) == attn.ATTN_ERR_INVALID_ARG
+    assert L.attn_fwd_fp8_ws(*base, *ok_ds, 1, 1, 16, 16, 96, 0.125, 0, P, need,
+                             None) == attn.ATTN_ERR_UNSUPPORTED
+    # nothing to compute: returns at once, workspace or not
+    assert L.attn_fwd_fp8_ws(*base, *ok_ds, 0, 1, 16, 16, 64, 0.125, 0, None, 0,
+                             None) == attn.ATTN_OK
+
+
 def test_splitkv_rejects_bad_workspace(L):
     need = L.attn_splitkv_workspace_bytes(1, 1, 16, 64, 4)
     args = (P, P, P, P, P, None, None, None, 1, 1, 16, 16, 64, 0.125, 0, 0)
@@ -134,11 +161,20 @@ def test_selftest_wait_rejects_bad_limits(L):
     # the abort-path check: limit out of range, or nothing to cut short
     fp = ctypes.c_void_p(P)
     assert L.attn_selftest_abort(fp, fp, fp, fp, None, None, None, None, 1, 1, 128, 128, 64,
-                                 0.125, 0, attn.ATTN_BF16, 0, None) == attn.ATTN_ERR_INVALID_ARG
+                                 0.125, 0, attn.ATTN_BF16, None, 0, 0, None) == attn.ATTN_ERR_INVALID_ARG
     assert L.attn_selftest_abort(fp, fp, fp, fp, None, None, None, None, 1, 1, 128, 0, 64,
-                                 0.125, 0, attn.ATTN_BF16, 500, None) == attn.ATTN_ERR_INVALID_ARG
+                                 0.125, 0, attn.ATTN_BF16, None, 0, 500, None) == attn.ATTN_ERR_INVALID_ARG
     assert L.attn_selftest_abort(fp, fp, fp, fp, None, None, None, None, 1, 1, 128, 128, 96,
-                                 0.125, 0, attn.ATTN_BF16, 500, None) == attn.ATTN_ERR_UNSUPPORTED
+                                 0.125, 0, attn.ATTN_BF16, None, 0, 500, None) == attn.ATTN_ERR_UNSUPPORTED
+    # a workspace only for e4m3 at d = 64 / 128, aligned and large enough
+    need = L.attn_fwd_fp8_workspace_bytes(1, 1, 128, 64)
+    assert L.attn_selftest_abort(fp, fp, fp, fp, None, None, None, None, 1, 1, 128, 128, 64,
+                                 0.125, 0, attn.ATTN_BF16, fp, need, 500, None) == attn.ATTN_ERR_INVALID_ARG
+    assert L.attn_selftest_abort(fp, fp, fp, fp, None, fp, fp, fp, 1, 1, 128, 128, 64, 0.125, 0,
+                                 attn.ATTN_FP8_E4M3, fp, need - 1, 500, None) == attn.ATTN_ERR_INVALID_ARG
+    assert L.attn_selftest_abort(fp, fp, fp, fp, None, fp, fp, fp, 1, 1, 128, 128, 64, 0.125, 0,
+                                 attn.ATTN_FP8_E4M3, ctypes.c_void_p(P + 4), need, 500,
+                                 None) == attn.ATTN_ERR_INVALID_ARG
     assert L.attn_selftest_wait(0, None) == attn.ATTN_ERR_INVALID_ARG
     assert L.attn_selftest_wait(20 * 1000 * 1000, None) == attn.ATTN_ERR_INVALID_ARG
 
