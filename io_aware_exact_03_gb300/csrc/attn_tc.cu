@@ -12,18 +12,21 @@
 //     heads at a time so their K/V stay in L2, heaviest causal pairs first;
 //   * warp 0 (producer) streams Q_A, Q_B once and then K_0, V_0, K_1, V_1, ...
 //     through a ring of shared-memory slots with TMA, guarded by mbarriers;
-//   * warp 1 issues the tcgen05 MMAs and owns TMEM (the whole warp runs the
-//     issue loop on warp-uniform operands, one elected lane issues):
-//     S_t = Q_t K_j^T into the TMEM score buffer of tile t, and
-//     O_t += P_t V_j with P_t read from TMEM (P overwrites its own S buffer;
-//     the next S_t MMA is issued right behind that P V MMA: one thread's
-//     MMAs execute in issue order);
-//   * warps 2-5 (tile A) and 6-9 (tile B), one query row per thread, run the
-//     online softmax: TMEM -> registers, causal / ragged mask on the tiles that
-//     need it, row maximum, exp2, row sum, P back to TMEM as bf16 / fp16 /
-//     e4m3; they rescale the running output in TMEM only when the row maximum
-//     grew (bf16 / fp16: by more than 2^8, so P stays <= 256), and write O /
-//     lse at the end.
+//   * warps 1 and 2 issue the tcgen05 MMAs, one warp per tile (the whole warp
+//     runs the issue loop on warp-uniform operands, one elected lane issues;
+//     warp 1 owns TMEM): S_t = Q_t K_j^T into one TMEM score buffer that the
+//     two tiles take in turns (A_0, B_0, A_1, ...), and O_t += P_t V_j with
+//     P_t read from a TMEM buffer of its own;
+//   * warps 3-6 (tile A) and 7-10 (tile B), one query row per thread, run the
+//     online softmax: TMEM -> registers (after which the score buffer is free
+//     for the other tile's next Q K^T), causal / ragged mask on the tiles that
+//     need it, row maximum, exp2, row sum, P to its TMEM buffer as bf16 /
+//     fp16 (fp16 for e4m3 inputs); they rescale the running output in TMEM
+//     only when the row maximum grew by more than 2^8 (P stays <= 256), and
+//     write O / lse at the end;
+//   * e4m3 inputs: V is widened to fp16 on chip by a converter warp (warp 11)
+//     with shares taken by the producer and the issuers, or, with a caller
+//     workspace, once per call by widen_e4m3_kernel before this kernel.
 //   The two softmax groups interleave with each other's MMAs: while group A
 //   turns S_A into P_A the tensor core runs P_B V_j and the next S_B, and the
 //   other way round (the pages' ping-pong between two warp groups).
@@ -51,10 +54,12 @@ using namespace ptx;
 
 __device__ unsigned g_tc_status = 0;
 
-// Kernel variant of e4m3 inputs whose V arrives already widened to fp16 (the
-// host runs widen_e4m3_kernel into the caller's workspace first): Q and K are
-// e4m3 as in kE4M3, V tiles come into the ring by TMA as fp16.
-constexpr int kE4M3_V16 = 16;
+// Kernel kinds: the input dtype (kBF16, kFP16, kE4M3), plus the flag kV16
+// for e4m3 inputs whose V arrives already widened to fp16 (the host runs
+// widen_e4m3_kernel into the caller's workspace first): Q and K are e4m3, V
+// tiles come into the ring by TMA as fp16.
+constexpr int kV16 = 16;
+constexpr int kE4M3_V16 = kE4M3 | kV16;
 
 constexpr int BM = 128;        // query rows per tile (MMA M)
 constexpr int BN = 128;        // keys per tile (MMA N of Q K^T, K of P V)
@@ -63,84 +68,77 @@ constexpr int kSmemLimit = 232448;  // max dynamic shared memory per CTA
 
 template <int D, int KIND>
 struct Cfg {
-    static constexpr bool E4 = (KIND == kE4M3 || KIND == kE4M3_V16);  // e4m3 Q and K
+    static constexpr int BASE = KIND & 15;                 // input dtype
+    static constexpr bool E4 = (BASE == kE4M3);            // e4m3 Q and K
     static constexpr int E = E4 ? 1 : 2;                   // bytes per element of Q, K
     static constexpr int RB = D * E;                       // bytes per row
     static constexpr int CB = RB >= 128 ? 128 : RB;        // bytes per swizzle chunk
     static constexpr int NC = RB / CB;                     // chunks per row
     static constexpr int TILE = BM * RB;                   // bytes per 128-row tile
     static constexpr int CHUNK = BM * CB;                  // bytes per chunk of a tile
+    // TMEM: one score buffer S that the two tiles take in turns (each tile's
+    // softmax frees it as soon as it has loaded its scores), P_A and P_B (64
+    // columns each: 128 16-bit values per row) and O_A, O_B.  With P in
+    // buffers of its own, a tile's next Q K^T waits only for the other
+    // tile's softmax to load its scores, not for the tile's own P V (as it
+    // would with P written over S); measured against P over S (bf16, d =
+    // 128): C4 0.650 -> 0.645 ms, C3 0.108 -> 0.103; against P in shared
+    // memory (d = 64): C2 0.032 -> 0.0285 ms.
     // e4m3 inputs: P goes to the P V product as fp16, not e4m3.  An e4m3 P
     // keeps 3 mantissa bits, so a weight that is a sizeable share of its row
     // but not the row maximum is off by up to 2^-4 of itself, and with V
     // values of a few tens (the 0.1 % x10 outliers) that is an O error of
     // several 1e-2 to a few 1e-1 on rare rows; fp16 P (10 bits) keeps every
     // row within about 1e-3 of exact.  The P V MMA is then kind::f16 with
-    // A = P in TMEM and B = V widened from e4m3 to fp16 in shared memory by a
-    // converter warp, a tile ahead of its use (every e4m3 value is exact in
-    // fp16).  TMEM: one score
-    // buffer S shared by the two tiles (each tile's softmax frees it as soon as
-    // it has loaded its scores, and the two issuers take turns), P_A, P_B
-    // (64 columns each) and O_A, O_B.
-    static constexpr bool F16P = E4;
-    // V as fp16 from global memory (kE4M3_V16): no widening on chip, no
-    // converter warp; the ring's slots are sized for the larger fp16 V tile.
-    static constexpr bool V16G = (KIND == kE4M3_V16);
-    // P_t in shared memory (K-major, 128-byte swizzle) instead of over S_t in
-    // TMEM (16-bit types at d = 64): S_t is free as soon as the softmax has
-    // loaded it, so the next Q K^T runs while the softmax works.  The cost is
-    // shared-memory bandwidth (128 B/clk per SM): for 16-bit types at d = 128
-    // a step would move ~384 KB through shared memory, more than the MMAs'
-    // 2048 cycles allow (measured 14 % slower on the causal N = 16384 case),
-    // so they keep P over S in TMEM.
-    static constexpr bool P_SMEM = !F16P && (D == 64);
-    // Warps: 0 producer; with P_SMEM or F16P, 1 and 2 are MMA issuers, one
-    // per tile, each answering only its own tile's barriers (without them
-    // warp 1 issues for both tiles); then 2 x 4 softmax warps; F16P adds a
-    // V converter warp last.
-    static constexpr int ISSUERS = (P_SMEM || F16P) ? 2 : 1;
+    // A = P in TMEM and B = V in fp16 (every e4m3 value is exact in fp16),
+    // widened either on chip, a tile ahead of its use, or once per call into
+    // a workspace (kV16).
+    static constexpr bool V16G = (KIND & kV16) != 0;
+    // e4m3 V widened on chip (converter warp, two fp16 V buffers); otherwise
+    // P V reads the 16-bit V tile straight from its ring slot
+    static constexpr bool CONV = E4 && !V16G;
+    // Warps: 0 producer; 1 and 2 MMA issuers, one per tile, each answering
+    // only its own tile's barriers; then 2 x 4 softmax warps; on-chip
+    // widening adds a V converter warp last.
+    static constexpr int ISSUERS = 2;
     // 16-bit inputs: the O tile (bf16 / fp16) is exactly a Q tile, so the
     // epilogue stages O in the tile's own Q buffer (free once its last P V is
     // done) and writes it with one TMA store.
     static constexpr bool TMA_O = !E4;
     static constexpr int SOFTMAX_WARP0 = 1 + ISSUERS;
     static constexpr int CONVERTER_WARP = SOFTMAX_WARP0 + 8;
-    static constexpr int THREADS = 32 * (SOFTMAX_WARP0 + 8 + (F16P && !V16G ? 1 : 0));
-    static constexpr int PT = P_SMEM ? BM * BN * E : 0;    // bytes of one P tile in smem
-    static constexpr int P_CHUNK = BM * 128;               // bytes of a 128-byte-wide P chunk
-    // fp16 copy of one V tile (F16P): 128 keys x D, 128-byte swizzled chunks
-    // of 64 values, like a 16-bit V tile loaded by TMA
+    static constexpr int THREADS = 32 * (SOFTMAX_WARP0 + 8 + (CONV ? 1 : 0));
+    // a 16-bit V tile (a ring tile for 16-bit inputs, the fp16 copy for
+    // e4m3): 128 keys x D, 128-byte swizzled chunks of 64 values
     static constexpr int V16_CB = 2 * D >= 128 ? 128 : 2 * D;
     static constexpr int V16_CHUNK = BN * V16_CB;
-    static constexpr int V16T = F16P ? BN * 2 * D : 0;
-    static constexpr int V16_NC = 2 * D / V16_CB;          // 128-byte chunks per fp16 V row
+    static constexpr int V16T = BN * 2 * D;
+    static constexpr int V16_NC = 2 * D / V16_CB;          // 128-byte chunks per 16-bit V row
     // the two fp16 V buffers widened on chip (kE4M3 only)
-    static constexpr int V16BUF = (F16P && !V16G) ? V16T : 0;
+    static constexpr int V16BUF = CONV ? V16T : 0;
     // bytes per ring slot: a K or V tile of the input type, or (V16G) the
     // larger of an e4m3 K tile and an fp16 V tile
     static constexpr int SLOT = (V16G && V16T > TILE) ? V16T : TILE;
     // q_full, s_full x2, p_full x2, pv_done x2, drain, s_free x2, drain of
     // issuer B, v16_full x2, v16_empty x2
     static constexpr int NB_FIXED = 1 + 2 + 2 + 2 + 1 + 2 + 1 + 4;
-    static constexpr int SLOTS_FIT =
-        (kSmemLimit - 1024 - 2 * TILE - 2 * PT - 2 * V16BUF - 512) / SLOT;
-    // K/V ring depth; F16P needs it even (K items in even slots, V in odd)
-    static constexpr int SLOTS = (SLOTS_FIT > 8 ? 8 : SLOTS_FIT) & (F16P ? ~1 : ~0);
+    static constexpr int SLOTS_FIT = (kSmemLimit - 1024 - 2 * TILE - 2 * V16BUF - 512) / SLOT;
+    // K/V ring depth; on-chip widening needs it even (K items in even slots,
+    // V in odd: the two kinds of slot are released by different warps)
+    static constexpr int SLOTS = (SLOTS_FIT > 8 ? 8 : SLOTS_FIT) & (CONV ? ~1 : ~0);
     static constexpr uint32_t LAYOUT = (CB == 128) ? 2u : 4u;  // 128B / 64B swizzle
-    static constexpr int MMA_K = 32 / E;                   // K per Q K^T MMA instruction
     static constexpr int NB = NB_FIXED + 2 * SLOTS;        // mbarriers
     static constexpr size_t SMEM_USED =
-        1024 + (size_t)TILE * 2 + (size_t)SLOT * SLOTS + 2 * PT + 2 * (size_t)V16BUF + NB * 8 + 16;
+        1024 + (size_t)TILE * 2 + (size_t)SLOT * SLOTS + 2 * (size_t)V16BUF + NB * 8 + 16;
     // at least ~120 KB so two CTAs never share an SM (each takes all of TMEM)
     static constexpr size_t SMEM = SMEM_USED > 122880 ? SMEM_USED : 122880;
-    static constexpr uint32_t FMT = (KIND == kBF16) ? 1u : 0u;  // bf16 = 1, f16 / e4m3 = 0
-    static_assert(!V16G || D <= 128, "fp16 V from global memory: d = 64 or 128");
+    static constexpr uint32_t FMT = (BASE == kBF16) ? 1u : 0u;  // bf16 = 1, f16 / e4m3 = 0
+    static_assert(!V16G || (E4 && D <= 128), "fp16 V from global memory: e4m3, d = 64 or 128");
     static constexpr uint32_t IDESC_QK = instr_desc(FMT, FMT, 0, 0, BM, BN);
-    // P V: 16-bit operands (F16P: fp16 P and fp16 V)
-    static constexpr uint32_t IDESC_PV = instr_desc(F16P ? 0u : FMT, F16P ? 0u : FMT, 0, 1, BM, D);
+    // P V: 16-bit operands (e4m3 inputs: fp16 P and fp16 V)
+    static constexpr uint32_t IDESC_PV = instr_desc(E4 ? 0u : FMT, E4 ? 0u : FMT, 0, 1, BM, D);
     static constexpr int PV_K = 16;                        // keys per P V MMA instruction
-    static constexpr int PE = F16P ? 2 : E;                // bytes per P element
-    static constexpr uint32_t P_COLS = BN * PE / 4;        // TMEM columns holding P
+    static constexpr uint32_t P_COLS = BN * 2 / 4;         // TMEM columns holding P (16-bit)
     // Rescale the running output only when the row maximum grew by more than
     // this (log2 units): P values then stay <= 2^8, inside every P type's range.
     static constexpr float RESCALE_THRESHOLD = 8.0f;
@@ -148,13 +146,10 @@ struct Cfg {
     static_assert(SMEM_USED <= (size_t)kSmemLimit, "shared memory budget");
 };
 
-// TMEM columns.  bf16 / fp16: S_A [0,128), S_B [128,256), P_t over the start
-// of S_t.  e4m3 (F16P): one S [0,128) for both tiles, P_A [128,192),
-// P_B [192,256).  O_A [256, 256+D), O_B [256+D, 256+2D).
-template <bool F16P>
-__device__ __forceinline__ uint32_t col_s(int t) { return F16P ? 0u : 128u * t; }
-template <bool F16P>
-__device__ __forceinline__ uint32_t col_p(int t) { return F16P ? 128u + 64u * t : 128u * t; }
+// TMEM columns: one S [0,128) for both tiles, P_A [128,192), P_B [192,256),
+// O_A [256, 256+D), O_B [256+D, 256+2D).
+constexpr uint32_t kColS = 0;
+__device__ __forceinline__ uint32_t col_p(int t) { return 128u + 64u * (uint32_t)t; }
 template <int D>
 __device__ __forceinline__ uint32_t col_o(int t) { return 256u + (uint32_t)(D * t); }
 
@@ -210,8 +205,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sQ = smem;                      // two tiles: A then B
-    uint8_t* sP = smem + 2 * C::TILE;        // two P tiles (P_SMEM only)
-    uint8_t* sV16 = sP + 2 * C::PT;          // two fp16 V tiles (F16P without V16G)
+    uint8_t* sV16 = smem + 2 * C::TILE;      // two fp16 V tiles (on-chip widening only)
     uint8_t* sKV = sV16 + 2 * C::V16BUF;     // SLOTS slots of C::SLOT bytes
     uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + (size_t)C::SLOTS * C::SLOT);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NB);
@@ -224,8 +218,8 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
     const uint32_t b_drain = smem_u32(bars + 7);
     const uint32_t b_s_free = smem_u32(bars + 8);     // + 8 * tile
     const uint32_t b_drain_b = smem_u32(bars + 10);
-    const uint32_t b_v16_full = smem_u32(bars + 11);  // + 8 * buffer (F16P)
-    const uint32_t b_v16_empty = smem_u32(bars + 13); // + 8 * buffer (F16P)
+    const uint32_t b_v16_full = smem_u32(bars + 11);  // + 8 * buffer (on-chip widening)
+    const uint32_t b_v16_empty = smem_u32(bars + 13); // + 8 * buffer (on-chip widening)
     const uint32_t b_kv_full = smem_u32(bars + 15);               // + 8 * slot
     const uint32_t b_kv_empty = smem_u32(bars + 15 + C::SLOTS);   // + 8 * slot
 
@@ -289,10 +283,10 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         }
         for (int s = 0; s < C::SLOTS; ++s) {
             mbar_init(b_kv_full + 8 * s, 1);
-            // one release per issuer that reads the ring; F16P: V items (odd
-            // slots) are released by the four warps that widen them (V16G:
-            // read by both issuers' P V MMAs, like the K items)
-            mbar_init(b_kv_empty + 8 * s, (C::F16P && !C::V16G && (s & 1)) ? 4 : C::ISSUERS);
+            // one release per issuer (both read every K and V item); with
+            // on-chip widening the V items (odd slots) are released instead by
+            // the four warps that widen them
+            mbar_init(b_kv_empty + 8 * s, (C::CONV && (s & 1)) ? 4 : C::ISSUERS);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -312,8 +306,8 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    // F16P: V_j's e4m3 tile (ring item 2j + 1) widened into fp16 buffer j % 2,
-    // laid out as a 16-bit V tile loaded by TMA would be (128-byte rows of 64
+    // On-chip widening: V_j's e4m3 tile (ring item 2j + 1) widened into fp16
+    // buffer j % 2, laid out as a 16-bit V tile loaded by TMA would be (128-byte rows of 64
     // values, 128-byte swizzle; every e4m3 value is exact in fp16).  The work
     // is shared out by 16-byte units between the converter warp, the producer
     // warp and each MMA issuer (right after issuing its P V of the step
@@ -494,7 +488,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        if constexpr (C::F16P && !C::V16G) {
+        if constexpr (C::CONV) {
             // The whole warp runs the loop (lane 0 issues the copies) and also
             // widens its share of every V tile: its share of V_c right after
             // V_{c+LAG}'s load has gone out.  LAG must stay below the ring's
@@ -502,7 +496,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             // complete widening of V_c frees); 3 measured best on C5 (0.576
             // ms per call against 0.581 for 1 or 2).
             constexpr int LAG = 3;
-            static_assert(!C::F16P || LAG < C::SLOTS / 2, "the producer's share must come before its slot is needed");
+            static_assert(!C::CONV || LAG < C::SLOTS / 2, "the producer's share must come before its slot is needed");
             if (n_max > 0) {
                 if (lane == 0) {
                     const int nq = (n_kv[0] > 0) + (n_kv[1] > 0);
@@ -609,54 +603,33 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                         const uint64_t db = kd + off16;
                         const uint32_t acc = (c | ks) != 0;
                         if constexpr (C::E4)
-                            mma_f8_ss_1(tmem + col_s<C::F16P>(t), da, db, C::IDESC_QK, acc);
+                            mma_f8_ss_1(tmem + kColS, da, db, C::IDESC_QK, acc);
                         else
-                            mma_f16_ss_1(tmem + col_s<C::F16P>(t), da, db, C::IDESC_QK, acc);
+                            mma_f16_ss_1(tmem + kColS, da, db, C::IDESC_QK, acc);
                     }
                 }
             };
             auto issue_pv = [&](int t, int slot, bool first) {
-                if constexpr (C::F16P) {
-                    // A = fp16 P_t in TMEM (8 columns per 16 keys); B = the fp16
-                    // V tile in buffer `slot` (V16G: in ring slot `slot`),
-                    // MN-major: 8-key groups 8*128 bytes apart, 64-value
-                    // d-chunks V16_CHUNK apart
-                    const uint8_t* vt = C::V16G ? sKV + (size_t)slot * C::SLOT
-                                                : sV16 + (size_t)slot * C::V16BUF;
-                    const uint64_t vd = smem_desc(smem_u32(vt), C::V16_CHUNK, 8 * C::V16_CB, 2u);
+                // A = 16-bit P_t in TMEM (8 columns per 16 keys); B = the 16-bit
+                // V tile in ring slot `slot` (on-chip widening: in fp16 buffer
+                // `slot`), MN-major: 8-key groups 8*128 bytes apart, 64-value
+                // d-chunks V16_CHUNK apart
+                const uint8_t* vt = C::CONV ? sV16 + (size_t)slot * C::V16BUF
+                                            : sKV + (size_t)slot * C::SLOT;
+                const uint64_t vd = smem_desc(smem_u32(vt), C::V16_CHUNK, 8 * C::V16_CB, 2u);
 #pragma unroll
-                    for (int ks = 0; ks < BN / C::PV_K; ++ks) {
-                        const uint64_t db = vd + ((uint32_t)(ks * C::PV_K * C::V16_CB) >> 4);
-                        const uint32_t acc = (!first || ks > 0) ? 1u : 0u;
-                        mma_f16_ts_1(tmem + col_o<D>(t), tmem + col_p<true>(t) + ks * (C::PV_K * 2 / 4),
-                                     db, C::IDESC_PV, acc);
-                    }
-                    return;
-                }
-                // V is MN-major: 8-key groups 8*CB apart, d-chunks CHUNK apart
-                const uint64_t vd =
-                    smem_desc(smem_u32(sKV + (size_t)slot * C::SLOT), C::CHUNK, 8 * C::CB, C::LAYOUT);
-#pragma unroll
-                for (int ks = 0; ks < BN / C::MMA_K; ++ks) {
-                    const uint64_t db = vd + ((uint32_t)(ks * C::MMA_K * C::CB) >> 4);
+                for (int ks = 0; ks < BN / C::PV_K; ++ks) {
+                    const uint64_t db = vd + ((uint32_t)(ks * C::PV_K * C::V16_CB) >> 4);
                     const uint32_t acc = (!first || ks > 0) ? 1u : 0u;
-                    if constexpr (C::P_SMEM) {
-                        // P K-major in 128-byte chunks; each MMA takes 32 bytes of K
-                        const uint32_t off = (ks * 32 / 128) * C::P_CHUNK + (ks * 32) % 128;
-                        const uint64_t da =
-                            smem_desc(smem_u32(sP + t * C::PT) + off, 16, 1024, 2u);
-                        mma_f16_ss_1(tmem + col_o<D>(t), da, db, C::IDESC_PV, acc);
-                    } else {
-                        const uint32_t a_tmem = tmem + col_p<false>(t) + ks * (C::MMA_K * C::E / 4);
-                        mma_f16_ts_1(tmem + col_o<D>(t), a_tmem, db, C::IDESC_PV, acc);
-                    }
+                    mma_f16_ts_1(tmem + col_o<D>(t), tmem + col_p(t) + ks * (C::PV_K * 2 / 4),
+                                 db, C::IDESC_PV, acc);
                 }
             };
             auto slot_of = [](int it) { return it % C::SLOTS; };
             auto par_of = [](int it) { return (uint32_t)(it / C::SLOTS) & 1u; };
 
             bool ok = true;
-            if constexpr (C::F16P) {
+            {
                 // One issuer per tile; the two share one TMEM score buffer S.
                 // The score MMAs into S run in the order A_0 B_0 A_1 B_1 ...
                 // (a tile past its own key range drops out), and each waits
@@ -700,7 +673,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                         mma_commit_1(b_kv_empty + 8 * slot_of(0));
                     }
                 }
-                if constexpr (!C::V16G)
+                if constexpr (C::CONV)
                     if (ok && n_max > 0) ok = widen_share(0, vk0, vk1);
                 for (int j = 0; j < nt && ok; ++j) {
                     const int itK = 2 * j + 2;
@@ -714,16 +687,16 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                         mma_commit_1(b_kv_empty + 8 * slot_of(itK));
                     }
                     const int itV = 2 * j + 1;
-                    if constexpr (C::V16G)
+                    if constexpr (!C::CONV)
                         ok = wb(b_kv_full + 8 * slot_of(itV), par_of(itV));
                     else
                         ok = wb(b_v16_full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u);
                     if (ok) ok = wb(b_p_full + 8 * t, (uint32_t)j & 1u);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_pv(t, C::V16G ? slot_of(itV) : (j & 1), j == 0);
+                    issue_pv(t, C::CONV ? (j & 1) : slot_of(itV), j == 0);
                     mma_commit_1(b_pv_done + 8 * t);
-                    if constexpr (C::V16G) {
+                    if constexpr (!C::CONV) {
                         mma_commit_1(b_kv_empty + 8 * slot_of(itV));
                     } else {
                         mma_commit_1(b_v16_empty + 8 * (j & 1));
@@ -734,7 +707,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                 for (int j = nt; j < n_max && ok; ++j) {
                     ok = wb(b_kv_full + 8 * slot_of(2 * j), par_of(2 * j));
                     if (ok) mbar_arrive_1(b_kv_empty + 8 * slot_of(2 * j));
-                    if constexpr (C::V16G) {
+                    if constexpr (!C::CONV) {
                         if (ok) ok = wb(b_kv_full + 8 * slot_of(2 * j + 1), par_of(2 * j + 1));
                         if (ok) mbar_arrive_1(b_kv_empty + 8 * slot_of(2 * j + 1));
                     } else {
@@ -748,115 +721,11 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                     mma_commit_1(drain_t);
                     wait_drain(drain_t, 0, p.drain_ns);
                 }
-            } else if constexpr (C::P_SMEM) {
-                // One issuer per tile.  S_t is free once the softmax has loaded
-                // it, so the scores of K_{j+1} are issued as soon as that
-                // happens and run while the softmax works; P_t V_j follows when
-                // P_t is in shared memory.  Every ring item gets one release
-                // from each issuer: items this tile never reads (keys beyond
-                // its causal range) are released once they have landed, so a
-                // release never runs ahead of the item's own fill.
-                const int t = __shfl_sync(0xffffffffu, warp, 0) - 1;
-                const int nt = n_kv[t];
-                const uint32_t drain_t = t == 0 ? b_drain : b_drain_b;
-                ok = wb(b_q_full, 0);
-                if (ok && nt > 0) {
-                    ok = wb(b_kv_full + 8 * slot_of(0), par_of(0));
-                    if (ok) {
-                        tc_fence_after();
-                        issue_qk(t, slot_of(0));
-                        mma_commit_1(b_s_full + 8 * t);
-                        mma_commit_1(b_kv_empty + 8 * slot_of(0));
-                    }
-                }
-                for (int j = 0; j < nt && ok; ++j) {
-                    const int itV = 2 * j + 1, itK = 2 * j + 2;
-                    if (j + 1 < nt) {
-                        ok = wb(b_kv_full + 8 * slot_of(itK), par_of(itK));
-                        if (ok) ok = wb(b_s_free + 8 * t, (uint32_t)j & 1u);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_qk(t, slot_of(itK));
-                        mma_commit_1(b_s_full + 8 * t);
-                        mma_commit_1(b_kv_empty + 8 * slot_of(itK));
-                    }
-                    ok = wb(b_kv_full + 8 * slot_of(itV), par_of(itV));
-                    if (ok) ok = wb(b_p_full + 8 * t, (uint32_t)j & 1u);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(t, slot_of(itV), j == 0);
-                    mma_commit_1(b_pv_done + 8 * t);
-                    mma_commit_1(b_kv_empty + 8 * slot_of(itV));
-                }
-                // items of K/V tiles [nt, n_max): not read by this tile
-                for (int it = 2 * nt; it < 2 * n_max && ok; ++it) {
-                    ok = wb(b_kv_full + 8 * slot_of(it), par_of(it));
-                    if (ok) mbar_arrive_1(b_kv_empty + 8 * slot_of(it));
-                }
-                if (!ok) {
-                    // make sure none of this issuer's MMAs still runs when TMEM is freed
-                    mma_commit_1(drain_t);
-                    wait_drain(drain_t, 0, p.drain_ns);
-                }
-            } else {
-                ok = wb(b_q_full, 0);
-                if (ok) ok = wb(b_kv_full + 8 * slot_of(0), par_of(0));
-                if (ok) {
-                    tc_fence_after();
-                    for (int t = 0; t < 2; ++t) {
-                        if (n_kv[t] == 0) continue;
-                        issue_qk(t, slot_of(0));
-                        mma_commit_1(b_s_full + 8 * t);
-                    }
-                    mma_commit_1(b_kv_empty + 8 * slot_of(0));
-                }
-            }
-            // Per tile: O_t += P_t V_j, then at once S_t = Q_t K_{j+1}^T into the
-            // same TMEM columns.  One thread's tcgen05.mma operations execute in
-            // issue order, so the P V MMA has read P_t before the next score
-            // MMA overwrites it; no completion wait is needed in between.
-            // While softmax A works, the tensor core runs tile B's pair of MMAs
-            // and the other way round.
-            for (int j = 0; j < n_max && ok && !C::P_SMEM && !C::F16P; ++j) {
-                const int itV = 2 * j + 1, itK = 2 * j + 2;
-                ok = wb(b_kv_full + 8 * slot_of(itV), par_of(itV));
-                bool k_ready = false;
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (j < n_kv[t]) {
-                        ok = wb(b_p_full + 8 * t, (uint32_t)j & 1u);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_pv(t, slot_of(itV), j == 0);
-                        mma_commit_1(b_pv_done + 8 * t);
-                    }
-                    if (j + 1 < n_kv[t]) {
-                        if (!k_ready) {
-                            ok = wb(b_kv_full + 8 * slot_of(itK), par_of(itK));
-                            k_ready = true;
-                        }
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_qk(t, slot_of(itK));
-                        mma_commit_1(b_s_full + 8 * t);
-                    }
-                }
-                if (!ok) break;
-                // release V_j (every P V of it is issued) and K_{j+1}; the last
-                // V's release is not needed (nothing is loaded after it)
-                if (j + 1 < n_max) {
-                    mma_commit_1(b_kv_empty + 8 * slot_of(itV));
-                    mma_commit_1(b_kv_empty + 8 * slot_of(itK));
-                }
-            }
-            if (!ok && !C::P_SMEM && !C::F16P) {
-                // make sure no MMA is still reading or writing when TMEM is freed
-                mma_commit_1(b_drain);
-                wait_drain(b_drain, 0, p.drain_ns);
             }
         }
         __syncwarp();
-    } else if (C::F16P && !C::V16G && warp == C::CONVERTER_WARP) {
-        // ------------------------------------------- V converter (F16P only)
+    } else if (C::CONV && warp == C::CONVERTER_WARP) {
+        // --------------------------------------- V converter (on-chip widening)
         // Its share of every V tile's units (producer and issuers take the rest).
         for (int j = 0; j < n_max; ++j)
             if (!widen_share(j, 0, V_CONV)) break;
@@ -884,14 +753,11 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         const float c = p.scale * dq * dk * 1.4426950408889634f;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        // this thread's row of P_t in shared memory (P_SMEM only)
-        const uint32_t p_row = smem_u32(sP + t * C::PT) + (uint32_t)(r >> 3) * 1024u +
-                               (uint32_t)(r & 7) * 128u;
 
-        // P_SMEM / F16P: the scores of the next step and the release of the P
-        // buffer are tested early (mbar_test) and the results used later, so
-        // the barrier round trips overlap the softmax; a failed test falls back
-        // to the bounded wait.
+        // The scores of the next step and the release of the P buffer are
+        // tested early (mbar_test) and the results used later, so the barrier
+        // round trips overlap the softmax; a failed test falls back to the
+        // bounded wait.
         uint32_t s_pre = 0, pv_pre = 0;
         for (int j = 0; j < nt && ok; ++j) {
             if (!__all_sync(0xffffffffu, s_pre != 0u) &&
@@ -904,19 +770,17 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             uint32_t sr[BN];
 #pragma unroll
             for (int u = 0; u < BN / 32; ++u)
-                tmem_ld32(t_row + col_s<C::F16P>(t) + 32 * u,
+                tmem_ld32(t_row + kColS + 32 * u,
                           *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * u]));
             tmem_ld_wait();
 #pragma unroll
             for (int u = 0; u < BN / 32; ++u)
                 reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[32 * u]));
-            if constexpr (C::P_SMEM || C::F16P) {
-                // the scores are in registers: the next score MMA may overwrite them
-                tc_fence_before();
-                __syncwarp();
-                mbar_arrive_1(b_s_free + 8 * t);
-                if (j > 0) pv_pre = mbar_test(pv_done, (uint32_t)(j - 1) & 1u);
-            }
+            // the scores are in registers: the next score MMA may overwrite them
+            tc_fence_before();
+            __syncwarp();
+            mbar_arrive_1(b_s_free + 8 * t);
+            if (j > 0) pv_pre = mbar_test(pv_done, (uint32_t)(j - 1) & 1u);
             float s[BN];
 #pragma unroll
             for (int x = 0; x < BN; ++x) s[x] = __uint_as_float(sr[x]);
@@ -953,13 +817,10 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
 #pragma unroll
             for (int k = 0; k < 8; ++k) sc[k] = 0.f;
             // P_t as bf16 / fp16 (e4m3 inputs: fp16), 32 TMEM columns (64
-            // scores) at a time so only one chunk of packed P is live.  P over
-            // S: the first P_COLS columns of S_t, already read above (the
-            // previous P_t V MMA read P before this S_t was written).  P in
-            // shared memory or in its own TMEM buffer (F16P): the buffer is
-            // free once P_{j-1} V_{j-1} has completed.  The scale-and-subtract
-            // and the sums use packed f32x2 instructions.
-            constexpr int PER_CHUNK = 32 * 4 / C::PE;  // score columns per 32 TMEM columns
+            // scores) at a time so only one chunk of packed P is live.  P_t's
+            // buffer is free once P_{j-1} V_{j-1} has completed.  The
+            // scale-and-subtract and the sums use packed f32x2 instructions.
+            constexpr int PER_CHUNK = 32 * 4 / 2;  // 16-bit scores per 32 TMEM columns
 #pragma unroll
             for (int u = 0; u < (int)C::P_COLS / 32; ++u) {
                 uint32_t pk[32];
@@ -971,48 +832,27 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                     const float p0 = ex2(a0), p1 = ex2(a1);
                     const int k = ((x / 2) & 3) * 2;
                     fadd2(sc[k], sc[k + 1], sc[k], sc[k + 1], p0, p1);
-                    pk[x / 2] = (KIND == kBF16) ? pack_bf16(p0, p1) : pack_f16(p0, p1);
+                    pk[x / 2] = (C::BASE == kBF16) ? pack_bf16(p0, p1) : pack_f16(p0, p1);
                 }
-                if constexpr (C::P_SMEM || C::F16P) {
-                    if (u == 0 && j > 0 && !__all_sync(0xffffffffu, pv_pre != 0u) &&
-                        !__all_sync(0xffffffffu, wait_bar(pv_done, (uint32_t)(j - 1) & 1u,
-                                                          abort_flag, lim))) {
-                        ok = false;
-                        break;
-                    }
-                    if (C::F16P && u == 0 && j > 0) tc_fence_after();  // P V_{j-1} has read P_t
+                if (u == 0 && j > 0 && !__all_sync(0xffffffffu, pv_pre != 0u) &&
+                    !__all_sync(0xffffffffu, wait_bar(pv_done, (uint32_t)(j - 1) & 1u,
+                                                      abort_flag, lim))) {
+                    ok = false;
+                    break;
                 }
-                if constexpr (C::P_SMEM) {
-                    // row r of a 128-byte-swizzled K-major tile: 16-byte unit w
-                    // sits at unit w ^ (r % 8)
-                    const uint32_t row_base =
-                        p_row + (uint32_t)u * C::P_CHUNK;
-#pragma unroll
-                    for (int w = 0; w < 8; ++w)
-                        st_shared_v4(row_base + ((uint32_t)(w ^ (r & 7)) << 4), pk[4 * w],
-                                     pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
-                } else {
-                    tmem_st32(t_row + col_p<C::F16P>(t) + 32 * u, pk);
-                }
+                if (u == 0 && j > 0) tc_fence_after();  // P V_{j-1} has read P_t
+                tmem_st32(t_row + col_p(t) + 32 * u, pk);
             }
             if (!ok) break;
-            if constexpr (C::P_SMEM || C::F16P) {
-                s_pre = (j + 1 < nt) ? mbar_test(s_full, (uint32_t)(j + 1) & 1u) : 0u;
-            }
-            if constexpr (C::P_SMEM) fence_proxy_async_smem();
+            s_pre = (j + 1 < nt) ? mbar_test(s_full, (uint32_t)(j + 1) & 1u) : 0u;
             const float sum =
                 ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));
             l = l * alpha + sum;
 
             if (any && j > 0) {
                 // O_t is touched only to rescale it; it is stable once
-                // P_{j-1} V_{j-1} has completed (P_SMEM / F16P: already
-                // confirmed before the first P store)
-                if (!(C::P_SMEM || C::F16P) &&
-                    !__all_sync(0xffffffffu, wait_bar(pv_done, (uint32_t)(j - 1) & 1u, abort_flag, lim))) {
-                    ok = false;
-                    break;
-                }
+                // P_{j-1} V_{j-1} has completed (confirmed before the first P
+                // store above)
                 tc_fence_after();
                 // 64 columns per load round: two loads in flight per wait
 #pragma unroll
@@ -1129,7 +969,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                         for (int x = 0; x < 16; ++x) {
                             const float a0 = __uint_as_float(oo[2 * x]) * inv;
                             const float a1 = __uint_as_float(oo[2 * x + 1]) * inv;
-                            packed[x] = (KIND == kFP16) ? pack_f16(a0, a1) : pack_bf16(a0, a1);
+                            packed[x] = (C::BASE == kFP16) ? pack_f16(a0, a1) : pack_bf16(a0, a1);
                         }
                         const uint32_t row_base = smem_u32(sQ + t * C::TILE + (u / 2) * C::CHUNK) +
                                                   (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u;
@@ -1159,7 +999,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                     for (int x = 0; x < 16; ++x) {
                         const float a0 = __uint_as_float(oo[2 * x]) * inv;
                         const float a1 = __uint_as_float(oo[2 * x + 1]) * inv;
-                        packed[x] = (KIND == kFP16) ? pack_f16(a0, a1) : pack_bf16(a0, a1);
+                        packed[x] = (C::BASE == kFP16) ? pack_f16(a0, a1) : pack_bf16(a0, a1);
                     }
                     if (valid) {
                         uint4* dst = reinterpret_cast<uint4*>(orow + 32 * u);
@@ -1294,7 +1134,7 @@ cudaError_t launch_t(const Problem& pr, cudaStream_t stream, int n_splits = 1,
     using C = Cfg<D, KIND>;
     CUtensorMap mq, mk, mv, mo;
     const int ce = C::CB / C::E;
-    const int dt = C::E4 ? (int)kE4M3 : KIND;  // element type of Q and K
+    const int dt = C::BASE;  // element type of Q and K (and V, O for 16-bit inputs)
     // O has the layout of Q; for 16-bit inputs also its element size
     // e4m3 at d = 128: O is bf16, 64-column chunks staged in the Q buffer
     const bool o8 = C::E4 && D == 128 && n_splits == 1;

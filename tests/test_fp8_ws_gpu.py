@@ -118,3 +118,19 @@ def test_abort_path(shape):
     O, lse = run_gpu(case, dev, "fp8ws")
     O_ref, lse_ref = oracle_full(case, inputs)
     compare(case, O, lse, O_ref, lse_ref)
+
+
+def test_no_keys_needs_no_workspace():
+    """N_k = 0: nothing to widen (the workspace size is 0 and none is needed);
+    every row gets O = 0 and lse = -inf, as from attn_fwd_fp8."""
+    f8 = torch.float8_e4m3fn
+    q = (torch.randn(2, 70, 2, 128, device="cuda") * 4).to(f8)
+    kv = torch.empty(2, 0, 2, 128, device="cuda", dtype=f8)
+    ones = torch.ones(2, 2, device="cuda")
+    assert attn.attn_fwd_fp8_workspace_bytes(2, 2, 0, 128) == 0
+    o = torch.full((2, 70, 2, 128), 7.0, device="cuda", dtype=torch.bfloat16)
+    lse = torch.zeros(2, 2, 70, device="cuda")
+    attn.attn_fwd_fp8_ws(q, kv, kv, ones, ones, ones, o=o, lse=lse, scale=0.1)
+    attn.attn_check_status()
+    assert torch.all(o == 0)
+    assert torch.all(torch.isneginf(lse))
