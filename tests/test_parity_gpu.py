@@ -182,8 +182,8 @@ def test_bounded_wait_times_out_and_context_stays_usable():
 
 ABORT = [
     # B, H, N_q, N_k, d, causal, dtype: one per kernel form
-    (1, 2, 300, 300, 64, True, "bf16"),     # P in shared memory, two issuers, 16-bit
-    (1, 2, 300, 300, 128, True, "bf16"),    # P over S in TMEM, one issuer
+    (1, 2, 300, 300, 64, True, "bf16"),     # 16-bit, d = 64 (ring of 16 KiB slots)
+    (1, 2, 300, 300, 128, True, "bf16"),    # 16-bit, d = 128 (ring of 32 KiB slots)
     (1, 2, 300, 300, 128, False, "e4m3"),   # fp16 P, V widened on chip, e4m3 with descales
     (1, 2, 300, 300, 256, True, "bf16"),    # head dimension 256, one tile per CTA
     (1, 2, 300, 300, 256, False, "e4m3"),   # head dimension 256 with the V converter warp
