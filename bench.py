@@ -61,7 +61,8 @@ def parse():
     ap.add_argument("--case", choices=["C1", "C2", "C3", "C4", "C5", "LKV", "D256", "D256F", "BWD"], default=None,
                     help="measure one workload case alone instead of the C4 + C5 step")
     ap.add_argument("--splits", type=int, default=1,
-                    help="with --case: split each query tile's K/V range over this many CTAs")
+                    help="with --case: split each query tile's K/V range over this many CTAs "
+                         "(0: the count attn_splitkv_num_splits suggests for the case on this GPU)")
     return ap.parse_args()
 
 
@@ -314,6 +315,9 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     attn.build()
     attn.lib()
+    if args.splits == 0:
+        c0 = case_by_name(args.case) if args.case else None
+        args.splits = attn.attn_splitkv_num_splits(c0.B, c0.H, c0.N_q, c0.N_k, c0.d) if c0 else 1
 
     names, desc = workload(args)
     cases = [case_by_name(n) for n in names]

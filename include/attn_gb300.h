@@ -186,6 +186,14 @@ ATTN_API attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void
  * arguments). */
 ATTN_API size_t attn_splitkv_workspace_bytes(int B, int H, int N_q, int d, int num_splits);
 
+/* A num_splits for attn_fwd_splitkv on a GPU with num_sms SMs: the count (1 ..
+ * 32) that minimises an estimate of the time in 128-key steps, waves of CTAs
+ * x (key tiles per CTA + 3 steps of fixed cost per CTA) + the combine pass
+ * (1 + splits / 8 steps).  1 when splitting does not pay (enough query tiles
+ * to fill the GPU) or for invalid arguments.  Host arithmetic only: no CUDA
+ * call. */
+ATTN_API int attn_splitkv_num_splits(int B, int H, int N_q, int N_k, int d, int num_sms);
+
 /* Backward pass: gradients of the forward's O with respect to q, k and v for an
  * upstream gradient dO (the pages name training speedups, "FlashAttention
  * (HI)" page, section "Empirical results", but do not write the backward pass

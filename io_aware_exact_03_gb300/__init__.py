@@ -23,7 +23,8 @@ from . import ext_build as _build
 __all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_fp8_ws", "attn_fwd_fp8_workspace_bytes",
            "attn_fwd_simt", "attn_fwd_splitkv", "attn_fwd_gqa",
            "attn_quantize_e4m3",
-           "attn_splitkv_workspace_bytes", "attn_check_status", "attn_status_string",
+           "attn_splitkv_workspace_bytes", "attn_splitkv_num_splits", "attn_check_status",
+           "attn_status_string",
            "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_host", "attn_fwd_host_workspace_bytes",
            "attn_selftest_wait", "attn_selftest_abort",
            "AttnError", "lib", "build"]
@@ -78,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd_splitkv.restype = i
         L.attn_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
         L.attn_splitkv_workspace_bytes.restype = sz
+        L.attn_splitkv_num_splits.argtypes = [i, i, i, i, i, i]
+        L.attn_splitkv_num_splits.restype = i
         L.attn_fwd_splitkv_static.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, i, i, i, i, i, f,
                                               i, i, i, vp]
         L.attn_fwd_splitkv_static.restype = i
@@ -294,6 +297,15 @@ def attn_quantize_e4m3(x, signs=None, codes=None, descale=None, stream=None):
                                   H, d, _ptr(signs), _stream(stream, x.device))
     _raise(st, "attn_quantize_e4m3")
     return codes, descale
+
+
+def attn_splitkv_num_splits(B, H, N_q, N_k, d, num_sms=None) -> int:
+    """Suggested num_splits for attn_fwd_splitkv (num_sms: of the current CUDA
+    device when not given)."""
+    if num_sms is None:
+        torch = _torch()
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return int(lib().attn_splitkv_num_splits(int(B), int(H), int(N_q), int(N_k), int(d), int(num_sms)))
 
 
 def attn_splitkv_workspace_bytes(B, H, N_q, d, num_splits) -> int:

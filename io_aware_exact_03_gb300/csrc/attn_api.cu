@@ -149,6 +149,30 @@ size_t attn_splitkv_workspace_bytes(int B, int H, int N_q, int d, int num_splits
     return attn::splitkv_workspace_bytes(B, H, N_q, d, num_splits);
 }
 
+int attn_splitkv_num_splits(int B, int H, int N_q, int N_k, int d, int num_sms) {
+    if (B <= 0 || H <= 0 || N_q <= 0 || N_k <= 0 || num_sms <= 0) return 1;
+    if (d != 64 && d != 128 && d != 256) return 1;
+    // CTAs without splitting: one per (batch, head, query-tile pair), or per
+    // query tile at d = 256; key tiles of 128 keys each CTA walks
+    const long long rows_per_cta = d == 256 ? 128 : 256;
+    const long long units = (long long)B * H * ((N_q + rows_per_cta - 1) / rows_per_cta);
+    const long long tiles = (N_k + 127) / 128;
+    // estimated time in key-tile steps: waves x (tiles per CTA + ~3 steps of
+    // fixed cost per CTA), plus the combine pass (~1 step + s / 8)
+    int best = 1;
+    double best_cost = 0.0;
+    for (int sp = 1; sp <= attn::kMaxSplits && sp <= tiles; ++sp) {
+        const long long waves = (units * sp + num_sms - 1) / num_sms;
+        const long long per = (tiles + sp - 1) / sp;
+        const double cost = (double)waves * (double)(per + 3) + (sp > 1 ? 1.0 + sp / 8.0 : 0.0);
+        if (sp == 1 || cost < best_cost) {
+            best = sp;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
 attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
                                const float* q_descale, const float* k_descale,
                                const float* v_descale, int B, int H, int N_q, int N_k, int d,

@@ -147,6 +147,24 @@ def test_fp8_ws_rejects_bad_arguments(L):
                              None) == attn.ATTN_OK
 
 
+def test_splitkv_num_splits(L):
+    # long K/V, few query tiles: B1 H8 N_q 512 N_k 65536 has 16 CTAs unsplit; 9 splits fill
+    # 144 of 152 SMs in one wave (8 would leave 24 idle, 10 would need a second wave)
+    assert L.attn_splitkv_num_splits(1, 8, 512, 65536, 128, 152) == 9
+    # a single query row against 65536 keys, 8 heads: 19 splits = 152 CTAs, one wave
+    assert L.attn_splitkv_num_splits(1, 8, 1, 65536, 128, 152) == 19
+    # enough query tiles to fill the GPU: no split
+    assert L.attn_splitkv_num_splits(1, 16, 16384, 16384, 128, 152) == 1
+    assert L.attn_splitkv_num_splits(2, 16, 8192, 8192, 128, 152) == 1
+    # never more splits than key tiles, never more than 32
+    assert L.attn_splitkv_num_splits(1, 1, 128, 300, 64, 152) <= 3
+    assert 1 <= L.attn_splitkv_num_splits(1, 1, 1, 1 << 24, 256, 1024) <= 32
+    # degenerate or invalid arguments: 1
+    for args in [(0, 8, 512, 65536, 128, 152), (1, 8, 512, 0, 128, 152),
+                 (1, 8, 512, 65536, 96, 152), (1, 8, 512, 65536, 128, 0)]:
+        assert L.attn_splitkv_num_splits(*args) == 1
+
+
 def test_splitkv_rejects_bad_workspace(L):
     need = L.attn_splitkv_workspace_bytes(1, 1, 16, 64, 4)
     args = (P, P, P, P, P, None, None, None, 1, 1, 16, 16, 64, 0.125, 0, 0)

@@ -161,6 +161,16 @@ def test_splitkv_matches_oracle(shape):
     compare(case, O, lse, O_ref, lse_ref)
 
 
+def test_splitkv_with_the_suggested_count_on_long_kv():
+    """The long-K/V workload (B1 H8 N_q 512 N_k 65536, bf16) with the split count
+    attn_splitkv_num_splits suggests for this GPU, on 256 seeded rows against the
+    oracle."""
+    case = synthetic.EXTRA_CASES["LKV"]
+    n = attn.attn_splitkv_num_splits(case.B, case.H, case.N_q, case.N_k, case.d)
+    assert 1 < n <= 32
+    check_sampled(case, f"split{n}")
+
+
 def test_splitkv_agrees_with_single_pass_on_C3():
     case = synthetic.CASES["C3"]
     dev = to_device(synthetic.make_inputs(case))
