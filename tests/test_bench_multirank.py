@@ -58,3 +58,21 @@ def test_single_rank_helpers_without_a_process_group():
     assert bench.max_over_ranks(torch, dist, 5.0, "cpu") == 5.0
     assert bench.job_tflops(2e12, 4, 1, 8.0) == pytest.approx(1000.0)
     assert bench.shard_seed(1004, 0) == 1004 and bench.shard_seed(1004, 3) == 1304
+
+
+def test_launch_and_flop_counts():
+    """The counts the JSON line's gpu_launches and value are built from."""
+    C4, C5 = bench.case_by_name("C4"), bench.case_by_name("C5")
+    # C4 (bf16): one attention kernel; C5 (e4m3, d 128): the V widening pass and
+    # the attention kernel (attn_fwd_fp8_ws); split-KV adds the combine kernel;
+    # the backward pass is three kernels; d = 256 e4m3 widens on chip (one)
+    assert bench.launches_per_call(C4, 1) == 1
+    assert bench.launches_per_call(C5, 1) == 2
+    assert bench.launches_per_call(bench.case_by_name("LKV"), 9) == 2
+    assert bench.launches_per_call(bench.case_by_name("BWD"), 1) == 3
+    assert bench.launches_per_call(bench.case_by_name("D256F"), 1) == 1
+    # 4 B H N_q N_k d FLOPs, halved under the causal mask; the backward counts 2.5x
+    assert bench.work_flops(C4) == 4 * 1 * 16 * 16384 * 16384 * 128 / 2
+    assert bench.work_flops(C5) == 4 * 2 * 16 * 8192 * 8192 * 128
+    bwd = bench.case_by_name("BWD")
+    assert bench.work_flops(bwd) == 2.5 * 4 * 2 * 16 * 4096 * 4096 * 128 / 2
