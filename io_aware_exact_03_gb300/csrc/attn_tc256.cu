@@ -537,17 +537,13 @@ __global__ void __launch_bounds__(Cfg256<KIND>::THREADS, 1)
             }
             tc_fence_after();
             uint32_t sr[BN];
-            float cmx[BN / 32];  // each 32-column chunk's maximum, from the load itself
-#pragma unroll
-            for (int u = 0; u < BN / 32; ++u)
-                tmem_ld32_max(t_row + 128u * buf + 32 * u,
-                              *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * u]), cmx[u]);
+            float rmx;  // the row's maximum, from the load itself
+            tmem_ld128_max(t_row + 128u * buf, sr, rmx);
             tmem_ld_wait();
 #pragma unroll
-            for (int u = 0; u < BN / 32; ++u) {
+            for (int u = 0; u < BN / 32; ++u)
                 reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[32 * u]));
-                reg_fence_f(cmx[u]);
-            }
+            reg_fence_f(rmx);
             float s[BN];
 #pragma unroll
             for (int x = 0; x < BN; ++x) s[x] = __uint_as_float(sr[x]);
@@ -559,8 +555,8 @@ __global__ void __launch_bounds__(Cfg256<KIND>::THREADS, 1)
 #pragma unroll
                 for (int x = 0; x < BN; ++x)
                     if (x > cl) s[x] = -INFINITY;
-                // row maximum of the masked row (the load's chunk maxima
-                // include the masked columns)
+                // row maximum of the masked row (the load's maximum includes
+                // the masked columns)
                 float mc[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) mc[k] = fmaxf(s[k], s[k + 8]);
@@ -571,7 +567,7 @@ __global__ void __launch_bounds__(Cfg256<KIND>::THREADS, 1)
                 }
                 mx = max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
             } else {
-                mx = max3(cmx[0], cmx[1], fmaxf(cmx[2], cmx[3]));
+                mx = rmx;
             }
             const float m_new = mx * c;
             const bool need = m_new > m_used + C::RESCALE_THRESHOLD;
