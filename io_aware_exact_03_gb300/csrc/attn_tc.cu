@@ -82,8 +82,9 @@ struct Cfg {
     // buffers of its own, a tile's next Q K^T waits only for the other
     // tile's softmax to load its scores, not for the tile's own P V (as it
     // would with P written over S); measured against P over S (bf16, d =
-    // 128): C4 0.650 -> 0.645 ms, C3 0.108 -> 0.103; against P in shared
-    // memory (d = 64): C2 0.032 -> 0.0285 ms.
+    // 128, causal, B1 H16 N16384): 0.650 -> 0.645 ms, (B2 H16 N4096): 0.108
+    // -> 0.103 ms; against P in shared memory (bf16, d = 64, B4 H16 N1024):
+    // 0.032 -> 0.0285 ms.
     // e4m3 inputs: P goes to the P V product as fp16, not e4m3.  An e4m3 P
     // keeps 3 mantissa bits, so a weight that is a sizeable share of its row
     // but not the row maximum is off by up to 2^-4 of itself, and with V
@@ -314,13 +315,14 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
     // before), so that the fp16 stores are spread over the four SM
     // sub-partitions instead of loading one: from one warp they went through
     // its sub-partition's shared-memory / special-function issue path beside
-    // two softmax warps and cost ~17 % of C5's time.
+    // two softmax warps and cost ~17 % of the time on e4m3 B2 H16 N8192 d128.
     constexpr int V_UNITS = C::CB / 16;       // 16-byte units per e4m3 row
     constexpr int V_PER = BN * V_UNITS / 32;  // units per lane, whole tile
     // shares, in units per lane: converter warp [0, V_CONV), producer warp
     // [V_PROD0, +V_PROD), issuer t [V_ISS0 + t V_ISS, +V_ISS).  Measured on
-    // C5 (ms per call, units of 1/32 of a tile per warp): all on the converter
-    // 0.635; converter 16, issuers 8 each 0.605; 8 each 0.616; issuers 16
+    // e4m3 B2 H16 N8192 d128 (ms per call, units of 1/32 of a tile per
+    // warp): all on the converter 0.635; converter 16, issuers 8 each 0.605;
+    // 8 each 0.616; issuers 16
     // each 0.734; converter 16, producer 8, issuers 4 each 0.572-0.581;
     // converter 20, producer 8, issuers 2 each 0.567-0.571 (kept: the issuers'
     // MMA issue tolerates little extra work); converter 24, producer 4,
@@ -493,8 +495,8 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             // widens its share of every V tile: its share of V_c right after
             // V_{c+LAG}'s load has gone out.  LAG must stay below the ring's
             // depth in tiles (V_{c+SLOTS/2} reuses V_c's slot, which only the
-            // complete widening of V_c frees); 3 measured best on C5 (0.576
-            // ms per call against 0.581 for 1 or 2).
+            // complete widening of V_c frees); 3 measured best on e4m3 B2
+            // H16 N8192 d128 (0.576 ms per call against 0.581 for 1 or 2).
             constexpr int LAG = 3;
             static_assert(!C::CONV || LAG < C::SLOTS / 2, "the producer's share must come before its slot is needed");
             if (n_max > 0) {
