@@ -61,6 +61,12 @@ __device__ unsigned g_tc_status = 0;
 constexpr int kV16 = 16;
 constexpr int kE4M3_V16 = kE4M3 | kV16;
 
+// a compile-time int passed as a value (picks a generic lambda's instance)
+template <int N>
+struct IntC {
+    static constexpr int value = N;
+};
+
 constexpr int BM = 128;        // query rows per tile (MMA M)
 constexpr int BN = 128;        // keys per tile (MMA N of Q K^T, K of P V)
 constexpr uint32_t kTmemCols = 512;
@@ -320,13 +326,13 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
     constexpr int V_PER = BN * V_UNITS / 32;  // units per lane, whole tile
     // shares, in units per lane: converter warp [0, V_CONV), producer warp
     // [V_PROD0, +V_PROD), issuer t [V_ISS0 + t V_ISS, +V_ISS).  Measured on
-    // e4m3 B2 H16 N8192 d128 (ms per call, units of 1/32 of a tile per
+    // e4m3 B2 H16 N8192 d128 (ms per call; shares in 32nds of a tile per
     // warp): all on the converter 0.635; converter 16, issuers 8 each 0.605;
-    // 8 each 0.616; issuers 16
-    // each 0.734; converter 16, producer 8, issuers 4 each 0.572-0.581;
-    // converter 20, producer 8, issuers 2 each 0.567-0.571 (kept: the issuers'
-    // MMA issue tolerates little extra work); converter 24, producer 4,
-    // issuers 2 each 0.595; one-unit issuer shares 0.59-0.60.
+    // 8 each on all four warps 0.616; issuers 16 each 0.734; converter 16,
+    // producer 8, issuers 4 each 0.572-0.581; converter 20, producer 8,
+    // issuers 2 each 0.567-0.571 (kept: the issuers' MMA issue tolerates
+    // little extra work); converter 24, producer 4, issuers 2 each 0.595;
+    // one-unit issuer shares 0.59-0.60.
     constexpr int V_CONV = 5 * V_PER / 8, V_ISS = V_PER / 16, V_PROD = V_PER - V_CONV - 2 * V_ISS;
     constexpr int V_PROD0 = V_CONV, V_ISS0 = V_CONV + V_PROD;
     static_assert(V_CONV + V_PROD + 2 * V_ISS == V_PER, "the shares cover every unit");
@@ -363,13 +369,16 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         if (!ok) return false;
         const uint32_t src = smem_u32(sKV + (size_t)slot * C::SLOT);
         const uint32_t dst = smem_u32(sV16 + (size_t)(j & 1) * C::V16BUF);
-        // loads in batches of 8 units (4, 2 or 1 where the share is not a multiple of 8)
-        if ((k_end - k_begin) % 8 == 0) {
+        // Units in batches of NU: the batch's loads all go out before its first
+        // conversion.  Batches of 8, or of 4, 2 or 1 where the share is not a
+        // multiple of 8.
+        auto widen_units = [&](auto nu) {
+            constexpr int NU = decltype(nu)::value;
 #pragma unroll 1
-            for (int k0 = k_begin; k0 < k_end; k0 += 8) {
-                uint32_t x[8][4];
+            for (int k0 = k_begin; k0 < k_end; k0 += NU) {
+                uint32_t x[NU][4];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
+                for (int k = 0; k < NU; ++k) {
                     int rr, w;
                     unit_of(lane + 32 * (k0 + k), rr, w);
                     // e4m3 row rr: 128-byte swizzle (w ^ rr%8) or 64-byte (w ^ (rr/2)%4)
@@ -377,7 +386,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                     ld_shared_v4(src + (uint32_t)(rr * C::CB + wp * 16), x[k]);
                 }
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
+                for (int k = 0; k < NU; ++k) {
                     int rr, w;
                     unit_of(lane + 32 * (k0 + k), rr, w);
                     uint32_t hv[8];
@@ -393,94 +402,16 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                     st_shared_v4(row + (uint32_t)(((u0 + 1) ^ (rr & 7)) << 4), hv[4], hv[5], hv[6], hv[7]);
                 }
             }
-        } else if ((k_end - k_begin) % 4 == 0) {
-#pragma unroll 1
-            for (int k0 = k_begin; k0 < k_end; k0 += 4) {
-                uint32_t x[4][4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    int rr, w;
-                    unit_of(lane + 32 * (k0 + k), rr, w);
-                    // e4m3 row rr: 128-byte swizzle (w ^ rr%8) or 64-byte (w ^ (rr/2)%4)
-                    const int wp = (C::CB == 128) ? (w ^ (rr & 7)) : (w ^ ((rr >> 1) & 3));
-                    ld_shared_v4(src + (uint32_t)(rr * C::CB + wp * 16), x[k]);
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    int rr, w;
-                    unit_of(lane + 32 * (k0 + k), rr, w);
-                    uint32_t hv[8];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        hv[2 * e] = e4m3x2_to_f16x2((uint16_t)(x[k][e] & 0xffffu));
-                        hv[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(x[k][e] >> 16));
-                    }
-                    // values d = 16 w .. 16 w + 15: fp16 chunk w / 4, units 2 (w % 4), +1
-                    const uint32_t row = dst + (uint32_t)((w >> 2) * C::V16_CHUNK + rr * C::V16_CB);
-                    const int u0 = 2 * (w & 3);
-                    st_shared_v4(row + (uint32_t)((u0 ^ (rr & 7)) << 4), hv[0], hv[1], hv[2], hv[3]);
-                    st_shared_v4(row + (uint32_t)(((u0 + 1) ^ (rr & 7)) << 4), hv[4], hv[5], hv[6], hv[7]);
-                }
-            }
-        } else if ((k_end - k_begin) % 2 == 0) {
-#pragma unroll 1
-            for (int k0 = k_begin; k0 < k_end; k0 += 2) {
-                uint32_t x[2][4];
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    int rr, w;
-                    unit_of(lane + 32 * (k0 + k), rr, w);
-                    // e4m3 row rr: 128-byte swizzle (w ^ rr%8) or 64-byte (w ^ (rr/2)%4)
-                    const int wp = (C::CB == 128) ? (w ^ (rr & 7)) : (w ^ ((rr >> 1) & 3));
-                    ld_shared_v4(src + (uint32_t)(rr * C::CB + wp * 16), x[k]);
-                }
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    int rr, w;
-                    unit_of(lane + 32 * (k0 + k), rr, w);
-                    uint32_t hv[8];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        hv[2 * e] = e4m3x2_to_f16x2((uint16_t)(x[k][e] & 0xffffu));
-                        hv[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(x[k][e] >> 16));
-                    }
-                    // values d = 16 w .. 16 w + 15: fp16 chunk w / 4, units 2 (w % 4), +1
-                    const uint32_t row = dst + (uint32_t)((w >> 2) * C::V16_CHUNK + rr * C::V16_CB);
-                    const int u0 = 2 * (w & 3);
-                    st_shared_v4(row + (uint32_t)((u0 ^ (rr & 7)) << 4), hv[0], hv[1], hv[2], hv[3]);
-                    st_shared_v4(row + (uint32_t)(((u0 + 1) ^ (rr & 7)) << 4), hv[4], hv[5], hv[6], hv[7]);
-                }
-            }
-        } else {
-#pragma unroll 1
-            for (int k0 = k_begin; k0 < k_end; k0 += 1) {
-                uint32_t x[1][4];
-#pragma unroll
-                for (int k = 0; k < 1; ++k) {
-                    int rr, w;
-                    unit_of(lane + 32 * (k0 + k), rr, w);
-                    // e4m3 row rr: 128-byte swizzle (w ^ rr%8) or 64-byte (w ^ (rr/2)%4)
-                    const int wp = (C::CB == 128) ? (w ^ (rr & 7)) : (w ^ ((rr >> 1) & 3));
-                    ld_shared_v4(src + (uint32_t)(rr * C::CB + wp * 16), x[k]);
-                }
-#pragma unroll
-                for (int k = 0; k < 1; ++k) {
-                    int rr, w;
-                    unit_of(lane + 32 * (k0 + k), rr, w);
-                    uint32_t hv[8];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        hv[2 * e] = e4m3x2_to_f16x2((uint16_t)(x[k][e] & 0xffffu));
-                        hv[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(x[k][e] >> 16));
-                    }
-                    // values d = 16 w .. 16 w + 15: fp16 chunk w / 4, units 2 (w % 4), +1
-                    const uint32_t row = dst + (uint32_t)((w >> 2) * C::V16_CHUNK + rr * C::V16_CB);
-                    const int u0 = 2 * (w & 3);
-                    st_shared_v4(row + (uint32_t)((u0 ^ (rr & 7)) << 4), hv[0], hv[1], hv[2], hv[3]);
-                    st_shared_v4(row + (uint32_t)(((u0 + 1) ^ (rr & 7)) << 4), hv[4], hv[5], hv[6], hv[7]);
-                }
-            }
-        }
+        };
+        const int n_units = k_end - k_begin;
+        if (n_units % 8 == 0)
+            widen_units(IntC<8>{});
+        else if (n_units % 4 == 0)
+            widen_units(IntC<4>{});
+        else if (n_units % 2 == 0)
+            widen_units(IntC<2>{});
+        else
+            widen_units(IntC<1>{});
         fence_proxy_async_smem();
         __syncwarp();
         mbar_arrive_1(b_v16_full + 8 * (j & 1));
@@ -490,6 +421,17 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
+        // Q_A and Q_B (a tile with no key tile to read is not loaded), once
+        auto load_q = [&] {
+            const int nq = (n_kv[0] > 0) + (n_kv[1] > 0);
+            mbar_arrive_expect_tx(b_q_full, (uint32_t)(nq * C::TILE));
+            for (int t = 0; t < 2; ++t) {
+                if (n_kv[t] == 0) continue;
+                for (int c = 0; c < C::NC; ++c)
+                    tma_load_4d(smem_u32(sQ + t * C::TILE + c * C::CHUNK), &tmQ, b_q_full,
+                                c * (C::CB / C::E), h, q0[t], b);
+            }
+        };
         if constexpr (C::CONV) {
             // The whole warp runs the loop (lane 0 issues the copies) and also
             // widens its share of every V tile: its share of V_c right after
@@ -500,16 +442,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             constexpr int LAG = 3;
             static_assert(!C::CONV || LAG < C::SLOTS / 2, "the producer's share must come before its slot is needed");
             if (n_max > 0) {
-                if (lane == 0) {
-                    const int nq = (n_kv[0] > 0) + (n_kv[1] > 0);
-                    mbar_arrive_expect_tx(b_q_full, (uint32_t)(nq * C::TILE));
-                    for (int t = 0; t < 2; ++t) {
-                        if (n_kv[t] == 0) continue;
-                        for (int c = 0; c < C::NC; ++c)
-                            tma_load_4d(smem_u32(sQ + t * C::TILE + c * C::CHUNK), &tmQ, b_q_full,
-                                        c * (C::CB / C::E), h, q0[t], b);
-                    }
-                }
+                if (lane == 0) load_q();
                 __syncwarp();
                 // item 2j = K_j, item 2j+1 = V_j (the order the MMAs first use them)
                 int it = 0, next_share = 0;
@@ -541,14 +474,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             }
         } else {
             if (lane == 0 && n_max > 0) {
-                const int nq = (n_kv[0] > 0) + (n_kv[1] > 0);
-                mbar_arrive_expect_tx(b_q_full, (uint32_t)(nq * C::TILE));
-                for (int t = 0; t < 2; ++t) {
-                    if (n_kv[t] == 0) continue;
-                    for (int c = 0; c < C::NC; ++c)
-                        tma_load_4d(smem_u32(sQ + t * C::TILE + c * C::CHUNK), &tmQ, b_q_full,
-                                    c * (C::CB / C::E), h, q0[t], b);
-                }
+                load_q();
                 // item 2j = K_j, item 2j+1 = V_j (the order the MMAs first use them)
                 int it = 0;
                 bool ok = true;
@@ -631,98 +557,96 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             auto par_of = [](int it) { return (uint32_t)(it / C::SLOTS) & 1u; };
 
             bool ok = true;
-            {
-                // One issuer per tile; the two share one TMEM score buffer S.
-                // The score MMAs into S run in the order A_0 B_0 A_1 B_1 ...
-                // (a tile past its own key range drops out), and each waits
-                // until the softmax of the one before it has loaded its scores
-                // (s_free).  P_t V_j reads fp16 P_t from TMEM and the fp16 copy
-                // of V_j in buffer j % 2 (widened by the converter warp and both
-                // issuers); the buffer is released when the MMA has read it.
-                // V16G: the fp16 V_j is ring item 2j + 1 itself, released to the
-                // producer by both issuers' P V commits, like K_j.
-                // Key tiles this tile never reads release their K slot and V
-                // buffer once filled (and still get this issuer's share of V).
-                const int t = __shfl_sync(0xffffffffu, warp, 0) - 1;
-                const int nt = n_kv[t], nt_o = n_kv[1 - t];
-                const uint32_t drain_t = t == 0 ? b_drain : b_drain_b;
-                auto s_ready = [&](int j) -> bool {
-                    int pt = -1, pj = 0;  // the score MMA before tile t's j-th
-                    if (t == 0) {
-                        if (j >= 1) {
-                            pt = (j - 1 < nt_o) ? 1 : 0;
-                            pj = j - 1;
-                        }
-                    } else if (j < nt_o) {
-                        pt = 0;
-                        pj = j;
-                    } else if (j >= 1) {
-                        pt = 1;
+            // One issuer per tile; the two share one TMEM score buffer S.
+            // The score MMAs into S run in the order A_0 B_0 A_1 B_1 ...
+            // (a tile past its own key range drops out), and each waits
+            // until the softmax of the one before it has loaded its scores
+            // (s_free).  P_t V_j reads fp16 P_t from TMEM and the fp16 copy
+            // of V_j in buffer j % 2 (widened by the converter warp and both
+            // issuers); the buffer is released when the MMA has read it.
+            // V16G: the fp16 V_j is ring item 2j + 1 itself, released to the
+            // producer by both issuers' P V commits, like K_j.
+            // Key tiles this tile never reads release their K slot and V
+            // buffer once filled (and still get this issuer's share of V).
+            const int t = __shfl_sync(0xffffffffu, warp, 0) - 1;
+            const int nt = n_kv[t], nt_o = n_kv[1 - t];
+            const uint32_t drain_t = t == 0 ? b_drain : b_drain_b;
+            auto s_ready = [&](int j) -> bool {
+                int pt = -1, pj = 0;  // the score MMA before tile t's j-th
+                if (t == 0) {
+                    if (j >= 1) {
+                        pt = (j - 1 < nt_o) ? 1 : 0;
                         pj = j - 1;
                     }
-                    return pt < 0 || wb(b_s_free + 8 * pt, (uint32_t)pj & 1u);
-                };
-                // this issuer's quarter of every V tile's units
-                const int vk0 = V_ISS0 + t * V_ISS, vk1 = vk0 + V_ISS;
-                ok = wb(b_q_full, 0);
-                if (ok && nt > 0) {
-                    ok = wb(b_kv_full + 8 * slot_of(0), par_of(0));
-                    if (ok) ok = s_ready(0);
-                    if (ok) {
-                        tc_fence_after();
-                        issue_qk(t, slot_of(0));
-                        mma_commit_1(b_s_full + 8 * t);
-                        mma_commit_1(b_kv_empty + 8 * slot_of(0));
-                    }
+                } else if (j < nt_o) {
+                    pt = 0;
+                    pj = j;
+                } else if (j >= 1) {
+                    pt = 1;
+                    pj = j - 1;
                 }
-                if constexpr (C::CONV)
-                    if (ok && n_max > 0) ok = widen_share(0, vk0, vk1);
-                for (int j = 0; j < nt && ok; ++j) {
-                    const int itK = 2 * j + 2;
-                    if (j + 1 < nt) {
-                        ok = wb(b_kv_full + 8 * slot_of(itK), par_of(itK));
-                        if (ok) ok = s_ready(j + 1);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_qk(t, slot_of(itK));
-                        mma_commit_1(b_s_full + 8 * t);
-                        mma_commit_1(b_kv_empty + 8 * slot_of(itK));
-                    }
-                    const int itV = 2 * j + 1;
-                    if constexpr (!C::CONV)
-                        ok = wb(b_kv_full + 8 * slot_of(itV), par_of(itV));
-                    else
-                        ok = wb(b_v16_full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u);
-                    if (ok) ok = wb(b_p_full + 8 * t, (uint32_t)j & 1u);
+                return pt < 0 || wb(b_s_free + 8 * pt, (uint32_t)pj & 1u);
+            };
+            // this issuer's quarter of every V tile's units
+            const int vk0 = V_ISS0 + t * V_ISS, vk1 = vk0 + V_ISS;
+            ok = wb(b_q_full, 0);
+            if (ok && nt > 0) {
+                ok = wb(b_kv_full + 8 * slot_of(0), par_of(0));
+                if (ok) ok = s_ready(0);
+                if (ok) {
+                    tc_fence_after();
+                    issue_qk(t, slot_of(0));
+                    mma_commit_1(b_s_full + 8 * t);
+                    mma_commit_1(b_kv_empty + 8 * slot_of(0));
+                }
+            }
+            if constexpr (C::CONV)
+                if (ok && n_max > 0) ok = widen_share(0, vk0, vk1);
+            for (int j = 0; j < nt && ok; ++j) {
+                const int itK = 2 * j + 2;
+                if (j + 1 < nt) {
+                    ok = wb(b_kv_full + 8 * slot_of(itK), par_of(itK));
+                    if (ok) ok = s_ready(j + 1);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_pv(t, C::CONV ? (j & 1) : slot_of(itV), j == 0);
-                    mma_commit_1(b_pv_done + 8 * t);
-                    if constexpr (!C::CONV) {
-                        mma_commit_1(b_kv_empty + 8 * slot_of(itV));
-                    } else {
-                        mma_commit_1(b_v16_empty + 8 * (j & 1));
-                        // the MMAs run on their own: widen this issuer's share of the next V
-                        if (j + 1 < n_max) ok = widen_share(j + 1, vk0, vk1);
-                    }
+                    issue_qk(t, slot_of(itK));
+                    mma_commit_1(b_s_full + 8 * t);
+                    mma_commit_1(b_kv_empty + 8 * slot_of(itK));
                 }
-                for (int j = nt; j < n_max && ok; ++j) {
-                    ok = wb(b_kv_full + 8 * slot_of(2 * j), par_of(2 * j));
-                    if (ok) mbar_arrive_1(b_kv_empty + 8 * slot_of(2 * j));
-                    if constexpr (!C::CONV) {
-                        if (ok) ok = wb(b_kv_full + 8 * slot_of(2 * j + 1), par_of(2 * j + 1));
-                        if (ok) mbar_arrive_1(b_kv_empty + 8 * slot_of(2 * j + 1));
-                    } else {
-                        if (ok) ok = wb(b_v16_full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u);
-                        if (ok) mbar_arrive_1(b_v16_empty + 8 * (j & 1));
-                        if (ok && j + 1 < n_max) ok = widen_share(j + 1, vk0, vk1);
-                    }
+                const int itV = 2 * j + 1;
+                if constexpr (!C::CONV)
+                    ok = wb(b_kv_full + 8 * slot_of(itV), par_of(itV));
+                else
+                    ok = wb(b_v16_full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u);
+                if (ok) ok = wb(b_p_full + 8 * t, (uint32_t)j & 1u);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(t, C::CONV ? (j & 1) : slot_of(itV), j == 0);
+                mma_commit_1(b_pv_done + 8 * t);
+                if constexpr (!C::CONV) {
+                    mma_commit_1(b_kv_empty + 8 * slot_of(itV));
+                } else {
+                    mma_commit_1(b_v16_empty + 8 * (j & 1));
+                    // the MMAs run on their own: widen this issuer's share of the next V
+                    if (j + 1 < n_max) ok = widen_share(j + 1, vk0, vk1);
                 }
-                if (!ok) {
-                    // make sure none of this issuer's MMAs still runs when TMEM is freed
-                    mma_commit_1(drain_t);
-                    wait_drain(drain_t, 0, p.drain_ns);
+            }
+            for (int j = nt; j < n_max && ok; ++j) {
+                ok = wb(b_kv_full + 8 * slot_of(2 * j), par_of(2 * j));
+                if (ok) mbar_arrive_1(b_kv_empty + 8 * slot_of(2 * j));
+                if constexpr (!C::CONV) {
+                    if (ok) ok = wb(b_kv_full + 8 * slot_of(2 * j + 1), par_of(2 * j + 1));
+                    if (ok) mbar_arrive_1(b_kv_empty + 8 * slot_of(2 * j + 1));
+                } else {
+                    if (ok) ok = wb(b_v16_full + 8 * (j & 1), (uint32_t)(j >> 1) & 1u);
+                    if (ok) mbar_arrive_1(b_v16_empty + 8 * (j & 1));
+                    if (ok && j + 1 < n_max) ok = widen_share(j + 1, vk0, vk1);
                 }
+            }
+            if (!ok) {
+                // make sure none of this issuer's MMAs still runs when TMEM is freed
+                mma_commit_1(drain_t);
+                wait_drain(drain_t, 0, p.drain_ns);
             }
         }
         __syncwarp();
@@ -768,7 +692,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                 break;
             }
             tc_fence_after();
-            // all four 32-column loads in flight before one wait
+            // one 128-column load, which also returns the row's maximum
             uint32_t sr[BN];
             float rmx;  // the row's maximum, from the load itself
             tmem_ld128_max(t_row + kColS, sr, rmx);
@@ -885,7 +809,6 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             __syncwarp();
             mbar_arrive_1(p_full);
         }
-
 
         if (ok && nt > 0)
             ok = __all_sync(0xffffffffu, wait_bar(pv_done, (uint32_t)(nt - 1) & 1u, abort_flag, lim));
@@ -1178,12 +1101,12 @@ cudaError_t launch_t(const Problem& pr, cudaStream_t stream, int n_splits = 1,
     p.part_o = part_o;
     p.part_lse = part_lse;
     const long long n_bh = (long long)pr.B * pr.H;
-    // heads scheduled together: their K/V (2 N_k d E bytes each) fill ~48 MiB of L2
-    // Heads scheduled together: their K/V (2 N_k d E bytes per K/V head, a
-    // K/V head shared by H / H_kv query heads) fill ~48 MiB of L2.  The groups
-    // are then evened out so the last one is not a lone small group that
-    // would run by itself at the end.
-    const long long kv_head_bytes = (long long)(pr.N_k > 0 ? pr.N_k : 1) * D * (C::V16G ? 3 : 2 * C::E);
+    // Heads scheduled together: their K/V (2 N_k d E bytes per K/V head, or
+    // 3 N_k d with e4m3 K and fp16 V; a K/V head is shared by H / H_kv query
+    // heads) fill ~48 MiB of L2.  The groups are then evened out so the last
+    // one is not a lone small group that would run by itself at the end.
+    const long long kv_head_bytes =
+        (long long)(pr.N_k > 0 ? pr.N_k : 1) * D * (C::V16G ? 3 : 2 * C::E);
     long long G = (48LL << 20) * (pr.H / pr.H_kv) / kv_head_bytes;
     if (G < 1) G = 1;
     if (G > n_bh) G = n_bh;

@@ -159,49 +159,12 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]; kind::f16 (bf16 / fp16 inputs).
-__device__ __forceinline__ void mma_f16_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                           uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem desc]; kind::f16.
-__device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                           uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
-// kind::f8f6f4 (e4m3 inputs here), both operand forms.
-__device__ __forceinline__ void mma_f8_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_f8_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                          uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
-// Warp-converged forms: every lane of the warp executes the instruction with
-// the same operands and an elect.sync predicate lets exactly one lane issue
-// it.  The operands are then computed by the whole warp (warp-uniform values)
-// instead of inside a one-lane branch.
+// D[tmem] (+)= A * B[smem desc], accumulating when acc != 0.  _ss takes A from
+// shared memory (a descriptor), _ts from TMEM; kind::f16 is for bf16 / fp16
+// operands, kind::f8f6f4 for e4m3 ones.  Every lane of the warp executes the
+// instruction with the same operands and an elect.sync predicate lets exactly
+// one lane issue it, so the operands are computed by the whole warp
+// (warp-uniform values) instead of inside a one-lane branch.
 #define ATTN_ELECT_MMA(KIND_STR, A_FORM)                                              \
     asm volatile("{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\t"              \
                  "elect.sync _|e, 0xffffffff;\n\t"                                       \
@@ -241,14 +204,6 @@ __device__ __forceinline__ void mbar_arrive_1(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
         "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}\n" ::"r"(bar)
-        : "memory");
-}
-
-// Arrive once on an mbarrier when every tcgen05 op issued so far by this
-// thread has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
         : "memory");
 }
 
