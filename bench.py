@@ -16,8 +16,8 @@ one step are 288 MiB (> the 129 MB L2), so no L2 flush is needed.
 Multi-GPU (torchrun): every rank runs its own shard (its own seeds), no
 collective on the data path; value = all ranks' FLOPs / max-over-ranks time.
 
---impl reference times the fp64 CPU oracle (the reference of this port, there
-being no upstream code to run) on a bounded sample of the same workload.
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload: there is no upstream code to run, so the oracle is the reference arm.
 """
 
 from __future__ import annotations
