@@ -3,8 +3,9 @@
  *
  * The operation ("FlashAttention (HI)" page, section "Problems of standard attention",
  * formula Attention(Q,K,V) = softmax(Q K^T / sqrt(d_k)) V; computed as the
- * pages' fused, tiled kernel with an online softmax, sections "Tiling",
- * "Online softmax" and "Fusing operations into one CUDA kernel"):
+ * pages' fused, tiled kernel with an online softmax, sections "Tiling and
+ * block processing", "Online softmax computation" and "Combining operations
+ * in one CUDA kernel"):
  *
  *   for every batch b, head h and query row i
  *     s_j    = scale * <q[b,i,h,:], k[b,j,h,:]>          for j in A(i)

@@ -8,8 +8,9 @@ is present, the calls raise.
 
 Operation: O = softmax(Q K^T * scale [+ causal mask]) V and the per-row
 logsumexp ("FlashAttention (HI)" page, section "Problems of standard attention",
-computed as in its sections "Tiling", "Online softmax" and "Fusing operations
-into one CUDA kernel").  Layout [B, N, H, d], lse [B, H, N_q].
+computed as in its sections "Tiling and block processing", "Online softmax
+computation" and "Combining operations in one CUDA kernel").  Layout
+[B, N, H, d], lse [B, H, N_q].
 """
 
 from __future__ import annotations
