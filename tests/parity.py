@@ -73,6 +73,19 @@ def oracle_full(case, inputs):
     return oracle.attention(q, k, v, case.scale, case.causal)
 
 
+def backward_gqa_reference(q, k, v, dO, scale, causal):
+    """fp64 gradients with K/V shared by H / H_kv query heads: the oracle
+    differentiates the expanded problem (query head h with its own copy of K/V
+    head h // group) and dk, dv are summed over each head's copies, which is
+    the gradient of the shared tensors.  Arrays [B, N, heads, d]."""
+    from oracle import backward
+    B, N_k, H_kv, d = k.shape
+    g = q.shape[2] // H_kv
+    rq, rk, rv = backward.attention_backward(q, np.repeat(k, g, axis=2), np.repeat(v, g, axis=2),
+                                             dO, scale, causal)
+    return rq, rk.reshape(B, N_k, H_kv, g, d).sum(axis=3), rv.reshape(B, N_k, H_kv, g, d).sum(axis=3)
+
+
 def compare(case, O_gpu, lse_gpu, O_ref, lse_ref, tol=None):
     """Element-wise check; rows with lse = -inf must have O == 0 exactly."""
     tol = tol or TOL[case.dtype]
