@@ -22,12 +22,13 @@ import os
 from . import ext_build as _build
 
 __all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_fp8_ws", "attn_fwd_fp8_workspace_bytes",
-           "attn_fwd_simt", "attn_fwd_splitkv", "attn_fwd_gqa",
+           "attn_fwd_simt", "attn_fwd_splitkv", "attn_fwd_splitkv_static", "attn_fwd_gqa",
            "attn_quantize_e4m3",
            "attn_splitkv_workspace_bytes", "attn_splitkv_num_splits", "attn_check_status",
            "attn_status_string",
-           "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_host", "attn_fwd_host_workspace_bytes",
-           "attn_selftest_wait", "attn_selftest_abort",
+           "attn_bwd", "attn_bwd_gqa", "attn_bwd_workspace_bytes", "attn_fwd_host",
+           "attn_fwd_host_workspace_bytes", "attn_selftest_wait", "attn_selftest_abort",
+           "attn_last_cuda_error",
            "AttnError", "lib", "build"]
 
 (ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT,
@@ -332,6 +333,22 @@ def attn_fwd_splitkv(q, k, v, num_splits, o=None, lse=None, scale=None, causal=F
     return o, lse
 
 
+def attn_fwd_splitkv_static(q, k, v, num_splits, o=None, lse=None, scale=None, causal=False,
+                            q_descale=None, k_descale=None, v_descale=None, stream=None):
+    """attn_fwd_splitkv with no caller workspace: the partials go to the
+    library's fixed ATTN_STATIC_SCRATCH_BYTES device array (calls whose work
+    overlaps on the GPU share it).  Pass o and lse to allocate nothing here."""
+    B, N_q, H, d, N_k = _check_inputs(q, k, v)
+    o, lse = _outputs(q, o, lse, B, N_q, H, d)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib().attn_fwd_splitkv_static(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                       _ptr(q_descale), _ptr(k_descale), _ptr(v_descale), B, H,
+                                       N_q, N_k, d, scale, int(bool(causal)), _dtype_code(q),
+                                       int(num_splits), _stream(stream, q.device))
+    _raise(st, "attn_fwd_splitkv_static")
+    return o, lse
+
+
 def attn_bwd_workspace_bytes(B, H, N_q):
     return int(lib().attn_bwd_workspace_bytes(int(B), int(H), int(N_q)))
 
@@ -419,6 +436,16 @@ def attn_bwd(q, k, v, o, lse, dO, scale=None, causal=False, dq=None, dk=None, dv
                             _dtype_code(q), _ptr(workspace), ws_bytes, _stream(stream, q.device))
     _raise(st, "attn_bwd")
     return dq, dk, dv
+
+
+# attn_bwd already takes k, v with H_kv heads dividing H (it calls the C
+# attn_bwd_gqa); the same-name entry point of the C ABI.
+attn_bwd_gqa = attn_bwd
+
+
+def attn_last_cuda_error() -> str:
+    """Name of the CUDA error behind the calling thread's last ATTN_ERR_CUDA."""
+    return lib().attn_last_cuda_error().decode()
 
 
 def attn_selftest_wait(timeout_us=1000, stream=None, device=None):

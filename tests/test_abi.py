@@ -110,6 +110,21 @@ def test_python_binding_refuses_cpu_tensors():
     q = torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         attn.attn_fwd(q, q, q)
+    with pytest.raises(ValueError):
+        attn.attn_fwd_splitkv_static(q, q, q, 2)
+
+
+def test_binding_has_every_declared_entry_point():
+    # the Python binding carries the C ABI's names, one function per entry point
+    declared = set(declared_functions())
+    assert len(declared) >= 20
+    missing = sorted(n for n in declared if not callable(getattr(attn, n, None)))
+    assert not missing, missing
+    assert declared <= set(attn.__all__)
+
+
+def test_last_cuda_error_through_the_binding(L):
+    assert isinstance(attn.attn_last_cuda_error(), str)
 
 
 def test_splitkv_workspace_size(L):
