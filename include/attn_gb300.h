@@ -45,7 +45,8 @@
  * Errors: arguments are checked before anything is launched and give
  *   ATTN_ERR_INVALID_ARG (null pointer, negative size, misaligned pointer,
  *   non-finite or non-positive scale, bad dtype) or ATTN_ERR_UNSUPPORTED
- *   (d not 64, 128 or 256; a grid dimension out of range).  ATTN_ERR_CUDA reports a
+ *   (d not 64, 128 or 256; N_q or N_k above ATTN_MAX_SEQ_LEN; a grid dimension
+ *   out of range).  ATTN_ERR_CUDA reports a
  *   failed tensor-map encode or launch (cudaGetLastError is cleared).
  *   Kernels never trap: every wait inside them is bounded; a wait that runs
  *   out sets a device status word, the kernel returns, and attn_check_status
@@ -266,6 +267,11 @@ ATTN_API attn_status_t attn_fwd_host(const void* q, const void* k, const void* v
 /* Workspace bytes attn_fwd_host needs (0 for invalid or empty arguments). */
 ATTN_API size_t attn_fwd_host_workspace_bytes(int B, int H, int N_q, int N_k, int d,
                                               attn_dtype_t dtype);
+
+/* Longest sequence (N_q, N_k; N of attn_quantize_e4m3) any entry point takes:
+ * row and key indices, and TMA coordinates up to two query tiles past the
+ * end, stay within int.  Longer sequences give ATTN_ERR_UNSUPPORTED. */
+#define ATTN_MAX_SEQ_LEN (2147483647 - 256)
 
 /* Size of the fixed scratch array attn_fwd_splitkv_static uses (bytes). */
 #define ATTN_STATIC_SCRATCH_BYTES (32 * 1024 * 1024)

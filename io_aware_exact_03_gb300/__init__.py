@@ -34,6 +34,7 @@ __all__ = ["attn_fwd", "attn_fwd_fp8", "attn_fwd_fp8_ws", "attn_fwd_fp8_workspac
 (ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT,
  ATTN_ERR_SCRATCH_LIMIT) = range(6)
 ATTN_STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
+ATTN_MAX_SEQ_LEN = 2147483647 - 256
 ATTN_BF16, ATTN_FP16, ATTN_FP8_E4M3, ATTN_FP32 = range(4)
 
 _LIB = None

@@ -18,6 +18,7 @@ attn_status_t validate(const attn::Problem& p) {
     if (p.dtype != attn::kBF16 && p.dtype != attn::kFP16 && p.dtype != attn::kE4M3)
         return ATTN_ERR_INVALID_ARG;
     if (p.d != 64 && p.d != 128 && p.d != 256) return ATTN_ERR_UNSUPPORTED;
+    if (p.N_q > ATTN_MAX_SEQ_LEN || p.N_k > ATTN_MAX_SEQ_LEN) return ATTN_ERR_UNSUPPORTED;
     const bool empty = p.B == 0 || p.H == 0 || p.N_q == 0;
     if (empty) return ATTN_OK;
     if (!p.q || !p.o) return ATTN_ERR_INVALID_ARG;
@@ -216,6 +217,7 @@ attn_status_t attn_quantize_e4m3(const void* x, attn_dtype_t x_dtype, void* code
     if (x_dtype != ATTN_BF16 && x_dtype != ATTN_FP16 && x_dtype != ATTN_FP32)
         return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+    if (N > ATTN_MAX_SEQ_LEN) return ATTN_ERR_UNSUPPORTED;
     if (B == 0 || H == 0) return ATTN_OK;
     if (!descale || !aligned(descale, 4)) return ATTN_ERR_INVALID_ARG;
     if (N > 0 && (!x || !codes || !aligned(codes, 16) || !aligned(x, 16)))
@@ -245,6 +247,7 @@ attn_status_t attn_bwd_gqa(const void* q, const void* k, const void* v, const vo
         return ATTN_ERR_INVALID_ARG;
     }
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (N_q > ATTN_MAX_SEQ_LEN || N_k > ATTN_MAX_SEQ_LEN) return ATTN_ERR_UNSUPPORTED;
     if (B == 0 || H == 0 || (N_q == 0 && N_k == 0)) return ATTN_OK;
     const void* need16[] = {q, k, v, o, dO, dq, dk, dv};
     const bool has_q = N_q > 0, has_k = N_k > 0;

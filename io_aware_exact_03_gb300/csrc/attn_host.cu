@@ -115,6 +115,7 @@ attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o
     if (B < 0 || H < 0 || N_q < 0 || N_k < 0 || !valid_dtype(dt)) return ATTN_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+    if (N_q > ATTN_MAX_SEQ_LEN || N_k > ATTN_MAX_SEQ_LEN) return ATTN_ERR_UNSUPPORTED;
     if (B == 0 || H == 0 || N_q == 0) return ATTN_OK;
     if (!q || !o || (N_k > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
     if (dt == attn::kE4M3 && (!q_descale || !k_descale || !v_descale)) return ATTN_ERR_INVALID_ARG;

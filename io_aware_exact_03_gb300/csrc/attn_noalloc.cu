@@ -66,6 +66,7 @@ extern "C" ATTN_API attn_status_t attn_fwd_splitkv_static(
     if (dtype != ATTN_BF16 && dtype != ATTN_FP16 && dtype != ATTN_FP8_E4M3)
         return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+    if (N_q > ATTN_MAX_SEQ_LEN || N_k > ATTN_MAX_SEQ_LEN) return ATTN_ERR_UNSUPPORTED;
     if (num_splits < 2 || num_splits > attn::kMaxSplits) return ATTN_ERR_INVALID_ARG;
     if (B == 0 || H == 0 || N_q == 0) return ATTN_OK;
     if (!q || !o || (N_k > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;

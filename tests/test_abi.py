@@ -91,6 +91,32 @@ def test_rejects_bad_arguments(L):
     assert call_fwd(L, d=512) == attn.ATTN_ERR_UNSUPPORTED
 
 
+def test_sequence_length_limit(L):
+    # N_q or N_k above ATTN_MAX_SEQ_LEN is refused by every entry point before
+    # any CUDA call (even for an otherwise empty problem); the limit itself is
+    # accepted (B = 0 keeps these calls from launching)
+    over, top = attn.ATTN_MAX_SEQ_LEN + 1, attn.ATTN_MAX_SEQ_LEN
+    U, OK = attn.ATTN_ERR_UNSUPPORTED, attn.ATTN_OK
+    for B, N_q, N_k, want in ((1, over, 16, U), (1, 16, over, U), (0, top, top, OK)):
+        assert call_fwd(L, B=B, N_q=N_q, N_k=N_k) == want
+        fp8 = (P, P, P, P, P, P, P, P, B, 1, N_q, N_k, 128, 0.1, 0)
+        assert L.attn_fwd_fp8(*fp8, None) == want
+        assert L.attn_fwd_fp8_ws(*fp8, P, 1 << 40, None) == want
+        assert L.attn_fwd_simt(*fp8, attn.ATTN_BF16, None) == want
+        assert L.attn_fwd_gqa(P, P, P, P, P, None, None, None, B, 2, 1, N_q, N_k, 64, 0.1, 0,
+                              attn.ATTN_BF16, None) == want
+        assert L.attn_fwd_splitkv(P, P, P, P, P, None, None, None, B, 1, N_q, N_k, 64, 0.1, 0,
+                                  attn.ATTN_BF16, 2, P, 1 << 40, None) == want
+        assert L.attn_fwd_splitkv_static(P, P, P, P, P, None, None, None, B, 1, N_q, N_k, 64,
+                                         0.1, 0, attn.ATTN_BF16, 2, None) == want
+        assert L.attn_bwd(P, P, P, P, P, P, P, P, P, B, 1, N_q, N_k, 64, 0.1, 0, attn.ATTN_BF16,
+                          P, 1 << 40, None) == want
+        assert L.attn_fwd_host(P, P, P, P, P, None, None, None, B, 1, N_q, N_k, 64, 0.1, 0,
+                               attn.ATTN_BF16, 0x100000, 1 << 40, None) == want
+    assert L.attn_quantize_e4m3(P, attn.ATTN_FP32, P, P, 1, over, 1, 64, None, None) == U
+    assert L.attn_quantize_e4m3(P, attn.ATTN_FP32, P, P, 0, top, 1, 64, None, None) == OK
+
+
 def test_empty_problems_launch_nothing(L):
     # B, H or N_q == 0: nothing to compute; returns before any CUDA call
     assert call_fwd(L, B=0, q=None, k=None, v=None, o=None, lse=None) == attn.ATTN_OK
