@@ -200,9 +200,9 @@ def test_one_pass_equals_two_pass_full_C1_C2(oracle_lib):
         assert np.abs(l1 - l2).max() < 1e-12
 
 
-@pytest.mark.parametrize("name", ["C3", "C4", "C5"])
+@pytest.mark.parametrize("name", ["C3", "C4", "C5", "LKV", "D256", "D256F"])
 def test_one_pass_equals_two_pass_sampled(oracle_lib, name):
-    case = synthetic.CASES[name]
+    case = synthetic.CASES.get(name) or synthetic.EXTRA_CASES[name]
     q, k, v = oracle.case_inputs_f64(synthetic.make_inputs(case))
     rows = synthetic.sample_rows(case, 64)
     O1, l1 = oracle.attention_rows(q, k, v, case.scale, case.causal, rows)
