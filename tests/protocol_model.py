@@ -1,0 +1,369 @@
+"""A model of the tensor-core forward kernel's synchronisation, run under random
+interleavings on the CPU.
+
+The kernel (attn_tc_kernel for 16-bit inputs and for e4m3 with V widened once
+per call; with `conv`, e4m3 with V widened on chip) has these roles, and the
+model gives each its own agent:
+
+* the producer warp, filling a ring of K/V slots by TMA (item 2j = K_j,
+  item 2j + 1 = V_j) after waiting for the slot's release (kv_empty);
+* one MMA issuer per query tile t in {A, B}: S = Q_t K_j^T into the one score
+  buffer the two tiles share, in the order A_0, B_0, A_1, B_1, ... (each score
+  MMA waits until the softmax of the one before it has loaded its scores,
+  s_free), then O_t += P_t V_j once P_t is in (p_full); each MMA is followed by
+  commits (s_full, pv_done, and the slot's kv_empty);
+* four softmax warps per tile: wait for the scores (s_full), load them, signal
+  s_free, wait until the previous P_t V has completed (pv_done) before
+  overwriting P_t, then signal p_full; at the end wait for the last P_t V;
+* on-chip widening (`conv`): each e4m3 V tile is widened into fp16 buffer
+  j mod 2 in four shares, by a converter warp, the producer (its share of V_c
+  once V_{c+3} has been loaded) and each issuer (right after its P V of the
+  step before); a share waits for the V tile (kv_full) and for the buffer
+  (v16_empty: both tiles' P V of V_{j-2} done), then arrives on v16_full and
+  on the V slot's release (kv_empty, four releases per V slot); P V reads the
+  fp16 buffer once v16_full is complete and releases it with its commit.
+
+The asynchronous parts are modelled as events the scheduler may take at any
+time: a TMA load lands (completing the slot's kv_full phase); the tensor core
+executes the oldest pending operation of either issuer (one issuer's MMAs and
+commits complete in issue order, the two issuers' interleave freely).
+
+An mbarrier completes a phase once its arrival count and its expected
+transactions are both used up.  A wait for phase n (parity n & 1) passes when
+the barrier's completed-phase count differs in parity from n; that is only the
+right answer when exactly n + 1 phases have completed, so the model raises on
+any pass at another count (a waiter two phases off would be fooled).  It also
+checks every buffer at the moment an operation touches it: the score buffer is
+overwritten only after all four warps of the tile that owns it loaded it, an
+MMA reads the K or V tile it expects, P_t is overwritten only after the
+P_t V that reads it has executed, O_t is rescaled only between two P_t V, and
+a slot is refilled only after every MMA reading it has executed.  A run that
+stops with agents still waiting is a deadlock.
+"""
+
+from __future__ import annotations
+
+import random
+
+
+class ProtocolError(AssertionError):
+    pass
+
+
+class Bar:
+    """An mbarrier: arrival count, expected transactions, completed phases."""
+
+    def __init__(self, name: str, count: int):
+        self.name, self.count, self.pending, self.tx, self.k = name, count, count, 0, 0
+
+    def arrive(self):
+        if self.pending <= 0:
+            raise ProtocolError(f"{self.name}: arrival beyond the count")
+        self.pending -= 1
+        self._complete()
+
+    def expect_tx(self, n: int = 1):
+        self.tx += n
+
+    def land(self):
+        self.tx -= 1
+        if self.tx < 0:
+            raise ProtocolError(f"{self.name}: more bytes landed than expected")
+        self._complete()
+
+    def _complete(self):
+        if self.pending == 0 and self.tx == 0:
+            self.k += 1
+            self.pending = self.count
+
+    def passes(self, n: int) -> bool:
+        """The parity rule of a wait (or test) for phase n."""
+        ok = (self.k & 1) != (n & 1)
+        if ok and self.k != n + 1:
+            raise ProtocolError(f"{self.name}: a wait for phase {n} passed with {self.k} "
+                                f"phases completed")
+        return ok
+
+
+class Kernel:
+    """One CTA: two query tiles with n_kv = (nt_A, nt_B) key tiles each, a ring
+    of `slots` K/V slots.  `mutant` plants one protocol mistake (for the tests
+    that show the model catches it)."""
+
+    LAG = 3   # the producer widens its share of V_c after loading V_{c+LAG}
+
+    def __init__(self, n_kv, slots, seed, mutant=None, conv=False):
+        self.n_kv, self.S, self.mutant, self.conv = tuple(n_kv), slots, mutant, conv
+        if mutant == "lag_half_ring":
+            self.LAG = slots // 2
+        elif conv and (slots % 2 or self.LAG >= slots // 2):
+            raise ValueError("on-chip widening needs an even ring deeper than 2 * LAG")
+        self.n_max = max(n_kv)
+        self.rnd = random.Random(seed)
+        self.q_full = Bar("q_full", 1)
+        self.s_full = [Bar(f"s_full{t}", 1) for t in range(2)]
+        self.p_full = [Bar(f"p_full{t}", 4) for t in range(2)]
+        self.pv_done = [Bar(f"pv_done{t}", 1) for t in range(2)]
+        self.s_free = [Bar(f"s_free{t}", 4) for t in range(2)]
+        release = 1 if mutant == "one_release_per_slot" else 2
+        self.kv_full = [Bar(f"kv_full{s}", 1) for s in range(slots)]
+        # with on-chip widening V items (odd slots) are released by the four warps that widen them
+        self.kv_empty = [Bar(f"kv_empty{s}", 4 if conv and s % 2 else release) for s in range(slots)]
+        self.v16_full = [Bar(f"v16_full{b}", 4) for b in range(2)]
+        self.v16_empty = [Bar(f"v16_empty{b}", 2) for b in range(2)]
+        self.v16_item = [None, None]         # V tile whose shares the fp16 buffer holds
+        self.v16_shares = [set(), set()]
+        self.pv_of_v = {}                    # V index -> P V executed that read it
+        # buffer state
+        self.slot_item = [None] * slots      # item whose bytes are in the slot (None: in flight)
+        self.slot_readers = [0] * slots      # issued MMAs that still have to read the slot
+        self.q_landed = [False, False]
+        self.S_owner = None                  # (t, j) of the scores in the shared buffer
+        self.S_loaded = set()                # softmax warps that loaded them
+        self.P = [[-1] * 4 for _ in range(2)]    # step whose P each warp's rows hold
+        self.pv_done_n = [0, 0]              # P_t V executed
+        self.qk_done_n = [0, 0]              # Q_t K^T executed
+        self.fifo = [[], []]                 # issued, not yet executed tensor-core operations
+        self.landings = []                   # TMA loads in flight: ("q", t) or ("kv", slot, item)
+
+    # ------------------------------------------------------------ roles
+    def producer(self):
+        if self.n_max == 0:
+            return
+        nq = sum(1 for t in range(2) if self.n_kv[t] > 0)
+        self.q_full.expect_tx(nq)
+        self.q_full.arrive()
+        for t in range(2):
+            if self.n_kv[t] > 0:
+                self.landings.append(("q", t))
+        next_share = 0
+        for it in range(2 * self.n_max):
+            slot = it % self.S
+            yield lambda s=slot, n=it // self.S - 1: self.kv_empty[s].passes(n)
+            if self.slot_readers[slot]:
+                raise ProtocolError(f"slot {slot} refilled with item {it} while an MMA still "
+                                    f"has to read item {self.slot_item[slot]}")
+            self.slot_item[slot] = None
+            self.kv_full[slot].expect_tx()
+            self.kv_full[slot].arrive()
+            self.landings.append(("kv", slot, it))
+            if self.conv and it % 2 and it // 2 >= self.LAG:
+                yield from self.widen_share(next_share, "producer")
+                next_share += 1
+        while self.conv and next_share < self.n_max:
+            yield from self.widen_share(next_share, "producer")
+            next_share += 1
+
+    def widen_share(self, j, who):
+        """One warp's share of V_j: e4m3 ring slot -> fp16 buffer j mod 2."""
+        it, b = 2 * j + 1, j % 2
+        slot = it % self.S
+        yield lambda: self.kv_full[slot].passes(it // self.S)
+        if self.mutant != "no_v16_empty_wait":
+            yield lambda: self.v16_empty[b].passes(j // 2 - 1)
+        if self.slot_item[slot] != it:
+            raise ProtocolError(f"{who} widened slot {slot} holding {self.slot_item[slot]} as V_{j}")
+        if j >= 2 and self.pv_of_v.get(j - 2, 0) != sum(n > j - 2 for n in self.n_kv):
+            raise ProtocolError(f"{who} overwrote fp16 V_{j - 2} before both P V read it")
+        if self.v16_item[b] != j:
+            self.v16_item[b], self.v16_shares[b] = j, set()
+        self.slot_readers[slot] += 1
+        yield None                                       # loads, conversion, stores
+        self.slot_readers[slot] -= 1
+        self.v16_shares[b].add(who)
+        self.v16_full[b].arrive()
+        self.kv_empty[slot].arrive()
+
+    def converter(self):
+        for j in range(self.n_max if self.conv else 0):
+            yield from self.widen_share(j, "converter")
+
+    def issuer(self, t):
+        nt, nt_o = self.n_kv[t], self.n_kv[1 - t]
+        if self.n_max == 0:
+            return
+        S = self.S
+
+        def wait_full(it):
+            return lambda: self.kv_full[it % S].passes(it // S)
+
+        def s_ready(j):
+            # the score MMA before tile t's j-th in the order A_0 B_0 A_1 B_1 ...
+            if t == 0:
+                prev = ((1 if j - 1 < nt_o else 0), j - 1) if j >= 1 else None
+            elif j < nt_o:
+                prev = (0, j)
+            else:
+                prev = (1, j - 1) if j >= 1 else None
+            if prev is None or self.mutant == "no_s_free_wait":
+                return None
+            pt, pj = prev
+            return lambda: self.s_free[pt].passes(pj)
+
+        def issue(op, slot):
+            self.slot_readers[slot] += 1
+            self.fifo[t].append(op)
+
+        yield lambda: self.q_full.passes(0)
+        if nt > 0:
+            yield wait_full(0)
+            w = s_ready(0)
+            if w:
+                yield w
+            issue(("qk", t, 0, 0 % S), 0 % S)
+            self.fifo[t] += [("commit", self.s_full[t]), ("commit", self.kv_empty[0 % S])]
+        if self.conv:
+            yield from self.issuer_conv(t, wait_full, s_ready, issue)
+            return
+        for j in range(nt):
+            itK, itV = 2 * j + 2, 2 * j + 1
+            if j + 1 < nt:
+                yield wait_full(itK)
+                w = s_ready(j + 1)
+                if w:
+                    yield w
+                issue(("qk", t, j + 1, itK % S), itK % S)
+                self.fifo[t] += [("commit", self.s_full[t]), ("commit", self.kv_empty[itK % S])]
+            yield wait_full(itV)
+            yield lambda j=j: self.p_full[t].passes(j)
+            issue(("pv", t, j, itV % S), itV % S)
+            self.fifo[t] += [("commit", self.pv_done[t]), ("commit", self.kv_empty[itV % S])]
+        for j in range(nt, self.n_max):
+            # key tiles this tile never reads: release the slots once filled
+            for it in (2 * j, 2 * j + 1):
+                yield wait_full(it)
+                self.kv_empty[it % S].arrive()
+
+    def issuer_conv(self, t, wait_full, s_ready, issue):
+        nt, S = self.n_kv[t], self.S
+        who = f"issuer{t}"
+        yield from self.widen_share(0, who)
+        for j in range(nt):
+            itK = 2 * j + 2
+            if j + 1 < nt:
+                yield wait_full(itK)
+                w = s_ready(j + 1)
+                if w:
+                    yield w
+                issue(("qk", t, j + 1, itK % S), itK % S)
+                self.fifo[t] += [("commit", self.s_full[t]), ("commit", self.kv_empty[itK % S])]
+            yield lambda j=j: self.v16_full[j % 2].passes(j // 2)
+            yield lambda j=j: self.p_full[t].passes(j)
+            self.fifo[t] += [("pv16", t, j, j % 2), ("commit", self.pv_done[t]),
+                             ("commit", self.v16_empty[j % 2])]
+            if j + 1 < self.n_max:
+                yield from self.widen_share(j + 1, who)
+        for j in range(nt, self.n_max):
+            yield wait_full(2 * j)
+            self.kv_empty[(2 * j) % S].arrive()
+            yield lambda j=j: self.v16_full[j % 2].passes(j // 2)
+            self.v16_empty[j % 2].arrive()
+            if j + 1 < self.n_max:
+                yield from self.widen_share(j + 1, who)
+
+    def softmax(self, t, w):
+        nt = self.n_kv[t]
+        s_pre = False
+        for j in range(nt):
+            if not s_pre:
+                yield lambda j=j: self.s_full[t].passes(j)
+            if self.S_owner != (t, j):
+                raise ProtocolError(f"softmax {t}.{w} step {j} found the scores of {self.S_owner}")
+            self.S_loaded.add(w)
+            self.s_free[t].arrive()
+            pv_pre = j > 0 and self.pv_done[t].passes(j - 1)
+            yield None                                   # exponentials
+            if j > 0 and not pv_pre and self.mutant != "no_pv_wait":
+                yield lambda j=j: self.pv_done[t].passes(j - 1)
+            if self.pv_done_n[t] < j:
+                raise ProtocolError(f"softmax {t}.{w} overwrote P of step {j - 1} before its P V ran")
+            self.P[t][w] = j
+            s_pre = j + 1 < nt and self.s_full[t].passes(j + 1)
+            if self.pv_done_n[t] != j:                   # the O rescale of this step
+                raise ProtocolError(f"softmax {t}.{w} rescaled O while P V {self.pv_done_n[t]} ran")
+            yield None
+            self.p_full[t].arrive()
+        if nt > 0:
+            yield lambda: self.pv_done[t].passes(nt - 1)
+            if self.pv_done_n[t] != nt or self.qk_done_n[t] != nt:
+                raise ProtocolError(f"epilogue of tile {t} ran before its MMAs completed")
+
+    # ------------------------------------------------------- async events
+    def land(self, ev):
+        if ev[0] == "q":
+            self.q_landed[ev[1]] = True
+            self.q_full.land()
+        else:
+            _, slot, it = ev
+            self.slot_item[slot] = it
+            self.kv_full[slot].land()
+
+    def execute(self, t):
+        op = self.fifo[t].pop(0)
+        if op[0] == "commit":
+            op[1].arrive()
+            return
+        kind, tt, j, slot = op
+        if kind == "pv16":
+            b = slot
+            if self.v16_item[b] != j or len(self.v16_shares[b]) != 4:
+                raise ProtocolError(f"P V ({tt}, {j}) read fp16 buffer {b} holding V_{self.v16_item[b]} "
+                                    f"({len(self.v16_shares[b])} of 4 shares)")
+            if any(p != j for p in self.P[tt]) or self.pv_done_n[tt] != j:
+                raise ProtocolError(f"P V ({tt}, {j}) out of step")
+            self.pv_done_n[tt] += 1
+            self.pv_of_v[j] = self.pv_of_v.get(j, 0) + 1
+            return
+        if kind == "qk":
+            if self.slot_item[slot] != 2 * j or not self.q_landed[tt]:
+                raise ProtocolError(f"Q K^T ({tt}, {j}) read slot {slot} holding {self.slot_item[slot]}")
+            if self.S_owner is not None and len(self.S_loaded) < 4:
+                raise ProtocolError(f"Q K^T ({tt}, {j}) overwrote the unloaded scores of {self.S_owner}")
+            if self.qk_done_n[tt] != j:
+                raise ProtocolError("score MMAs of one tile out of order")
+            self.S_owner, self.S_loaded = (tt, j), set()
+            self.qk_done_n[tt] += 1
+        else:
+            if self.slot_item[slot] != 2 * j + 1:
+                raise ProtocolError(f"P V ({tt}, {j}) read slot {slot} holding {self.slot_item[slot]}")
+            if any(p != j for p in self.P[tt]):
+                raise ProtocolError(f"P V ({tt}, {j}) read P of steps {self.P[tt]}")
+            if self.pv_done_n[tt] != j:
+                raise ProtocolError("P V of one tile out of order")
+            self.pv_done_n[tt] += 1
+        self.slot_readers[slot] -= 1
+
+    # ---------------------------------------------------------- scheduler
+    def run(self, max_events=200000):
+        agents = [self.producer(), self.issuer(0), self.issuer(1), self.converter()]
+        agents += [self.softmax(t, w) for t in range(2) for w in range(4)]
+        waits = [None] * len(agents)
+        alive = [True] * len(agents)
+        for _ in range(max_events):
+            choices = [("agent", i) for i, a in enumerate(agents)
+                       if alive[i] and (waits[i] is None or waits[i]())]
+            choices += [("land", k) for k in range(len(self.landings))]
+            choices += [("mma", t) for t in range(2) if self.fifo[t]]
+            if not choices:
+                if any(alive):
+                    raise ProtocolError("deadlock: agents " + ", ".join(
+                        str(i) for i in range(len(agents)) if alive[i]) + " wait forever")
+                break
+            kind, i = self.rnd.choice(choices)
+            if kind == "land":
+                self.land(self.landings.pop(i))
+            elif kind == "mma":
+                self.execute(i)
+            else:
+                try:
+                    waits[i] = next(agents[i])
+                except StopIteration:
+                    alive[i] = False
+        else:
+            raise ProtocolError("no end within the event budget")
+        for b in ([self.q_full] + self.s_full + self.p_full + self.pv_done + self.s_free
+                  + self.kv_full + self.kv_empty + self.v16_full + self.v16_empty):
+            if b.pending != b.count or b.tx:
+                raise ProtocolError(f"{b.name} left with a partial phase")
+        if self.pv_done_n != [n for n in self.n_kv]:
+            raise ProtocolError("not every P V ran")

@@ -1,0 +1,57 @@
+"""The forward kernel's barrier protocol under random interleavings (CPU).
+
+tests/protocol_model.py restates the synchronisation of attn_tc_kernel for
+16-bit inputs, for e4m3 with V widened once per call and for e4m3 with V
+widened on chip (the producer's K/V ring, one MMA issuer per query tile, the
+score buffer the two tiles share, the softmax warps, the four V shares) and
+checks, at every step of thousands of random schedules, that no mbarrier
+parity wait is fooled, no buffer is read before it is written or overwritten
+while still needed, and nothing deadlocks.  The planted mistakes below (a slot
+released by one issuer only, a score MMA that does not wait for the other
+tile's softmax, a softmax that overwrites P without waiting for the P V
+reading it, a V share that does not wait for its fp16 buffer, the producer's
+share lagging by half the ring) must each be caught.
+"""
+
+import pytest
+
+from protocol_model import Kernel, ProtocolError
+
+# ring depths the kernel uses: 5 slots (16-bit, d = 128), 6 (e4m3 K with
+# fp16 V, d = 128), 8 (d = 64)
+SLOTS = (5, 6, 8)
+# key tiles of query tiles A and B: non-causal, causal (B one tile more),
+# ragged (a tile with no key, or past the end of the queries), and a split-KV
+# share; (0, 0) launches nothing
+N_KV = [(1, 1), (2, 2), (5, 5), (9, 9), (1, 2), (3, 4), (7, 8), (0, 1), (2, 0), (3, 0),
+        (0, 0), (2, 3)]
+
+
+@pytest.mark.parametrize("slots", SLOTS)
+@pytest.mark.parametrize("n_kv", N_KV, ids=lambda n: f"{n[0]}x{n[1]}")
+def test_protocol_holds_under_random_schedules(n_kv, slots):
+    for seed in range(60):
+        Kernel(n_kv, slots, seed=1000 * slots + seed).run()
+
+
+@pytest.mark.parametrize("n_kv", N_KV, ids=lambda n: f"{n[0]}x{n[1]}")
+def test_on_chip_widening_protocol_holds_under_random_schedules(n_kv):
+    # e4m3 with V widened on chip: 8 slots, K in even slots and V in odd ones
+    for seed in range(60):
+        Kernel(n_kv, 8, seed=seed, conv=True).run()
+
+
+@pytest.mark.parametrize("mutant,conv", [("one_release_per_slot", False), ("no_s_free_wait", False),
+                                         ("no_pv_wait", False), ("no_v16_empty_wait", True),
+                                         ("lag_half_ring", True)])
+def test_planted_protocol_mistakes_are_caught(mutant, conv):
+    # (the producer's share lagging by half the ring deadlocks: the slot it
+    # waits to refill is released only by its own share, which comes later)
+    caught = 0
+    for seed in range(200):
+        for n_kv in [(3, 4), (5, 5)]:
+            try:
+                Kernel(n_kv, 8 if conv else 5, seed=seed, mutant=mutant, conv=conv).run()
+            except ProtocolError:
+                caught += 1
+    assert caught > 0, f"{mutant} was never caught"
