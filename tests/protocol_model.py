@@ -1,5 +1,6 @@
-"""A model of the tensor-core forward kernel's synchronisation, run under random
-interleavings on the CPU.
+"""Models of the tensor-core forward kernels' synchronisation, run under random
+interleavings on the CPU (Kernel: attn_tc_kernel, d = 64 / 128; Kernel256:
+attn_tc256_kernel, described in its own docstring).
 
 The kernel (attn_tc_kernel for 16-bit inputs and for e4m3 with V widened once
 per call; with `conv`, e4m3 with V widened on chip) has these roles, and the
@@ -85,10 +86,54 @@ class Bar:
         return ok
 
 
-class Kernel:
-    """One CTA: two query tiles with n_kv = (nt_A, nt_B) key tiles each, a ring
-    of `slots` K/V slots.  `mutant` plants one protocol mistake (for the tests
-    that show the model catches it)."""
+class Model:
+    """Random scheduler shared by the kernel models: at each step it takes one
+    of the runnable agents (a generator whose last yielded wait now passes, or
+    that yielded None), a TMA load in flight, or the oldest pending operation of
+    one MMA issuer, uniformly at random."""
+
+    def agents(self):
+        raise NotImplementedError
+
+    def barriers(self):
+        raise NotImplementedError
+
+    def run(self, max_events=200000):
+        agents = self.agents()
+        waits = [None] * len(agents)
+        alive = [True] * len(agents)
+        for _ in range(max_events):
+            choices = [("agent", i) for i, a in enumerate(agents)
+                       if alive[i] and (waits[i] is None or waits[i]())]
+            choices += [("land", k) for k in range(len(self.landings))]
+            choices += [("mma", t) for t in range(len(self.fifo)) if self.fifo[t]]
+            if not choices:
+                if any(alive):
+                    raise ProtocolError("deadlock: agents " + ", ".join(
+                        str(i) for i in range(len(agents)) if alive[i]) + " wait forever")
+                break
+            kind, i = self.rnd.choice(choices)
+            if kind == "land":
+                self.land(self.landings.pop(i))
+            elif kind == "mma":
+                self.execute(i)
+            else:
+                try:
+                    waits[i] = next(agents[i])
+                except StopIteration:
+                    alive[i] = False
+        else:
+            raise ProtocolError("no end within the event budget")
+        for b in self.barriers():
+            if b.pending != b.count or b.tx:
+                raise ProtocolError(f"{b.name} left with a partial phase")
+        self.finish()
+
+
+class Kernel(Model):
+    """attn_tc_kernel, one CTA: two query tiles with n_kv = (nt_A, nt_B) key
+    tiles each, a ring of `slots` K/V slots.  `mutant` plants one protocol
+    mistake (for the tests that show the model catches it)."""
 
     LAG = 3   # the producer widens its share of V_c after loading V_{c+LAG}
 
@@ -334,36 +379,226 @@ class Kernel:
         self.slot_readers[slot] -= 1
 
     # ---------------------------------------------------------- scheduler
-    def run(self, max_events=200000):
-        agents = [self.producer(), self.issuer(0), self.issuer(1), self.converter()]
-        agents += [self.softmax(t, w) for t in range(2) for w in range(4)]
-        waits = [None] * len(agents)
-        alive = [True] * len(agents)
-        for _ in range(max_events):
-            choices = [("agent", i) for i, a in enumerate(agents)
-                       if alive[i] and (waits[i] is None or waits[i]())]
-            choices += [("land", k) for k in range(len(self.landings))]
-            choices += [("mma", t) for t in range(2) if self.fifo[t]]
-            if not choices:
-                if any(alive):
-                    raise ProtocolError("deadlock: agents " + ", ".join(
-                        str(i) for i in range(len(agents)) if alive[i]) + " wait forever")
-                break
-            kind, i = self.rnd.choice(choices)
-            if kind == "land":
-                self.land(self.landings.pop(i))
-            elif kind == "mma":
-                self.execute(i)
-            else:
-                try:
-                    waits[i] = next(agents[i])
-                except StopIteration:
-                    alive[i] = False
-        else:
-            raise ProtocolError("no end within the event budget")
-        for b in ([self.q_full] + self.s_full + self.p_full + self.pv_done + self.s_free
-                  + self.kv_full + self.kv_empty + self.v16_full + self.v16_empty):
-            if b.pending != b.count or b.tx:
-                raise ProtocolError(f"{b.name} left with a partial phase")
+    def agents(self):
+        return ([self.producer(), self.issuer(0), self.issuer(1), self.converter()]
+                + [self.softmax(t, w) for t in range(2) for w in range(4)])
+
+    def barriers(self):
+        return ([self.q_full] + self.s_full + self.p_full + self.pv_done + self.s_free
+                + self.kv_full + self.kv_empty + self.v16_full + self.v16_empty)
+
+    def finish(self):
         if self.pv_done_n != [n for n in self.n_kv]:
             raise ProtocolError("not every P V ran")
+
+
+class Kernel256(Model):
+    """attn_tc256_kernel, one CTA: one 128-row query tile, n key tiles.
+
+    Two score buffers: the scores of key tile j go to buffer j mod 2 and the
+    softmax writes P_j over them; the one MMA issuer sends P_j V_j and then the
+    scores of key tile j + 2 into the same buffer (its MMAs run in issue order).
+    The softmax can therefore run two key tiles ahead of the issuer's wait for
+    P, so P has one barrier per buffer (p_full), and the epilogue waits on
+    o_done, committed once after the last P V.  An occasional O rescale waits
+    for the previous P V (pv_done).  The ring moves half tiles: 16-bit inputs
+    load K_0, K_1, then V_j, K_{j+2}, ... (one release per item, by the issuer's
+    commit); e4m3 (`e4m3`) loads K_0, V_0, K_1, V_1, ... into 4 slots, so slots
+    0-1 only ever hold K and 2-3 only V, and two converter warps widen V_j's
+    halves into fp16 buffer j mod 2 (each frees its slot once its half is in
+    registers, then waits for the buffer: v16_empty, the P V of V_{j-2})."""
+
+    def __init__(self, n, seed, e4m3=False, mutant=None):
+        self.n, self.e4, self.mutant = n, e4m3, mutant
+        self.S = 4 if e4m3 else 5
+        self.rnd = random.Random(seed)
+        self.q_full = Bar("q_full", 1)
+        self.s_full = [Bar(f"s_full{b}", 1) for b in range(2)]
+        p0 = Bar("p_full0", 4)
+        self.p_full = [p0, p0] if mutant == "one_p_barrier" else [p0, Bar("p_full1", 4)]
+        self.pv_done = Bar("pv_done", 1)
+        self.o_done = Bar("o_done", 1)
+        self.v16_full = [Bar(f"v16_full{b}", 2) for b in range(2)]
+        self.v16_empty = [Bar(f"v16_empty{b}", 1) for b in range(2)]
+        self.kv_full = [Bar(f"kv_full{s}", 1) for s in range(self.S)]
+        self.kv_empty = [Bar(f"kv_empty{s}", 1) for s in range(self.S)]
+        self.slot_item = [None] * self.S
+        self.slot_readers = [0] * self.S
+        self.q_landed = False
+        self.buf = [[None] * 4 for _ in range(2)]   # per softmax warp: ("S", j) or ("P", j)
+        self.v16 = [[None, None], [None, None]]     # V index in each half of each fp16 buffer
+        self.pv_n = self.qk_n = 0
+        self.fifo = [[]]
+        self.landings = []
+
+    def groups(self):
+        n = self.n
+        if self.e4:
+            return [(g % 2 == 1, g // 2) for g in range(2 * n)]
+        order = [(False, t) for t in range(min(2, n))]
+        for j in range(n):
+            order.append((True, j))
+            if j + 2 < n:
+                order.append((False, j + 2))
+        return order
+
+    def producer(self):
+        if self.n == 0:
+            return
+        self.q_full.expect_tx()
+        self.q_full.arrive()
+        self.landings.append(("q",))
+        it = 0
+        for is_v, t in self.groups():
+            for half in range(2):
+                slot = it % self.S
+                yield lambda s=slot, n=it // self.S - 1: self.kv_empty[s].passes(n)
+                if self.slot_readers[slot]:
+                    raise ProtocolError(f"slot {slot} refilled while {self.slot_item[slot]} is read")
+                self.slot_item[slot] = None
+                self.kv_full[slot].expect_tx()
+                self.kv_full[slot].arrive()
+                self.landings.append(("kv", slot, (is_v, t, half)))
+                it += 1
+
+    def issuer(self):
+        n, S = self.n, self.S
+        if n == 0:
+            return
+        yield lambda: self.q_full.passes(0)
+
+        def wait_items(pos):
+            for q in (pos, pos + 1):
+                yield lambda q=q: self.kv_full[q % S].passes(q // S)
+
+        def qk(j, b, pos):
+            for q in (pos, pos + 1):
+                self.slot_readers[q % S] += 1
+            self.fifo[0] += [("qk", j, b, pos), ("commit", self.s_full[b]),
+                             ("commit", self.kv_empty[pos % S]), ("commit", self.kv_empty[(pos + 1) % S])]
+
+        it = 0
+        for t in range(min(2, n)):
+            pos = 4 * t if self.e4 else it
+            yield from wait_items(pos)
+            qk(t, t, pos)
+            it += 2
+        for j in range(n):
+            b = j & 1
+            if self.e4:
+                yield lambda j=j: self.v16_full[j & 1].passes(j >> 1)
+            else:
+                yield from wait_items(it)
+            yield lambda j=j, b=b: self.p_full[b].passes(j if self.mutant == "one_p_barrier" else j >> 1)
+            ops = [("pv", j, b, None if self.e4 else it), ("commit", self.pv_done)]
+            if j + 1 == n:
+                ops.append(("commit", self.o_done))
+            if self.e4:
+                ops.append(("commit", self.v16_empty[b]))
+            else:
+                for q in (it, it + 1):
+                    self.slot_readers[q % S] += 1
+                ops += [("commit", self.kv_empty[it % S]), ("commit", self.kv_empty[(it + 1) % S])]
+            self.fifo[0] += ops
+            it += 2
+            if j + 2 < n:
+                pos = 4 * (j + 2) if self.e4 else it
+                yield from wait_items(pos)
+                qk(j + 2, b, pos)
+                it += 2
+
+    def converter(self, hh):
+        for jv in range(self.n if self.e4 else 0):
+            it = 4 * jv + 2 + hh
+            slot = it % self.S
+            yield lambda: self.kv_full[slot].passes(it // self.S)
+            if self.slot_item[slot] != (True, jv, hh):
+                raise ProtocolError(f"converter {hh} found {self.slot_item[slot]} for V_{jv}")
+            self.slot_readers[slot] += 1
+            yield None                                   # the half tile into registers
+            self.slot_readers[slot] -= 1
+            self.kv_empty[slot].arrive()
+            yield lambda: self.v16_empty[jv & 1].passes((jv >> 1) - 1)
+            if jv >= 2 and self.pv_n < jv - 1:
+                raise ProtocolError(f"converter {hh} overwrote fp16 V_{jv - 2} before its P V")
+            self.v16[jv & 1][hh] = None
+            yield None                                   # conversion and stores
+            self.v16[jv & 1][hh] = jv
+            self.v16_full[jv & 1].arrive()
+
+    def softmax(self, w):
+        for j in range(self.n):
+            b = j & 1
+            yield lambda j=j, b=b: self.s_full[b].passes(j >> 1)
+            if self.buf[b][w] != ("S", j):
+                raise ProtocolError(f"softmax {w} step {j} found {self.buf[b][w]} in buffer {b}")
+            yield None                                   # exponentials
+            self.buf[b][w] = ("P", j)
+            if j > 0 and self.rnd.random() < 0.3:        # this warp rescales O
+                yield lambda j=j: self.pv_done.passes(j - 1)
+                if self.pv_n != j:
+                    raise ProtocolError(f"softmax {w} rescaled O at step {j} with {self.pv_n} P V done")
+            yield None
+            self.p_full[b].arrive()
+        if self.n > 0:
+            if self.mutant == "epilogue_on_pv_done":
+                yield lambda: self.pv_done.passes(self.n - 1)
+            else:
+                yield lambda: self.o_done.passes(0)
+            if self.pv_n != self.n:
+                raise ProtocolError(f"epilogue read O with {self.pv_n} of {self.n} P V done")
+
+    def land(self, ev):
+        if ev[0] == "q":
+            self.q_landed = True
+            self.q_full.land()
+        else:
+            _, slot, item = ev
+            self.slot_item[slot] = item
+            self.kv_full[slot].land()
+
+    def execute(self, _):
+        op = self.fifo[0].pop(0)
+        if op[0] == "commit":
+            op[1].arrive()
+            return
+        kind, j, b, pos = op
+        S = self.S
+        if kind == "qk":
+            got = [self.slot_item[q % S] for q in (pos, pos + 1)]
+            if got != [(False, j, 0), (False, j, 1)] or not self.q_landed:
+                raise ProtocolError(f"Q K^T {j} read {got}")
+            if j >= 2 and (any(c != ("P", j - 2) for c in self.buf[b]) or self.pv_n < j - 1):
+                raise ProtocolError(f"Q K^T {j} overwrote buffer {b} holding {self.buf[b]}")
+            if self.qk_n != j:
+                raise ProtocolError("score MMAs out of order")
+            self.buf[b] = [("S", j)] * 4
+            self.qk_n += 1
+        else:
+            if self.e4:
+                if self.v16[b] != [j, j]:
+                    raise ProtocolError(f"P V {j} read fp16 buffer {b} holding {self.v16[b]}")
+            else:
+                got = [self.slot_item[q % S] for q in (pos, pos + 1)]
+                if got != [(True, j, 0), (True, j, 1)]:
+                    raise ProtocolError(f"P V {j} read {got}")
+                for q in (pos, pos + 1):
+                    self.slot_readers[q % S] -= 1
+            if any(c != ("P", j) for c in self.buf[b]) or self.pv_n != j:
+                raise ProtocolError(f"P V {j} read buffer {b} holding {self.buf[b]}")
+            self.pv_n += 1
+            return
+        for q in (pos, pos + 1):
+            self.slot_readers[q % S] -= 1
+
+    def agents(self):
+        return ([self.producer(), self.issuer(), self.converter(0), self.converter(1)]
+                + [self.softmax(w) for w in range(4)])
+
+    def barriers(self):
+        return ([self.q_full, self.pv_done, self.o_done] + self.s_full + list({id(b): b for b in self.p_full}.values())
+                + self.v16_full + self.v16_empty + self.kv_full + self.kv_empty)
+
+    def finish(self):
+        if self.pv_n != self.n or self.qk_n != self.n:
+            raise ProtocolError("not every MMA ran")

@@ -10,12 +10,16 @@ while still needed, and nothing deadlocks.  The planted mistakes below (a slot
 released by one issuer only, a score MMA that does not wait for the other
 tile's softmax, a softmax that overwrites P without waiting for the P V
 reading it, a V share that does not wait for its fp16 buffer, the producer's
-share lagging by half the ring) must each be caught.
+share lagging by half the ring) must each be caught.  The head-dimension-256
+kernel (attn_tc256_kernel: one query tile, two score buffers with P written
+over its scores, half-tile ring items, two V converters for e4m3) gets the
+same treatment, with its two historical hazards planted: one P barrier for
+both buffers, and an epilogue that waits on pv_done instead of o_done.
 """
 
 import pytest
 
-from protocol_model import Kernel, ProtocolError
+from protocol_model import Kernel, Kernel256, ProtocolError
 
 # ring depths the kernel uses: 5 slots (16-bit, d = 128), 6 (e4m3 K with
 # fp16 V, d = 128), 8 (d = 64)
@@ -52,6 +56,25 @@ def test_planted_protocol_mistakes_are_caught(mutant, conv):
         for n_kv in [(3, 4), (5, 5)]:
             try:
                 Kernel(n_kv, 8 if conv else 5, seed=seed, mutant=mutant, conv=conv).run()
+            except ProtocolError:
+                caught += 1
+    assert caught > 0, f"{mutant} was never caught"
+
+
+@pytest.mark.parametrize("e4m3", [False, True], ids=["bf16", "e4m3"])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 8, 17])
+def test_d256_protocol_holds_under_random_schedules(n, e4m3):
+    for seed in range(60):
+        Kernel256(n, seed, e4m3=e4m3).run()
+
+
+@pytest.mark.parametrize("mutant", ["one_p_barrier", "epilogue_on_pv_done"])
+def test_d256_planted_mistakes_are_caught(mutant):
+    caught = 0
+    for seed in range(200):
+        for e4m3 in (False, True):
+            try:
+                Kernel256(5, seed, e4m3=e4m3, mutant=mutant).run()
             except ProtocolError:
                 caught += 1
     assert caught > 0, f"{mutant} was never caught"
