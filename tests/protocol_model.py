@@ -602,3 +602,287 @@ class Kernel256(Model):
     def finish(self):
         if self.pv_n != self.n or self.qk_n != self.n:
             raise ProtocolError("not every MMA ran")
+
+
+class KernelBwdDkdv(Model):
+    """bwd_dkdv_kernel, one CTA: one 128-key tile of one K/V head, `steps`
+    query tiles.  K and V are loaded once (kv_full); each step's item (Q, dO,
+    lse and D of 128 queries) comes through a ring of `slots`.  The issuer sends
+    S^T = K Q^T and dP^T = V dO^T (commit s_full), then for each half of the
+    queries waits for that half's P^T / dS^T (p_half, 4 warps each), sends the
+    accumulating dV, dK MMAs, and after both halves releases the item
+    (item_empty); acc_done after the last step.  Eight elementwise warps, two
+    groups of four (one per query half), read S^T, dP^T and the item's lse / D,
+    write P^T / dS^T over their half's columns and arrive on p_half."""
+
+    def __init__(self, steps, slots, seed):
+        self.n, self.S = steps, slots
+        self.rnd = random.Random(seed)
+        self.kv_full = Bar("kv_full", 1)
+        self.s_full = Bar("s_full", 1)
+        self.p_half = [Bar("p_half0", 4), Bar("p_half1", 4)]
+        self.acc_done = Bar("acc_done", 1)
+        self.item_full = [Bar(f"item_full{s}", 1) for s in range(slots)]
+        self.item_empty = [Bar(f"item_empty{s}", 1) for s in range(slots)]
+        self.slot_item = [None] * slots
+        self.slot_readers = [0] * slots
+        self.kv_landed = False
+        self.tm = [[None] * 4 for _ in range(2)]   # per query half, per warp: ("S", s) / ("P", s)
+        self.acc_n = [0, 0]                         # accumulating MMAs done per half
+        self.s_n = 0
+        self.fifo = [[]]
+        self.landings = []
+
+    def producer(self):
+        if self.n == 0:
+            return
+        self.kv_full.expect_tx()
+        self.kv_full.arrive()
+        self.landings.append(("kv",))
+        for s in range(self.n):
+            slot = s % self.S
+            yield lambda sl=slot, k=s // self.S - 1: self.item_empty[sl].passes(k)
+            if self.slot_readers[slot]:
+                raise ProtocolError(f"item slot {slot} refilled while step {self.slot_item[slot]} is read")
+            self.slot_item[slot] = None
+            self.item_full[slot].expect_tx()
+            self.item_full[slot].arrive()
+            self.landings.append(("item", slot, s))
+
+    def issuer(self):
+        if self.n == 0:
+            return
+        yield lambda: self.kv_full.passes(0)
+        for s in range(self.n):
+            slot = s % self.S
+            yield lambda sl=slot, k=s // self.S: self.item_full[sl].passes(k)
+            self.slot_readers[slot] += 3             # S^T / dP^T, then dV / dK of each half
+            self.fifo[0] += [("s", s, slot), ("commit", self.s_full)]
+            for h in range(2):
+                yield lambda h=h, s=s: self.p_half[h].passes(s)
+                self.fifo[0].append(("acc", s, slot, h))
+            self.fifo[0].append(("commit", self.item_empty[slot]))
+        self.fifo[0].append(("commit", self.acc_done))
+
+    def elementwise(self, h, w):
+        for s in range(self.n):
+            yield lambda s=s: self.s_full.passes(s)
+            slot = s % self.S
+            if self.tm[h][w] != ("S", s) or self.slot_item[slot] != s:
+                raise ProtocolError(f"elementwise {h}.{w} step {s} found {self.tm[h][w]}, item "
+                                    f"{self.slot_item[slot]}")
+            self.slot_readers[slot] += 1             # lse, D of the item
+            yield None
+            self.slot_readers[slot] -= 1
+            self.tm[h][w] = ("P", s)
+            self.p_half[h].arrive()
+        if self.n:
+            yield lambda: self.acc_done.passes(0)
+            if self.acc_n != [self.n, self.n]:
+                raise ProtocolError("epilogue read dV / dK before the last accumulation")
+
+    def land(self, ev):
+        if ev[0] == "kv":
+            self.kv_landed = True
+            self.kv_full.land()
+        else:
+            self.slot_item[ev[1]] = ev[2]
+            self.item_full[ev[1]].land()
+
+    def execute(self, _):
+        op = self.fifo[0].pop(0)
+        if op[0] == "commit":
+            op[1].arrive()
+        elif op[0] == "s":
+            _, s, slot = op
+            if not self.kv_landed or self.slot_item[slot] != s:
+                raise ProtocolError(f"S^T {s} read item {self.slot_item[slot]}")
+            if s and (any(c != ("P", s - 1) for half in self.tm for c in half) or self.acc_n != [s, s]):
+                raise ProtocolError(f"S^T {s} overwrote {self.tm} before the accumulations read it")
+            self.tm = [[("S", s)] * 4 for _ in range(2)]
+            self.s_n += 1
+            self.slot_readers[slot] -= 1
+        else:
+            _, s, slot, h = op
+            if self.slot_item[slot] != s or any(c != ("P", s) for c in self.tm[h]) or self.acc_n[h] != s:
+                raise ProtocolError(f"dV / dK {s} half {h} read {self.tm[h]}, item {self.slot_item[slot]}")
+            self.acc_n[h] += 1
+            self.slot_readers[slot] -= 1
+
+    def agents(self):
+        return [self.producer(), self.issuer()] + [self.elementwise(h, w) for h in range(2)
+                                                   for w in range(4)]
+
+    def barriers(self):
+        return ([self.kv_full, self.s_full, self.acc_done] + self.p_half + self.item_full
+                + self.item_empty)
+
+    def finish(self):
+        if self.acc_n != [self.n, self.n]:
+            raise ProtocolError("not every accumulation ran")
+
+
+class KernelBwdDq(Model):
+    """bwd_dq_kernel, one CTA: one 128-row query tile, n key tiles.  Q and dO
+    are loaded once; K_j and V_j come through rings of their own (`ks`, `vs`
+    slots).  S_j = Q K_j^T goes to score buffer j mod 2 and dS_j over it, dP_j
+    to one dP buffer.  The issuer sends S_{j+1} at once, dP_{j+1} once dP_j has
+    been read (dp_free), commits s_full, then for each half of the keys waits
+    for that half of dS_j (p_half) and sends dQ += dS K_j; K_j is released after
+    dQ_j, V_j after dP_j.  Four elementwise warps (one query row per thread)
+    read S_j and dP_j per half, arrive on dp_free once all of dP_j is read,
+    write dS over the S columns they read and arrive on p_half.  `robust`
+    models p_half as one barrier per (half, step parity), which keeps every
+    wait within one phase whatever the warps' relative speeds."""
+
+    def __init__(self, n, seed, ks=3, vs=2, robust=False):
+        self.n, self.KS, self.VS, self.robust = n, ks, vs, robust
+        self.rnd = random.Random(seed)
+        self.q_full = Bar("q_full", 1)
+        self.s_full = Bar("s_full", 1)
+        self.dp_free = Bar("dp_free", 4)
+        self.acc_done = Bar("acc_done", 1)
+        self.p_half = [[Bar(f"p_half{h}_{q}", 4) for q in range(2)] for h in range(2)]
+        if not robust:
+            self.p_half = [[b[0], b[0]] for b in self.p_half]
+        self.k_full = [Bar(f"k_full{s}", 1) for s in range(ks)]
+        self.k_empty = [Bar(f"k_empty{s}", 1) for s in range(ks)]
+        self.v_full = [Bar(f"v_full{s}", 1) for s in range(vs)]
+        self.v_empty = [Bar(f"v_empty{s}", 1) for s in range(vs)]
+        self.k_item, self.v_item = [None] * ks, [None] * vs
+        self.k_readers, self.v_readers = [0] * ks, [0] * vs
+        self.q_landed = False
+        self.sbuf = [[None] * 4 for _ in range(2)]  # per buffer, per warp: ("S", j) / ("dS", j)
+        self.dp = [None] * 4                         # per warp: ("dP", j) or ("read", j)
+        self.dq_n = [0, 0]
+        self.fifo = [[]]
+        self.landings = []
+
+    def _p_wait(self, h, j):
+        if self.robust:
+            return lambda: self.p_half[h][j & 1].passes(j >> 1)
+        return lambda: self.p_half[h][0].passes(j)
+
+    def producer(self):
+        if self.n == 0:
+            return
+        self.q_full.expect_tx()
+        self.q_full.arrive()
+        self.landings.append(("q",))
+        for j in range(self.n):
+            ks, vs = j % self.KS, j % self.VS
+            yield lambda ks=ks, k=j // self.KS - 1: self.k_empty[ks].passes(k)
+            if self.k_readers[ks]:
+                raise ProtocolError(f"K slot {ks} refilled while K_{self.k_item[ks]} is read")
+            self.k_item[ks] = None
+            self.k_full[ks].expect_tx()
+            self.k_full[ks].arrive()
+            self.landings.append(("k", ks, j))
+            yield lambda vs=vs, k=j // self.VS - 1: self.v_empty[vs].passes(k)
+            if self.v_readers[vs]:
+                raise ProtocolError(f"V slot {vs} refilled while V_{self.v_item[vs]} is read")
+            self.v_item[vs] = None
+            self.v_full[vs].expect_tx()
+            self.v_full[vs].arrive()
+            self.landings.append(("v", vs, j))
+
+    def issuer(self):
+        n, KS, VS = self.n, self.KS, self.VS
+        if n == 0:
+            return
+        yield lambda: self.q_full.passes(0)
+        yield lambda: self.k_full[0].passes(0)
+        yield lambda: self.v_full[0].passes(0)
+        self.k_readers[0] += 1
+        self.v_readers[0] += 1
+        self.fifo[0] += [("s", 0), ("dp", 0), ("commit", self.s_full), ("commit", self.v_empty[0])]
+        for j in range(n):
+            if j + 1 < n:
+                yield lambda j=j: self.k_full[(j + 1) % KS].passes((j + 1) // KS)
+                self.k_readers[(j + 1) % KS] += 1
+                self.fifo[0].append(("s", j + 1))
+                yield lambda j=j: self.v_full[(j + 1) % VS].passes((j + 1) // VS)
+                yield lambda j=j: self.dp_free.passes(j)
+                self.v_readers[(j + 1) % VS] += 1
+                self.fifo[0] += [("dp", j + 1), ("commit", self.s_full),
+                                 ("commit", self.v_empty[(j + 1) % VS])]
+            self.k_readers[j % KS] += 1
+            for h in range(2):
+                yield self._p_wait(h, j)
+                self.fifo[0].append(("dq", j, h))
+            self.fifo[0].append(("commit", self.k_empty[j % KS]))
+        self.fifo[0].append(("commit", self.acc_done))
+
+    def elementwise(self, w):
+        for j in range(self.n):
+            b = j & 1
+            yield lambda j=j: self.s_full.passes(j)
+            for h in range(2):
+                if self.sbuf[b][w] not in (("S", j), ("dS0", j)) or self.dp[w] not in (("dP", j), ("read", j)):
+                    raise ProtocolError(f"elementwise {w} step {j} half {h} found {self.sbuf[b][w]}, "
+                                        f"{self.dp[w]}")
+                if h == 1:
+                    self.dp[w] = ("read", j)
+                    self.dp_free.arrive()
+                yield None
+                self.sbuf[b][w] = ("dS0", j) if h == 0 else ("dS", j)
+                [self.p_half[h][j & 1] if self.robust else self.p_half[h][0]][0].arrive()
+        if self.n:
+            yield lambda: self.acc_done.passes(0)
+            if self.dq_n != [self.n, self.n]:
+                raise ProtocolError("epilogue read dQ before the last accumulation")
+
+    def land(self, ev):
+        if ev[0] == "q":
+            self.q_landed = True
+            self.q_full.land()
+        elif ev[0] == "k":
+            self.k_item[ev[1]] = ev[2]
+            self.k_full[ev[1]].land()
+        else:
+            self.v_item[ev[1]] = ev[2]
+            self.v_full[ev[1]].land()
+
+    def execute(self, _):
+        op = self.fifo[0].pop(0)
+        if op[0] == "commit":
+            op[1].arrive()
+            return
+        kind, j = op[0], op[1]
+        b = j & 1
+        if kind == "s":
+            if not self.q_landed or self.k_item[j % self.KS] != j:
+                raise ProtocolError(f"S_{j} read K_{self.k_item[j % self.KS]}")
+            if j >= 2 and (any(c != ("dS", j - 2) for c in self.sbuf[b]) or self.dq_n != [j - 1, j - 1]):
+                raise ProtocolError(f"S_{j} overwrote buffer {b} holding {self.sbuf[b]}")
+            self.sbuf[b] = [("S", j)] * 4
+            self.k_readers[j % self.KS] -= 1
+        elif kind == "dp":
+            if self.v_item[j % self.VS] != j:
+                raise ProtocolError(f"dP_{j} read V_{self.v_item[j % self.VS]}")
+            if j and any(c != ("read", j - 1) for c in self.dp):
+                raise ProtocolError(f"dP_{j} overwrote dP still unread: {self.dp}")
+            self.dp = [("dP", j)] * 4
+            self.v_readers[j % self.VS] -= 1
+        else:
+            h = op[2]
+            want = ("dS0", j) if h == 0 else ("dS", j)
+            ok = all(c in (("dS0", j), ("dS", j)) for c in self.sbuf[b]) if h == 0 else \
+                all(c == ("dS", j) for c in self.sbuf[b])
+            if not ok or self.dq_n[h] != j or self.k_item[j % self.KS] != j:
+                raise ProtocolError(f"dQ_{j} half {h} read {self.sbuf[b]} (want {want})")
+            self.dq_n[h] += 1
+            if h == 1:
+                self.k_readers[j % self.KS] -= 1
+
+    def agents(self):
+        return [self.producer(), self.issuer()] + [self.elementwise(w) for w in range(4)]
+
+    def barriers(self):
+        ph = {id(b): b for row in self.p_half for b in row}.values()
+        return ([self.q_full, self.s_full, self.dp_free, self.acc_done] + list(ph)
+                + self.k_full + self.k_empty + self.v_full + self.v_empty)
+
+    def finish(self):
+        if self.dq_n != [self.n, self.n]:
+            raise ProtocolError("not every dQ accumulation ran")
