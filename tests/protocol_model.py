@@ -39,7 +39,9 @@ overwritten only after all four warps of the tile that owns it loaded it, an
 MMA reads the K or V tile it expects, P_t is overwritten only after the
 P_t V that reads it has executed, O_t is rescaled only between two P_t V, and
 a slot is refilled only after every MMA reading it has executed.  A run that
-stops with agents still waiting is a deadlock.
+stops with agents still waiting is a deadlock.  With `timeout_p` the forward
+model also takes the abort path: one blocked wait runs out at a random moment,
+and the CTA must not exit with a TMA load or an MMA in flight.
 """
 
 from __future__ import annotations
@@ -86,11 +88,32 @@ class Bar:
         return ok
 
 
+class Wait:
+    """A bounded wait an agent yields: resumed with True once the phase passes,
+    or with False when the CTA's abort flag is set (or this wait runs out)."""
+
+    def __init__(self, pred):
+        self.pred = pred
+
+
+class Drain:
+    """A drain-only wait of the abort path: ignores the abort flag."""
+
+    def __init__(self, pred):
+        self.pred = pred
+
+
 class Model:
     """Random scheduler shared by the kernel models: at each step it takes one
     of the runnable agents (a generator whose last yielded wait now passes, or
     that yielded None), a TMA load in flight, or the oldest pending operation of
-    one MMA issuer, uniformly at random."""
+    one MMA issuer, uniformly at random.  Agents may yield a bare predicate (a
+    wait that only ever passes), a Wait, a Drain or None.  With `timeout_p` > 0
+    a blocked Wait may run out at any step (once per run): it raises the abort
+    flag, and from then on every blocked Wait returns False."""
+
+    abort = False
+    timeout_p = 0.0
 
     def agents(self):
         raise NotImplementedError
@@ -98,13 +121,28 @@ class Model:
     def barriers(self):
         raise NotImplementedError
 
+    def _ready(self, w):
+        if w is None:
+            return True
+        if isinstance(w, Wait):
+            return self.abort or w.pred()
+        if isinstance(w, Drain):
+            return w.pred()
+        return w()
+
     def run(self, max_events=200000):
         agents = self.agents()
         waits = [None] * len(agents)
         alive = [True] * len(agents)
+        started = [False] * len(agents)
         for _ in range(max_events):
+            if self.timeout_p and not self.abort and self.rnd.random() < self.timeout_p:
+                blocked = [i for i in range(len(agents)) if alive[i] and isinstance(waits[i], Wait)
+                           and not waits[i].pred()]
+                if blocked:
+                    self.abort = True                    # this wait ran out
             choices = [("agent", i) for i, a in enumerate(agents)
-                       if alive[i] and (waits[i] is None or waits[i]())]
+                       if alive[i] and self._ready(waits[i])]
             choices += [("land", k) for k in range(len(self.landings))]
             choices += [("mma", t) for t in range(len(self.fifo)) if self.fifo[t]]
             if not choices:
@@ -118,12 +156,20 @@ class Model:
             elif kind == "mma":
                 self.execute(i)
             else:
+                w = waits[i]
+                value = (w.pred() if isinstance(w, Wait) else True) if w is not None else None
                 try:
-                    waits[i] = next(agents[i])
+                    waits[i] = agents[i].send(value) if started[i] else next(agents[i])
+                    started[i] = True
                 except StopIteration:
                     alive[i] = False
+                if not any(alive) and (self.landings or any(
+                        op[0] != "commit" for f in self.fifo for op in f)):
+                    raise ProtocolError("the CTA exits with a TMA load or an MMA in flight")
         else:
             raise ProtocolError("no end within the event budget")
+        if self.abort:
+            return
         for b in self.barriers():
             if b.pending != b.count or b.tx:
                 raise ProtocolError(f"{b.name} left with a partial phase")
@@ -137,8 +183,10 @@ class Kernel(Model):
 
     LAG = 3   # the producer widens its share of V_c after loading V_{c+LAG}
 
-    def __init__(self, n_kv, slots, seed, mutant=None, conv=False):
+    def __init__(self, n_kv, slots, seed, mutant=None, conv=False, timeout_p=0.0,
+                 drain_always=False):
         self.n_kv, self.S, self.mutant, self.conv = tuple(n_kv), slots, mutant, conv
+        self.timeout_p, self.drain_always = timeout_p, drain_always
         if mutant == "lag_half_ring":
             self.LAG = slots // 2
         elif conv and (slots % 2 or self.LAG >= slots // 2):
@@ -156,6 +204,7 @@ class Kernel(Model):
         self.kv_empty = [Bar(f"kv_empty{s}", 4 if conv and s % 2 else release) for s in range(slots)]
         self.v16_full = [Bar(f"v16_full{b}", 4) for b in range(2)]
         self.v16_empty = [Bar(f"v16_empty{b}", 2) for b in range(2)]
+        self.drain = [Bar(f"drain{t}", 1) for t in range(2)]
         self.v16_item = [None, None]         # V tile whose shares the fp16 buffer holds
         self.v16_shares = [set(), set()]
         self.pv_of_v = {}                    # V index -> P V executed that read it
@@ -172,19 +221,26 @@ class Kernel(Model):
         self.landings = []                   # TMA loads in flight: ("q", t) or ("kv", slot, item)
 
     # ------------------------------------------------------------ roles
+    # Each role follows the kernel's own code, abort path included: a Wait
+    # that returns False makes the role leave its loop; the producer then
+    # drains the loads it issued (Q and the last `slots` ring items), an issuer
+    # commits its drain barrier and waits for it, the other roles just stop.
     def producer(self):
         if self.n_max == 0:
             return
+        S = self.S
         nq = sum(1 for t in range(2) if self.n_kv[t] > 0)
         self.q_full.expect_tx(nq)
         self.q_full.arrive()
         for t in range(2):
             if self.n_kv[t] > 0:
                 self.landings.append(("q", t))
-        next_share = 0
-        for it in range(2 * self.n_max):
-            slot = it % self.S
-            yield lambda s=slot, n=it // self.S - 1: self.kv_empty[s].passes(n)
+        it, next_share, ok = 0, 0, True
+        while ok and it < 2 * self.n_max:
+            slot = it % S
+            ok = yield Wait(lambda s=slot, n=it // S - 1: self.kv_empty[s].passes(n))
+            if not ok:
+                break
             if self.slot_readers[slot]:
                 raise ProtocolError(f"slot {slot} refilled with item {it} while an MMA still "
                                     f"has to read item {self.slot_item[slot]}")
@@ -192,20 +248,27 @@ class Kernel(Model):
             self.kv_full[slot].expect_tx()
             self.kv_full[slot].arrive()
             self.landings.append(("kv", slot, it))
-            if self.conv and it % 2 and it // 2 >= self.LAG:
-                yield from self.widen_share(next_share, "producer")
+            cur, it = it, it + 1
+            if self.conv and cur % 2 and cur // 2 >= self.LAG:
+                ok = yield from self.widen_share(next_share, "producer")
                 next_share += 1
-        while self.conv and next_share < self.n_max:
-            yield from self.widen_share(next_share, "producer")
+        while self.conv and ok and next_share < self.n_max:
+            ok = yield from self.widen_share(next_share, "producer")
             next_share += 1
+        if not ok or self.drain_always:
+            yield Drain(lambda: self.q_full.passes(0))
+            for k in range(max(0, it - S), it):
+                yield Drain(lambda k=k: self.kv_full[k % S].passes(k // S))
 
     def widen_share(self, j, who):
         """One warp's share of V_j: e4m3 ring slot -> fp16 buffer j mod 2."""
         it, b = 2 * j + 1, j % 2
         slot = it % self.S
-        yield lambda: self.kv_full[slot].passes(it // self.S)
-        if self.mutant != "no_v16_empty_wait":
-            yield lambda: self.v16_empty[b].passes(j // 2 - 1)
+        ok = yield Wait(lambda: self.kv_full[slot].passes(it // self.S))
+        if ok and self.mutant != "no_v16_empty_wait":
+            ok = yield Wait(lambda: self.v16_empty[b].passes(j // 2 - 1))
+        if not ok:
+            return False
         if self.slot_item[slot] != it:
             raise ProtocolError(f"{who} widened slot {slot} holding {self.slot_item[slot]} as V_{j}")
         if j >= 2 and self.pv_of_v.get(j - 2, 0) != sum(n > j - 2 for n in self.n_kv):
@@ -218,10 +281,12 @@ class Kernel(Model):
         self.v16_shares[b].add(who)
         self.v16_full[b].arrive()
         self.kv_empty[slot].arrive()
+        return True
 
     def converter(self):
         for j in range(self.n_max if self.conv else 0):
-            yield from self.widen_share(j, "converter")
+            if not (yield from self.widen_share(j, "converter")):
+                break
 
     def issuer(self, t):
         nt, nt_o = self.n_kv[t], self.n_kv[1 - t]
@@ -230,7 +295,7 @@ class Kernel(Model):
         S = self.S
 
         def wait_full(it):
-            return lambda: self.kv_full[it % S].passes(it // S)
+            return Wait(lambda: self.kv_full[it % S].passes(it // S))
 
         def s_ready(j):
             # the score MMA before tile t's j-th in the order A_0 B_0 A_1 B_1 ...
@@ -243,75 +308,86 @@ class Kernel(Model):
             if prev is None or self.mutant == "no_s_free_wait":
                 return None
             pt, pj = prev
-            return lambda: self.s_free[pt].passes(pj)
+            return Wait(lambda: self.s_free[pt].passes(pj))
 
         def issue(op, slot):
             self.slot_readers[slot] += 1
             self.fifo[t].append(op)
 
-        yield lambda: self.q_full.passes(0)
-        if nt > 0:
-            yield wait_full(0)
+        def qk(j, itK):
+            issue(("qk", t, j, itK % S), itK % S)
+            self.fifo[t] += [("commit", self.s_full[t]), ("commit", self.kv_empty[itK % S])]
+
+        ok = yield Wait(lambda: self.q_full.passes(0))
+        if ok and nt > 0:
+            ok = yield wait_full(0)
             w = s_ready(0)
-            if w:
-                yield w
-            issue(("qk", t, 0, 0 % S), 0 % S)
-            self.fifo[t] += [("commit", self.s_full[t]), ("commit", self.kv_empty[0 % S])]
-        if self.conv:
-            yield from self.issuer_conv(t, wait_full, s_ready, issue)
-            return
-        for j in range(nt):
+            if ok and w:
+                ok = yield w
+            if ok:
+                qk(0, 0)
+        if ok and self.conv:
+            ok = yield from self.widen_share(0, f"issuer{t}")
+        j = 0
+        while ok and j < nt:
             itK, itV = 2 * j + 2, 2 * j + 1
             if j + 1 < nt:
-                yield wait_full(itK)
+                ok = yield wait_full(itK)
                 w = s_ready(j + 1)
-                if w:
-                    yield w
-                issue(("qk", t, j + 1, itK % S), itK % S)
-                self.fifo[t] += [("commit", self.s_full[t]), ("commit", self.kv_empty[itK % S])]
-            yield wait_full(itV)
-            yield lambda j=j: self.p_full[t].passes(j)
-            issue(("pv", t, j, itV % S), itV % S)
-            self.fifo[t] += [("commit", self.pv_done[t]), ("commit", self.kv_empty[itV % S])]
-        for j in range(nt, self.n_max):
-            # key tiles this tile never reads: release the slots once filled
-            for it in (2 * j, 2 * j + 1):
-                yield wait_full(it)
-                self.kv_empty[it % S].arrive()
-
-    def issuer_conv(self, t, wait_full, s_ready, issue):
-        nt, S = self.n_kv[t], self.S
-        who = f"issuer{t}"
-        yield from self.widen_share(0, who)
-        for j in range(nt):
-            itK = 2 * j + 2
-            if j + 1 < nt:
-                yield wait_full(itK)
-                w = s_ready(j + 1)
-                if w:
-                    yield w
-                issue(("qk", t, j + 1, itK % S), itK % S)
-                self.fifo[t] += [("commit", self.s_full[t]), ("commit", self.kv_empty[itK % S])]
-            yield lambda j=j: self.v16_full[j % 2].passes(j // 2)
-            yield lambda j=j: self.p_full[t].passes(j)
-            self.fifo[t] += [("pv16", t, j, j % 2), ("commit", self.pv_done[t]),
-                             ("commit", self.v16_empty[j % 2])]
-            if j + 1 < self.n_max:
-                yield from self.widen_share(j + 1, who)
-        for j in range(nt, self.n_max):
-            yield wait_full(2 * j)
-            self.kv_empty[(2 * j) % S].arrive()
-            yield lambda j=j: self.v16_full[j % 2].passes(j // 2)
-            self.v16_empty[j % 2].arrive()
-            if j + 1 < self.n_max:
-                yield from self.widen_share(j + 1, who)
+                if ok and w:
+                    ok = yield w
+                if not ok:
+                    break
+                qk(j + 1, itK)
+            if self.conv:
+                ok = yield Wait(lambda j=j: self.v16_full[j % 2].passes(j // 2))
+            else:
+                ok = yield wait_full(itV)
+            if ok:
+                ok = yield Wait(lambda j=j: self.p_full[t].passes(j))
+            if not ok:
+                break
+            if self.conv:
+                self.fifo[t] += [("pv16", t, j, j % 2), ("commit", self.pv_done[t]),
+                                 ("commit", self.v16_empty[j % 2])]
+                if j + 1 < self.n_max:
+                    ok = yield from self.widen_share(j + 1, f"issuer{t}")
+            else:
+                issue(("pv", t, j, itV % S), itV % S)
+                self.fifo[t] += [("commit", self.pv_done[t]), ("commit", self.kv_empty[itV % S])]
+            j += 1
+        j = nt
+        while ok and j < self.n_max:
+            # key tiles this tile never reads: release them once filled
+            ok = yield wait_full(2 * j)
+            if ok:
+                self.kv_empty[(2 * j) % S].arrive()
+            if self.conv:
+                if ok:
+                    ok = yield Wait(lambda j=j: self.v16_full[j % 2].passes(j // 2))
+                if ok:
+                    self.v16_empty[j % 2].arrive()
+                if ok and j + 1 < self.n_max:
+                    ok = yield from self.widen_share(j + 1, f"issuer{t}")
+            else:
+                if ok:
+                    ok = yield wait_full(2 * j + 1)
+                if ok:
+                    self.kv_empty[(2 * j + 1) % S].arrive()
+            j += 1
+        if not ok or self.drain_always:
+            # none of this issuer's MMAs may still run when TMEM is freed
+            self.fifo[t].append(("commit", self.drain[t]))
+            yield Drain(lambda: self.drain[t].passes(0))
 
     def softmax(self, t, w):
         nt = self.n_kv[t]
-        s_pre = False
+        s_pre, ok = False, True
         for j in range(nt):
             if not s_pre:
-                yield lambda j=j: self.s_full[t].passes(j)
+                ok = yield Wait(lambda j=j: self.s_full[t].passes(j))
+                if not ok:
+                    break
             if self.S_owner != (t, j):
                 raise ProtocolError(f"softmax {t}.{w} step {j} found the scores of {self.S_owner}")
             self.S_loaded.add(w)
@@ -319,7 +395,9 @@ class Kernel(Model):
             pv_pre = j > 0 and self.pv_done[t].passes(j - 1)
             yield None                                   # exponentials
             if j > 0 and not pv_pre and self.mutant != "no_pv_wait":
-                yield lambda j=j: self.pv_done[t].passes(j - 1)
+                ok = yield Wait(lambda j=j: self.pv_done[t].passes(j - 1))
+                if not ok:
+                    break
             if self.pv_done_n[t] < j:
                 raise ProtocolError(f"softmax {t}.{w} overwrote P of step {j - 1} before its P V ran")
             self.P[t][w] = j
@@ -328,9 +406,9 @@ class Kernel(Model):
                 raise ProtocolError(f"softmax {t}.{w} rescaled O while P V {self.pv_done_n[t]} ran")
             yield None
             self.p_full[t].arrive()
-        if nt > 0:
-            yield lambda: self.pv_done[t].passes(nt - 1)
-            if self.pv_done_n[t] != nt or self.qk_done_n[t] != nt:
+        if ok and nt > 0:
+            ok = yield Wait(lambda: self.pv_done[t].passes(nt - 1))
+            if ok and (self.pv_done_n[t] != nt or self.qk_done_n[t] != nt):
                 raise ProtocolError(f"epilogue of tile {t} ran before its MMAs completed")
 
     # ------------------------------------------------------- async events

@@ -20,6 +20,14 @@ barriers kept one per step parity (the model shows that with one barrier per
 half, as the kernel has them now, a warp lagging a whole half step behind the
 others lets a faster warp's next-step arrival complete the phase: a parity
 wait two phases behind, or dQ reading a dS half not yet written).
+
+The abort path of the d <= 128 kernel is modelled too: at a random moment one
+blocked wait runs out, every role leaves as the kernel's code does, and when
+all roles are done (the CTA's exit) no TMA load and no MMA may still be in
+flight.  That holds when the producer and the issuers drain at the end of
+their roles whatever happened; as built they drain only when their own wait
+failed, so a role that had already finished leaves its last loads or MMAs
+undrained (tracked as an open item, like the dS barriers above).
 """
 
 import pytest
@@ -108,4 +116,31 @@ def test_bwd_dq_with_one_dS_barrier_per_half_needs_bounded_warp_skew():
             KernelBwdDq(9, seed, robust=False).run()
         except ProtocolError:
             failures += 1
+    assert failures > 0
+
+
+ABORT_N_KV = [(1, 1), (2, 2), (5, 5), (9, 9), (1, 2), (3, 4), (7, 8), (0, 1), (2, 0), (2, 3)]
+
+
+@pytest.mark.parametrize("conv,slots", [(False, 5), (False, 6), (False, 8), (True, 8)],
+                         ids=["16bit-5", "16bit-6", "16bit-8", "onchip-8"])
+def test_abort_path_with_drains_at_every_role_end_leaves_nothing_in_flight(conv, slots):
+    aborted = 0
+    for n_kv in ABORT_N_KV:
+        for seed in range(40):
+            k = Kernel(n_kv, slots, seed, conv=conv, timeout_p=0.02, drain_always=True)
+            k.run()
+            aborted += k.abort
+    assert aborted > 200        # most runs took the abort path somewhere
+
+
+def test_abort_path_as_built_can_leave_work_in_flight():
+    # a role that finished its loop before another role's wait ran out does not drain
+    failures = 0
+    for n_kv in ABORT_N_KV:
+        for seed in range(40):
+            try:
+                Kernel(n_kv, 5, seed, timeout_p=0.02).run()
+            except ProtocolError:
+                failures += 1
     assert failures > 0
